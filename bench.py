@@ -1,0 +1,422 @@
+"""Benchmark of the shard-local step (one JSON line on stdout from rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload KEY]
+                    [--impl ours|reference]
+
+One step = one rank's fused shard-local step over its whole shard: the N
+incoming bf16 gradient slices summed in fp32 and scaled by 1/N, AdamW on the
+fp32 master/m/v shard, the bf16 cast written into the rank's slot of the
+AllGather buffer. Inputs are synthetic (seeded generator), shaped like the
+named model's parameter list, and resident in HBM before the timed region;
+each step's working set (tens of GB) is far larger than L2, so no flush is
+needed between steps.
+
+With --gpus N > 1 (torchrun, one process per GPU) GPU i runs emulated rank
+i mod N_ranks of the same workload: per-GPU work is fixed (weak scaling) and
+no collective touches the data path; the timed region is bracketed by a
+barrier and a synchronize, and the slowest rank's time is reported.
+
+--impl reference times the CPU oracle (single thread) on a bounded sample of
+the same workload, on the host's cores, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "shard-step elements/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "elements/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCE = os.path.join(ROOT, "fsdp_sharded_mixed_gb300", "csrc", "shard_step.cu")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "shard_step_traffic.txt")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------- host helpers ----
+def dist_env():
+    """(rank, world_size, local_rank) from torchrun's environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def emulated_rank(global_rank, n_ranks):
+    """The data-parallel rank whose shard step GPU `global_rank` runs."""
+    return global_rank % n_ranks
+
+
+def max_over_ranks(value, device=None):
+    """Max of a float over all processes (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value, device=None):
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def kernel_sha():
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def committed_traffic(workload_key):
+    """ncu DRAM bytes per shard element for the current kernel source, from the
+    committed profile summary, or None when absent or taken on other code."""
+    try:
+        text = open(TRAFFIC_SUMMARY, encoding="utf-8").read()
+    except OSError:
+        return None
+    sha = kernel_sha()
+    for line in text.splitlines():
+        m = re.match(r"\s*traffic\s+(\S+)\s+kernel_sha=(\w+)\s+bytes_per_elem=([\d.]+)", line)
+        if m and m.group(1) == workload_key and m.group(2) == sha:
+            return float(m.group(3))
+    return None
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return float(peaks["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, uuid=None):
+        self.cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS),
+                    "--format=csv,noheader,nounits", "-lms", "100"]
+        if uuid:
+            self.cmd += ["-i", uuid]
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            cols = [c.strip() for c in line.split(",")]
+            if len(cols) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(cols[1]))
+                smax.append(float(cols[2]))
+                power.append(float(cols[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, cols[4:]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ CPU oracle ----
+def oracle_sample_rate(w, plan_S, P, rank, n_elems, steps, warmup=0):
+    """Time the single-threaded oracle on the first n_elems of rank's shard.
+    Returns (elements/s, seconds, cores used)."""
+    import numpy as np
+
+    import oracle
+    import synth
+    o = oracle.default()
+    N = w.world
+    n = max(8, min(plan_S, n_elems))
+    kw = dict(seed=w.seed, sigma=w.grad_sigma, p_limit=P, outlier_frac=w.outlier_frac,
+              outlier_scale=w.outlier_scale, bf16=True)
+    grads = [synth.fill(n, index0=rank * plan_S, rank=j, step=1, **kw) for j in range(N)]
+    master = synth.fill(n, index0=rank * plan_S, seed=w.seed, stream=synth.STREAM_MASTER,
+                        sigma=w.master_sigma, p_limit=P)
+    m, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
+    full = np.zeros(n * N, np.uint16)
+    hp = w.hparams
+    old_aff = None
+    if hasattr(os, "sched_setaffinity"):
+        old_aff = os.sched_getaffinity(0)
+        os.sched_setaffinity(0, {min(old_aff)})
+    try:
+        total = 0.0
+        for t in range(1, warmup + steps + 1):
+            t0 = time.perf_counter()
+            o.shard_step(world=N, rank=0, S=n, lo=0, hi=n, grads=grads, master=master, m=m,
+                         v=v, full_flat=full, lr=hp["lr"], beta1=hp["beta1"],
+                         beta2=hp["beta2"], eps=hp["eps"], wd=hp["weight_decay"], t=t)
+            if t > warmup:
+                total += time.perf_counter() - t0
+    finally:
+        if old_aff is not None:
+            os.sched_setaffinity(0, old_aff)
+    return n * steps / total, total, 1, n
+
+
+# ------------------------------------------------------------------ main ----
+def bytes_per_elem(world, grad_bytes=2, param_bytes=2):
+    return grad_bytes * world + 24 + param_bytes
+
+
+def run_reference(args, w):
+    """The reference arm: the CPU oracle, as it stands, one thread."""
+    rank, world_size, _ = dist_env()
+    if rank != 0:
+        return
+    import fsdp_sharded_mixed_gb300 as zs
+    plan = zs.zs_flatten_plan(w.numels, w.tied_to, world=w.world, align_elems=w.align)
+    budget_s, est_rate = 60.0, 20e6
+    sample = int(budget_s * est_rate / max(1, args.steps + args.warmup))
+    sample = max(4096, min(plan.S, sample)) // 8 * 8
+    r = emulated_rank(0, w.world)
+    rate, secs, cores, n = oracle_sample_rate(w, plan.S, plan.P, r, sample, args.steps,
+                                              warmup=args.warmup)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps * plan.S / n,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(w, plan),
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"first {n:,} elements of rank {r}'s shard per step "
+                                   f"(of {plan.S:,}); ms_per_step scaled to the full shard"},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    plan.free()
+
+
+def workload_config(w, plan):
+    return {"workload": f"{w.key}: {w.title}", "emulated_ranks": w.world,
+            "shard_elems": plan.S, "flat_params": plan.P, "flat_padded": plan.P_pad,
+            "grad_dtype": "bf16", "param_dtype": "bf16", "state_dtype": "fp32",
+            "bytes_per_elem": bytes_per_elem(w.world),
+            "l2": "no flush: each step streams >> 129 MB L2 (inputs larger than L2)"}
+
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import fsdp_sharded_mixed_gb300 as zs
+    import synth
+
+    grank, gworld, local = dist_env()
+    if gworld > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+
+    plan = zs.zs_flatten_plan(w.numels, w.tied_to, world=w.world, align_elems=w.align)
+    N, S, P = plan.world, plan.S, plan.P
+    r = emulated_rank(grank, N)
+    hp = w.hparams
+    bpe = bytes_per_elem(N)
+
+    # Inputs resident in HBM: one set of incoming slices, master from the
+    # generator, zero moments, the full AllGather buffer.
+    grads = [torch.empty(S, dtype=torch.int16, device=dev) for _ in range(N)]
+    for j, g in enumerate(grads):
+        synth.fill_device(g.data_ptr(), S, index0=r * S, seed=w.seed, rank=j, step=1,
+                          sigma=w.grad_sigma, p_limit=P, outlier_frac=w.outlier_frac,
+                          outlier_scale=w.outlier_scale, bf16=True, cuda_stream=sptr)
+    master = torch.empty(S, dtype=torch.float32, device=dev)
+    synth.fill_device(master.data_ptr(), S, index0=r * S, seed=w.seed,
+                      stream=synth.STREAM_MASTER, sigma=w.master_sigma, p_limit=P,
+                      bf16=False, cuda_stream=sptr)
+    m = torch.zeros(S, dtype=torch.float32, device=dev)
+    v = torch.zeros(S, dtype=torch.float32, device=dev)
+    full = torch.zeros(plan.P_pad, dtype=torch.int16, device=dev)
+    torch.cuda.synchronize()
+
+    step_no = [0]
+
+    def step():
+        step_no[0] += 1
+        zs.zs_shard_step(plan, r, 0, S, grads, zs.ZS_BF16, master, m, v, full, zs.ZS_BF16, hp,
+                         step_no[0], stream=sptr)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    t_end = time.time() + 0.4  # keep the GPU busy while nvidia-smi starts
+    while time.time() < t_end:
+        step()
+        torch.cuda.synchronize()
+
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    if gworld > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        events[k][0].record(stream)
+        step()
+        events[k][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if gworld > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed = t0.elapsed_time(t1) / 1e3
+    per_step = sorted(a.elapsed_time(b) for a, b in events)
+    launch_avg_s = sum(per_step) / len(per_step) / 1e3
+    t_max = max_over_ranks(elapsed, dev)
+    elems_all = sum_over_ranks(float(S) * args.steps, dev)
+    value = elems_all / t_max
+
+    # End to end through the C ABI from pinned host memory: every step copies
+    # the N incoming slices host->device and reads the updated slot back.
+    e2e = None
+    if not args.no_e2e:
+        h_grads = [torch.empty(S, dtype=torch.int16, pin_memory=True) for _ in range(N)]
+        for hg, g in zip(h_grads, grads):
+            hg.copy_(g)
+        h_out = torch.empty(S, dtype=torch.int16, pin_memory=True)
+        slot = full.narrow(0, r * S, S)
+
+        def e2e_step():
+            for hg, g in zip(h_grads, grads):
+                g.copy_(hg, non_blocking=True)
+            step()
+            h_out.copy_(slot, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if gworld > 1:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_t = max_over_ranks(a.elapsed_time(b) / 1e3, dev)
+        e2e_elems = sum_over_ranks(float(S) * args.e2e_steps, dev)
+        e2e = {"value": e2e_elems / e2e_t, "unit": UNIT, "h2d_bytes_per_step": 2 * N * S,
+               "d2h_bytes_per_step": 2 * S, "steps": args.e2e_steps,
+               "ms_per_step": 1e3 * e2e_t / args.e2e_steps}
+        del h_grads, h_out
+
+    if grank == 0:
+        peak, peak_kind = measured_peak()
+        achieved = bpe * S / launch_avg_s / 1e9
+        traffic_pe = committed_traffic(w.key)
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "peak_source": peak_kind,
+                    "traffic": None if traffic_pe is None else traffic_pe * S,
+                    "algorithmic_bytes": bpe * S, "kernel": "shard_step_kernel",
+                    "kernel_sha": kernel_sha()}
+        cpu = None
+        if not args.no_cpu_baseline and gworld == 1:
+            rate, secs, cores, n = oracle_sample_rate(w, S, P, r, args.cpu_sample_elems,
+                                                      args.cpu_steps)
+            cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                   "sample": f"first {n:,} elements of rank {r}'s shard x {args.cpu_steps} "
+                             f"steps ({secs:.1f} s, 1 pinned thread)"}
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": gworld,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": dict(workload_config(w, plan),
+                                                parallelism=f"replicas{gworld}",
+                                                emulated_rank_gpu0=r),
+            "hbm_gbs": bpe * value / gworld / 1e9,
+            "step_ms": {"median": statistics.median(per_step),
+                        "p10": per_step[len(per_step) // 10],
+                        "p90": per_step[(9 * len(per_step)) // 10]},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    del grads, master, m, v, full
+    plan.free()
+    if gworld > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llama-7b")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-elems", type=int, default=32 * 1024 * 1024)
+    ap.add_argument("--cpu-steps", type=int, default=8)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from synth.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,265 @@
+"""GB300-native shard-local step for ZeRO-1/2/3 and FSDP.
+
+A thin ctypes binding over ``libzs.so`` (the C ABI in ``include/zs.h``): the
+functions here carry the C names and only marshal arguments — tensor data
+pointers, sizes, the CUDA stream handle — to the library, whose CUDA kernels
+do every step of the path. PyTorch supplies device memory and streams. There
+is no fallback: without the compiled library every call raises.
+
+Entry points: ``zs_flatten_plan`` (flat layout, rank shards, buckets),
+``zs_shard_step`` (N-slice fp32 mean + AdamW + cast into the AllGather slot),
+``zs_gather_assemble`` (the AllGather's result and per-tensor views).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+CSRC = os.path.join(_HERE, "csrc")
+BUILD_DIR = os.path.join(_HERE, "_build")
+LIB_PATH = os.path.join(_HERE, "libzs.so")
+INCLUDE = os.path.join(_ROOT, "include")
+
+ZS_OK, ZS_ERR_INVAL, ZS_ERR_ALIGN, ZS_ERR_RANGE = 0, -1, -2, -3
+ZS_ERR_CUDA, ZS_ERR_NOMEM, ZS_ERR_TIMEOUT, ZS_ERR_UNSUPPORTED = -4, -5, -6, -7
+ZS_BF16, ZS_FP32, ZS_FP24 = 0, 1, 2
+ELEM_BYTES = {ZS_BF16: 2, ZS_FP32: 4, ZS_FP24: 3}
+ZS_MAX_WORLD = 1024
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-fmad=false", "-prec-div=true",
+              "-prec-sqrt=true", "-ftz=false", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
+CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-I/usr/local/cuda/include"]
+CUDA_SOURCES = ["shard_step.cu", "gather.cu"]
+HOST_SOURCES = ["api.cpp", "plan.cpp"]
+
+
+# ----------------------------------------------------------------- build ----
+def _compile_jobs():
+    jobs = []
+    for src in CUDA_SOURCES:
+        obj = os.path.join(BUILD_DIR, src + ".o")
+        jobs.append((["nvcc", "-c", *NVCC_FLAGS, os.path.join(CSRC, src), "-o", obj], obj))
+    for src in HOST_SOURCES:
+        obj = os.path.join(BUILD_DIR, src + ".o")
+        jobs.append((["g++", "-c", *CXX_FLAGS, os.path.join(CSRC, src), "-o", obj], obj))
+    return jobs
+
+
+def build(log=True):
+    """Compile the library for sm_103a in-tree (sources in parallel) and link."""
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    jobs = _compile_jobs()
+
+    def run(job):
+        cmd, _ = job
+        p = subprocess.run(cmd, capture_output=True, text=True)
+        return cmd, p.returncode, p.stdout + p.stderr
+
+    with ThreadPoolExecutor(len(jobs)) as ex:
+        results = list(ex.map(run, jobs))
+    report = []
+    for cmd, rc, out in results:
+        report.append("$ " + " ".join(cmd) + "\n" + out)
+        if rc != 0:
+            raise RuntimeError("libzs build failed:\n" + out)
+    link = ["nvcc", "-shared", *ARCH, "-o", LIB_PATH + ".tmp", *[o for _, o in jobs]]
+    p = subprocess.run(link, capture_output=True, text=True)
+    if p.returncode != 0:
+        raise RuntimeError("libzs link failed:\n" + p.stdout + p.stderr)
+    os.replace(LIB_PATH + ".tmp", LIB_PATH)
+    if log:
+        with open(os.path.join(BUILD_DIR, "build.log"), "w") as f:
+            f.write("\n".join(report))
+
+
+# ------------------------------------------------------------------- ABI ----
+class ZsError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+_lib = None
+_I32, _I64, _P = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+
+
+class AdamWHparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double),
+                ("beta2", ctypes.c_double), ("eps", ctypes.c_double),
+                ("weight_decay", ctypes.c_double)]
+
+
+EXPORTS = {
+    "zs_flatten_plan": ([_P, _P, _I32, _I32, _I64, _I64, _P], ctypes.c_int),
+    "zs_plan_info": ([_P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "zs_plan_offsets": ([_P, _P, _I32], ctypes.c_int),
+    "zs_plan_bucket_range": ([_P, _I32, _P, _P], ctypes.c_int),
+    "zs_plan_bucket": ([_P, _I32, _I32, _P, _P], ctypes.c_int),
+    "zs_plan_free": ([_P], ctypes.c_int),
+    "zs_shard_step": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _P, _P, _P, ctypes.c_int,
+                       ctypes.POINTER(AdamWHparams), _I64, _P], ctypes.c_int),
+    "zs_gather_assemble": ([_P, _I32, _P, _P, ctypes.c_int, _P, _P], ctypes.c_int),
+    "zs_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "zs_last_error": ([], ctypes.c_char_p),
+    "zs_check_device_error": ([_P], ctypes.c_int),
+    "zs_set_validation": ([_I32], _I32),
+    "zs_version": ([], ctypes.c_char_p),
+}
+
+
+def lib():
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: the CUDA library must be built "
+                               "(__graft_entry__.build()); there is no fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in EXPORTS.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(status):
+    if status != ZS_OK:
+        L = lib()
+        detail = L.zs_last_error().decode() or L.zs_status_string(status).decode()
+        raise ZsError(status, detail)
+
+
+def _ptr(x):
+    """Device address of a tensor (or an int address / None)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class Plan:
+    """Owns a ``zs_plan*``; freed when garbage-collected or by ``free()``."""
+
+    def __init__(self, handle, n_params):
+        self.handle = handle
+        self.n_params = n_params
+        info = zs_plan_info(self)
+        self.P, self.P_pad, self.S = info["P"], info["P_pad"], info["S"]
+        self.n_buckets, self.world = info["n_buckets"], info["world"]
+
+    def free(self):
+        if self.handle:
+            h, self.handle = self.handle, None
+            _check(lib().zs_plan_free(h))
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def zs_flatten_plan(numels, tied_to=None, world=1, align_elems=128, bucket_elems=0):
+    n = len(numels)
+    arr = (ctypes.c_int64 * max(n, 1))(*numels)
+    ties = None if tied_to is None else (ctypes.c_int32 * max(n, 1))(*tied_to)
+    out = ctypes.c_void_p()
+    _check(lib().zs_flatten_plan(arr, ties, n, world, align_elems, bucket_elems,
+                                 ctypes.byref(out)))
+    return Plan(out.value, n)
+
+
+def zs_plan_info(plan):
+    P, P_pad, S = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    nb, w, npar = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().zs_plan_info(plan.handle, ctypes.byref(P), ctypes.byref(P_pad),
+                              ctypes.byref(S), ctypes.byref(nb), ctypes.byref(w),
+                              ctypes.byref(npar)))
+    return dict(P=P.value, P_pad=P_pad.value, S=S.value, n_buckets=nb.value, world=w.value,
+                n_params=npar.value)
+
+
+def zs_plan_offsets(plan):
+    out = (ctypes.c_int64 * max(plan.n_params, 1))()
+    _check(lib().zs_plan_offsets(plan.handle, out, plan.n_params))
+    return list(out)[:plan.n_params]
+
+
+def zs_plan_bucket_range(plan, bucket):
+    lo, hi = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().zs_plan_bucket_range(plan.handle, bucket, ctypes.byref(lo), ctypes.byref(hi)))
+    return lo.value, hi.value
+
+
+def zs_plan_bucket(plan, bucket, rank):
+    lo, hi = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().zs_plan_bucket(plan.handle, bucket, rank, ctypes.byref(lo), ctypes.byref(hi)))
+    return lo.value, hi.value
+
+
+def zs_shard_step(plan, rank, lo, hi, grad_slices, grad_dtype, master, exp_avg, exp_avg_sq,
+                  full_flat, param_dtype, hp, step, stream=None):
+    """Enqueue rank ``rank``'s fused step over shard-local ``[lo, hi)``.
+
+    ``grad_slices``: N device tensors (or addresses); ``master``/``exp_avg``/
+    ``exp_avg_sq``: fp32 [S]; ``full_flat``: N*S elements of ``param_dtype``;
+    ``hp``: dict with lr, beta1, beta2, eps, weight_decay; ``step`` >= 1.
+    """
+    ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
+    h = AdamWHparams(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"])
+    _check(lib().zs_shard_step(plan.handle, rank, lo, hi, ptrs, grad_dtype, _ptr(master),
+                               _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(full_flat), param_dtype,
+                               ctypes.byref(h), step, _stream(stream)))
+
+
+def zs_gather_assemble(plan, rank, shard_srcs, full_flat, param_dtype, stream=None):
+    """Enqueue the assembly of the other ranks' shards into ``full_flat``;
+    return the per-parameter device addresses (the unflattened views)."""
+    srcs = (ctypes.c_void_p * max(len(shard_srcs), 1))(*[_ptr(s) for s in shard_srcs])
+    views = (ctypes.c_void_p * max(plan.n_params, 1))()
+    _check(lib().zs_gather_assemble(plan.handle, rank, srcs, _ptr(full_flat), param_dtype,
+                                    views, _stream(stream)))
+    return [v or 0 for v in list(views)[:plan.n_params]]
+
+
+def zs_check_device_error(stream=None):
+    _check(lib().zs_check_device_error(_stream(stream)))
+
+
+def zs_set_validation(level):
+    return lib().zs_set_validation(level)
+
+
+def zs_version():
+    return lib().zs_version().decode()
+
+
+def tensor_views(full_flat, addresses, shapes):
+    """Wrap the addresses ``zs_gather_assemble`` returned as views of the
+    ``full_flat`` tensor with the given shapes (no copy)."""
+    base = full_flat.data_ptr()
+    es = full_flat.element_size()
+    out = []
+    for addr, shape in zip(addresses, shapes):
+        off = (addr - base) // es
+        n = 1
+        for d in shape:
+            n *= d
+        out.append(full_flat.narrow(0, off, n).view(shape))
+    return out

@@ -1,0 +1,291 @@
+// api.cpp — the C ABI: argument validation, the per-step fp32 scalars, and
+// dispatch to the kernels. Every check that can fail runs before any kernel is
+// enqueued, so a bad call returns a status and leaves the GPU untouched.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "zs_internal.h"
+
+namespace {
+
+thread_local char g_err[512];
+int32_t g_validation = 1;
+
+typedef CUresult (*PFN_addressRange)(CUdeviceptr*, size_t*, CUdeviceptr);
+
+PFN_addressRange address_range_fn() {
+  static PFN_addressRange fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return (PFN_addressRange) nullptr;
+    }
+    return (PFN_addressRange)p;
+  }();
+  return fn;
+}
+
+struct Range {
+  uintptr_t lo, hi;
+  const char* name;
+  int index;
+  bool output;
+};
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Device-resident, on the current device, and (where the driver can tell)
+// [p, p+bytes) inside one allocation.
+zs_status check_device_buffer(const void* p, int64_t bytes, const char* fn, const char* name,
+                              int index) {
+  if (g_validation < 1 || bytes == 0) return ZS_OK;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return zs::fail(ZS_ERR_INVAL, "%s: %s[%d] is not a CUDA pointer", fn, name, index);
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return zs::fail(ZS_ERR_INVAL, "%s: %s[%d] is not device memory", fn, name, index);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return zs::fail(ZS_ERR_CUDA, "%s: cudaGetDevice failed", fn);
+  }
+  if (attr.type == cudaMemoryTypeDevice && attr.device != dev)
+    return zs::fail(ZS_ERR_INVAL, "%s: %s[%d] lives on device %d, current device is %d", fn,
+                    name, index, attr.device, dev);
+  if (PFN_addressRange range = address_range_fn()) {
+    CUdeviceptr base = 0;
+    size_t size = 0;
+    if (range(&base, &size, (CUdeviceptr)(uintptr_t)p) == CUDA_SUCCESS) {
+      if ((uintptr_t)p + (uint64_t)bytes > (uintptr_t)base + size)
+        return zs::fail(ZS_ERR_RANGE,
+                        "%s: %s[%d] needs %lld bytes but its allocation ends %lld bytes after it",
+                        fn, name, index, (long long)bytes,
+                        (long long)((uintptr_t)base + size - (uintptr_t)p));
+    }
+  }
+  return ZS_OK;
+}
+
+zs_status check_overlaps(const std::vector<Range>& rs, const char* fn) {
+  for (size_t a = 0; a < rs.size(); ++a) {
+    if (!rs[a].output || rs[a].lo == rs[a].hi) continue;
+    for (size_t b = 0; b < rs.size(); ++b) {
+      if (a == b || rs[b].lo == rs[b].hi) continue;
+      if (rs[a].lo < rs[b].hi && rs[b].lo < rs[a].hi)
+        return zs::fail(ZS_ERR_INVAL, "%s: %s[%d] overlaps %s[%d]", fn, rs[a].name,
+                        rs[a].index, rs[b].name, rs[b].index);
+    }
+  }
+  return ZS_OK;
+}
+
+// beta^t by right-to-left binary powering in IEEE double.
+double pow_binary(double base, int64_t e) {
+  double r = 1.0;
+  while (e > 0) {
+    if (e & 1) r = r * base;
+    base = base * base;
+    e >>= 1;
+  }
+  return r;
+}
+
+}  // namespace
+
+namespace zs {
+
+zs_status fail(zs_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+void clear_error() { g_err[0] = '\0'; }
+
+int elem_bytes(zs_dtype dt) {
+  switch (dt) {
+    case ZS_BF16: return 2;
+    case ZS_FP32: return 4;
+    case ZS_FP24: return 3;
+  }
+  return 0;
+}
+
+}  // namespace zs
+
+extern "C" zs_status zs_shard_step(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                                   const void* const* grad_slices, zs_dtype grad_dtype,
+                                   float* master, float* exp_avg, float* exp_avg_sq,
+                                   void* full_flat, zs_dtype param_dtype,
+                                   const zs_adamw_hparams* hp, int64_t step,
+                                   void* cuda_stream) {
+  static const char* fn = "zs_shard_step";
+  zs::clear_error();
+  if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
+  const int32_t N = plan->world;
+  const int64_t S = plan->S;
+  if (rank < 0 || rank >= N) return zs::fail(ZS_ERR_RANGE, "%s: rank %d not in [0, %d)", fn, rank, N);
+  if (lo < 0 || hi < lo || hi > S)
+    return zs::fail(ZS_ERR_RANGE, "%s: [lo, hi) = [%lld, %lld) not inside [0, %lld)", fn,
+                    (long long)lo, (long long)hi, (long long)S);
+  if (step < 1) return zs::fail(ZS_ERR_RANGE, "%s: step %lld < 1", fn, (long long)step);
+  if (grad_dtype != ZS_BF16 && grad_dtype != ZS_FP32)
+    return zs::fail(ZS_ERR_INVAL, "%s: gradient dtype %d is not bf16 or fp32", fn, (int)grad_dtype);
+  const int pb = zs::elem_bytes(param_dtype);
+  if (!pb) return zs::fail(ZS_ERR_INVAL, "%s: unknown parameter dtype %d", fn, (int)param_dtype);
+  if (!hp) return zs::fail(ZS_ERR_INVAL, "%s: hyper-parameters are NULL", fn);
+  if (!std::isfinite(hp->lr) || !std::isfinite(hp->weight_decay) || !std::isfinite(hp->eps) ||
+      hp->eps < 0 || !(hp->beta1 >= 0 && hp->beta1 < 1) || !(hp->beta2 >= 0 && hp->beta2 < 1))
+    return zs::fail(ZS_ERR_INVAL,
+                    "%s: need finite lr/wd, eps >= 0 and betas in [0, 1) "
+                    "(lr %g, beta1 %g, beta2 %g, eps %g, wd %g)",
+                    fn, hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay);
+  if (lo == hi) return ZS_OK;
+  if (!grad_slices || !master || !exp_avg || !exp_avg_sq || !full_flat)
+    return zs::fail(ZS_ERR_INVAL, "%s: NULL buffer", fn);
+  const int gb = grad_dtype == ZS_BF16 ? 2 : 4;
+  std::vector<Range> ranges;
+  ranges.reserve(N + 4);
+  for (int32_t j = 0; j < N; ++j) {
+    const void* g = grad_slices[j];
+    if (!g) return zs::fail(ZS_ERR_INVAL, "%s: grad_slices[%d] is NULL", fn, j);
+    if (!aligned16(g)) return zs::fail(ZS_ERR_ALIGN, "%s: grad_slices[%d] is not 16-byte aligned", fn, j);
+    ranges.push_back({(uintptr_t)g, (uintptr_t)g + (uint64_t)S * gb, "grad_slices", j, false});
+  }
+  const void* outs[4] = {master, exp_avg, exp_avg_sq, full_flat};
+  const char* names[4] = {"master", "exp_avg", "exp_avg_sq", "full_flat"};
+  const int64_t out_bytes[4] = {S * 4, S * 4, S * 4, plan->P_pad * pb};
+  for (int k = 0; k < 4; ++k) {
+    if (!aligned16(outs[k])) return zs::fail(ZS_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, names[k]);
+    ranges.push_back({(uintptr_t)outs[k], (uintptr_t)outs[k] + (uint64_t)out_bytes[k], names[k], 0, true});
+  }
+  if (zs_status st = check_overlaps(ranges, fn)) return st;
+  for (int32_t j = 0; j < N; ++j)
+    if (zs_status st = check_device_buffer(grad_slices[j], S * gb, fn, "grad_slices", j)) return st;
+  for (int k = 0; k < 4; ++k)
+    if (zs_status st = check_device_buffer(outs[k], out_bytes[k], fn, names[k], 0)) return st;
+
+  zs::ShardStepLaunch a;
+  a.grads = grad_slices;
+  a.world = N;
+  a.grad_dtype = grad_dtype;
+  a.param_dtype = param_dtype;
+  a.master = master;
+  a.m = exp_avg;
+  a.v = exp_avg_sq;
+  a.slot = static_cast<unsigned char*>(full_flat) + (uint64_t)rank * S * pb;
+  a.lo = lo;
+  a.hi = hi;
+  a.slot_vec_ok = ((uintptr_t)a.slot % (pb == 3 ? 8u : 16u)) == 0;
+  a.s.b1 = (float)hp->beta1;
+  a.s.b2 = (float)hp->beta2;
+  a.s.omb1 = (float)(1.0 - hp->beta1);
+  a.s.omb2 = (float)(1.0 - hp->beta2);
+  a.s.bc1 = (float)(1.0 - pow_binary(hp->beta1, step));
+  a.s.bc2 = (float)(1.0 - pow_binary(hp->beta2, step));
+  a.s.lr = (float)hp->lr;
+  a.s.eps = (float)hp->eps;
+  a.s.decay = (float)(1.0 - hp->lr * hp->weight_decay);
+  a.s.invN = (float)(1.0 / (double)N);
+  cudaError_t e = zs::launch_shard_step(a, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess)
+    return zs::fail(ZS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return ZS_OK;
+}
+
+extern "C" zs_status zs_gather_assemble(const zs_plan* plan, int32_t rank,
+                                        const void* const* shard_srcs, void* full_flat,
+                                        zs_dtype param_dtype, void** views_out,
+                                        void* cuda_stream) {
+  static const char* fn = "zs_gather_assemble";
+  zs::clear_error();
+  if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
+  const int32_t N = plan->world;
+  if (rank < 0 || rank >= N) return zs::fail(ZS_ERR_RANGE, "%s: rank %d not in [0, %d)", fn, rank, N);
+  const int pb = zs::elem_bytes(param_dtype);
+  if (!pb) return zs::fail(ZS_ERR_INVAL, "%s: unknown parameter dtype %d", fn, (int)param_dtype);
+  if (!full_flat) return zs::fail(ZS_ERR_INVAL, "%s: full_flat is NULL", fn);
+  if (!aligned16(full_flat)) return zs::fail(ZS_ERR_ALIGN, "%s: full_flat is not 16-byte aligned", fn);
+  if (!shard_srcs && N > 1) return zs::fail(ZS_ERR_INVAL, "%s: shard_srcs is NULL", fn);
+  const int64_t slot_bytes = plan->S * pb;
+  unsigned char* dst = static_cast<unsigned char*>(full_flat);
+  const uintptr_t dlo = (uintptr_t)dst, dhi = dlo + (uint64_t)plan->P_pad * pb;
+  std::vector<const unsigned char*> srcs(N, nullptr);
+  int active = 0;
+  if (slot_bytes > 0) {
+    if (zs_status st = check_device_buffer(full_flat, plan->P_pad * pb, fn, "full_flat", 0)) return st;
+    for (int32_t j = 0; j < N; ++j) {
+      const unsigned char* s = shard_srcs ? static_cast<const unsigned char*>(shard_srcs[j]) : nullptr;
+      if (j == rank || !s || s == dst + (uint64_t)j * slot_bytes) continue;
+      if (!aligned16(s)) return zs::fail(ZS_ERR_ALIGN, "%s: shard_srcs[%d] is not 16-byte aligned", fn, j);
+      const uintptr_t slo = (uintptr_t)s, shi = slo + (uint64_t)slot_bytes;
+      if (slo < dhi && dlo < shi)
+        return zs::fail(ZS_ERR_INVAL, "%s: shard_srcs[%d] overlaps full_flat", fn, j);
+      if (zs_status st = check_device_buffer(s, slot_bytes, fn, "shard_srcs", j)) return st;
+      srcs[j] = s;
+      ++active;
+    }
+  }
+  if (active > 0) {
+    zs::GatherLaunch g;
+    g.srcs = srcs.data();
+    g.world = N;
+    g.dst = dst;
+    g.slot_bytes = slot_bytes;
+    cudaError_t e = zs::launch_gather(g, static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess)
+      return zs::fail(ZS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  }
+  if (views_out)
+    for (int32_t k = 0; k < plan->n_params; ++k)
+      views_out[k] = dst + (uint64_t)plan->offsets[k] * pb;
+  return ZS_OK;
+}
+
+extern "C" const char* zs_status_string(zs_status st) {
+  switch (st) {
+    case ZS_OK: return "ok";
+    case ZS_ERR_INVAL: return "invalid argument";
+    case ZS_ERR_ALIGN: return "misaligned device pointer";
+    case ZS_ERR_RANGE: return "out of range";
+    case ZS_ERR_CUDA: return "CUDA error";
+    case ZS_ERR_NOMEM: return "out of host memory";
+    case ZS_ERR_TIMEOUT: return "device wait timed out";
+    case ZS_ERR_UNSUPPORTED: return "unsupported";
+  }
+  return "unknown status";
+}
+
+extern "C" const char* zs_last_error(void) { return g_err; }
+
+extern "C" zs_status zs_check_device_error(void* cuda_stream) {
+  zs::clear_error();
+  unsigned int word = 0;
+  cudaError_t e = zs::read_and_clear_device_error(static_cast<cudaStream_t>(cuda_stream), &word);
+  if (e != cudaSuccess)
+    return zs::fail(ZS_ERR_CUDA, "zs_check_device_error: %s", cudaGetErrorString(e));
+  if (word & 2u) return zs::fail(ZS_ERR_TIMEOUT, "zs_check_device_error: a device wait timed out");
+  if (word & 1u) return zs::fail(ZS_ERR_RANGE, "zs_check_device_error: a bounds check failed");
+  return ZS_OK;
+}
+
+extern "C" int32_t zs_set_validation(int32_t level) {
+  int32_t old = g_validation;
+  g_validation = level;
+  return old;
+}
+
+extern "C" const char* zs_version(void) { return "0.1.0"; }

@@ -1,0 +1,69 @@
+// zs_internal.h — declarations shared by the library's own translation units
+// (planner, C-ABI layer, kernels). Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/zs.h"
+
+struct zs_plan {
+  uint64_t magic;
+  int32_t world;
+  int32_t n_params;
+  int64_t align;
+  int64_t bucket_elems;
+  int64_t P, P_pad, S;
+  std::vector<int64_t> numels;
+  std::vector<int64_t> offsets;
+  std::vector<int32_t> owner;
+  std::vector<int64_t> bucket_lo, bucket_hi;
+};
+
+namespace zs {
+
+constexpr uint64_t kPlanMagic = 0x7A735F706C616E31ull;  // "zs_plan1"
+
+// Thread-local error detail; returns `st` so call sites can `return fail(...)`.
+zs_status fail(zs_status st, const char* fmt, ...);
+void clear_error();
+
+// True when `plan` is a live plan made by zs_flatten_plan.
+bool plan_is_live(const zs_plan* plan);
+
+// fp32 scalars of one optimizer step, computed on the host from doubles.
+struct StepScalars {
+  float b1, b2, omb1, omb2, bc1, bc2, lr, eps, decay, invN;
+};
+
+// Kernel launchers (shard_step.cu, gather.cu). They assume validated input.
+struct ShardStepLaunch {
+  const void* const* grads;  // host array of N device pointers
+  int32_t world;
+  zs_dtype grad_dtype, param_dtype;
+  float* master;
+  float* m;
+  float* v;
+  unsigned char* slot;  // full_flat + rank*S*elem_bytes
+  int64_t lo, hi;
+  bool slot_vec_ok;     // slot + 8k elements is aligned for vector stores
+  StepScalars s;
+};
+cudaError_t launch_shard_step(const ShardStepLaunch& a, cudaStream_t stream);
+
+struct GatherLaunch {
+  const unsigned char* const* srcs;  // host array of N pointers (NULL = skip)
+  int32_t world;
+  unsigned char* dst;                // full_flat
+  int64_t slot_bytes;
+};
+cudaError_t launch_gather(const GatherLaunch& a, cudaStream_t stream);
+
+// Device error word (set by bounds-checked builds and bounded waits).
+cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* word);
+
+int elem_bytes(zs_dtype dt);
+
+}  // namespace zs

@@ -1,0 +1,187 @@
+/*
+ * zs.h — C ABI of the GB300 shard-local step for ZeRO-1/2/3 and FSDP.
+ *
+ * The step every data-parallel rank runs once the gradient ReduceScatter has
+ * delivered its slices: sum the N incoming slices in fp32 and scale by 1/N,
+ * run AdamW on this rank's fp32 master/m/v shard, cast the updated master to
+ * the low-precision parameter straight into this rank's slot of the flat
+ * buffer the parameter AllGather fills, and hand out per-tensor views of that
+ * buffer. Pages followed (short names):
+ *   [Dissection]  "ZeRO vs FSDP: A Rigorous Dissection for Distributed Training
+ *                 Engineers"
+ *   [Lifecycle]   "FSDP2's parameter lifecycle, and the wrap-policy bug that
+ *                 turns one AllGather into ten"
+ *   [DP-to-ZeRO]  "从 Data Parallel 到 ZeRO/FSDP：训练显存到底怎样被切开"
+ *
+ * Conventions for every call:
+ *   - Returns zs_status: 0 on success, a negative code on error. No call
+ *     aborts or exits; zs_last_error() gives a one-line detail (per thread).
+ *   - Device buffers and CUDA streams are owned by the caller. The library
+ *     allocates host memory for plans only and never allocates device memory.
+ *   - Calls that take a stream enqueue work on it and return without
+ *     synchronising; `cuda_stream` is a cudaStream_t (NULL = legacy default).
+ *     Launch failures return ZS_ERR_CUDA.
+ *   - Device pointers must be 16-byte aligned, resident on the current device,
+ *     and (checked, where the driver can tell) cover the bytes the call uses;
+ *     anything else is rejected before a kernel runs.
+ */
+#ifndef ZS_H
+#define ZS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZS_MAX_WORLD 1024
+
+typedef enum {
+  ZS_OK = 0,
+  ZS_ERR_INVAL = -1,       /* bad argument: NULL, unknown dtype, bad plan, overlap */
+  ZS_ERR_ALIGN = -2,       /* a device pointer is not 16-byte aligned */
+  ZS_ERR_RANGE = -3,       /* index range, rank or size out of bounds */
+  ZS_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed */
+  ZS_ERR_NOMEM = -5,       /* host allocation for a plan failed */
+  ZS_ERR_TIMEOUT = -6,     /* a bounded device-side wait gave up */
+  ZS_ERR_UNSUPPORTED = -7  /* combination not built into this library */
+} zs_status;
+
+/* Element types. ZS_FP24 is a 3-byte float: the top 24 bits of an fp32
+ * pattern (sign, 8-bit exponent, 15-bit mantissa), rounded to nearest even,
+ * stored little-endian. It exists only for the parameter-width sweep. */
+typedef enum { ZS_BF16 = 0, ZS_FP32 = 1, ZS_FP24 = 2 } zs_dtype;
+
+typedef struct zs_plan zs_plan; /* opaque, host memory, owned by the library */
+
+typedef struct {
+  double lr, beta1, beta2, eps, weight_decay;
+} zs_adamw_hparams;
+
+/* ---------------------------------------------------------------------------
+ * zs_flatten_plan — the flat-parameter layout and the rank shards.
+ * [Dissection] §3.2 The FlatParameter Abstraction (concatenate a group's
+ * parameters into one 1-D tensor; bookkeeping restores shapes);
+ * [DP-to-ZeRO] "ZeRO Stage 1" (each rank owns about 1/N of the range);
+ * [DP-to-ZeRO] "Shared Parameters 与 Tied Weights" (a shared weight has one
+ * owner, flattened once); [DP-to-ZeRO] "ReduceScatter 必须尽早释放 Gradient"
+ * (buckets ready in backward order).
+ *
+ *   numels[n_params]   element count of each parameter, registration order.
+ *   tied_to[n_params]  -1 for a parameter with its own storage, or the index
+ *                      k < i of the parameter it shares storage with (numels
+ *                      must match); NULL = no ties.
+ *   world              N, the number of data-parallel ranks (1..ZS_MAX_WORLD).
+ *   align_elems        the padded total is a multiple of world*align_elems
+ *                      (>= 1; 128 in the workloads).
+ *   bucket_elems       0 = one bucket; else the greedy bucket limit in
+ *                      elements (whole tensors, newest first).
+ *   out                receives the plan; free it with zs_plan_free.
+ * Layout: unique parameters back to back in registration order, no padding
+ * between them; P = their total; P_pad = ceil(P / (N*align)) * N*align, the
+ * tail [P, P_pad) is padding that holds zero in every buffer; S = P_pad / N;
+ * rank r owns flat elements [r*S, (r+1)*S). The tail pad joins the bucket of
+ * the last-registered tensor (bucket 0, the first ready).
+ * Errors: ZS_ERR_INVAL (NULL, negative numel, bad tie), ZS_ERR_RANGE (world
+ * or sizes out of range, int64 overflow), ZS_ERR_NOMEM.
+ * ------------------------------------------------------------------------- */
+zs_status zs_flatten_plan(const int64_t* numels, const int32_t* tied_to, int32_t n_params,
+                          int32_t world, int64_t align_elems, int64_t bucket_elems,
+                          zs_plan** out);
+
+/* Plan queries. Any output pointer may be NULL. */
+zs_status zs_plan_info(const zs_plan* plan, int64_t* P, int64_t* P_pad, int64_t* S,
+                       int32_t* n_buckets, int32_t* world, int32_t* n_params);
+/* offsets[n_params]: flat element offset of each parameter (a tied parameter
+ * gets its owner's offset). */
+zs_status zs_plan_offsets(const zs_plan* plan, int64_t* offsets, int32_t n_params);
+/* Bucket b's flat range [flat_lo, flat_hi). */
+zs_status zs_plan_bucket_range(const zs_plan* plan, int32_t bucket, int64_t* flat_lo,
+                               int64_t* flat_hi);
+/* Rank r's shard-local part [lo, hi) of bucket b (may be empty, lo == hi). */
+zs_status zs_plan_bucket(const zs_plan* plan, int32_t bucket, int32_t rank, int64_t* lo,
+                         int64_t* hi);
+/* Frees a plan. Freeing a plan twice, or a pointer that is not a live plan,
+ * returns ZS_ERR_INVAL and touches nothing. */
+zs_status zs_plan_free(zs_plan* plan);
+
+/* ---------------------------------------------------------------------------
+ * zs_shard_step — the fused shard-local step of rank `rank` over shard-local
+ * elements [lo, hi) (0, S = the whole shard; a bucket's part otherwise).
+ * Reduce: [Dissection] §2.1 Mechanism and [Lifecycle] "The parameter
+ * lifecycle": after the ReduceScatter each rank owns the reduced gradient of
+ * its shard; [DP-to-ZeRO] "Data Parallel 保证的数学语义": that gradient is
+ * the ranks' mean. Update: [DP-to-ZeRO] "ZeRO Stage 1" (the owner rank
+ * updates its optimizer/parameter shard) with AdamW's fp32 master, m, v
+ * ([Dissection] §1.1-1.2). Cast + place: [DP-to-ZeRO] "ZeRO Stage 1"
+ * (all-gather the updated parameter shards) and "Mixed Precision 至少有四个
+ * Dtype" (the master's low-precision copy).
+ *
+ * Per element i in [lo, hi), in fp32, each operation rounded to nearest even
+ * and nothing fused:
+ *   g   = (((0 + x_0[i]) + x_1[i]) + ... + x_{N-1}[i]) * fp32(1/N)
+ *   m   = b1*m + (1-b1)*g;      v = b2*v + ((1-b2)*g)*g
+ *   u   = (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps)
+ *   p   = p*(1 - lr*wd) - lr*u;  full_flat[rank*S + i] = round(p)
+ * with b1, b2, 1-b1, 1-b2, 1-b1^t, 1-b2^t, lr, eps, 1-lr*wd and 1/N each
+ * computed once in double (beta^t by binary powering) and rounded to fp32.
+ *
+ *   grad_slices[N]  device pointers; slice j is source rank j's gradient for
+ *                   this rank's shard, element 0 of the shard at index 0,
+ *                   S elements of grad_dtype (ZS_BF16 or ZS_FP32). Read only.
+ *   master, exp_avg, exp_avg_sq
+ *                   device fp32 [S], element 0 of the shard; updated in place.
+ *   full_flat       device buffer of N*S elements of param_dtype; only
+ *                   elements [rank*S + lo, rank*S + hi) are written.
+ *   hp, step        AdamW hyper-parameters; step t >= 1 (bias correction).
+ * The slices, the three state arrays and full_flat must not overlap one
+ * another (slices may alias each other). Errors: ZS_ERR_INVAL (NULL, bad
+ * plan, bad dtype, overlap, non-finite or out-of-range hyper-parameter),
+ * ZS_ERR_ALIGN, ZS_ERR_RANGE (rank, lo/hi, step, a buffer shorter than its
+ * extent), ZS_ERR_CUDA (launch failure).
+ * ------------------------------------------------------------------------- */
+zs_status zs_shard_step(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                        const void* const* grad_slices, zs_dtype grad_dtype, float* master,
+                        float* exp_avg, float* exp_avg_sq, void* full_flat,
+                        zs_dtype param_dtype, const zs_adamw_hparams* hp, int64_t step,
+                        void* cuda_stream);
+
+/* ---------------------------------------------------------------------------
+ * zs_gather_assemble — the AllGather's result on one GPU, and the unflatten.
+ * [DP-to-ZeRO] "ZeRO Stage 1" (all-gather updated parameter shards; all
+ * ranks again hold identical full parameters); [Dissection] §3.2 (the
+ * bookkeeping that restores each parameter's view of the flat buffer).
+ *
+ *   shard_srcs[N]  device pointers to each rank's updated shard (S elements
+ *                  of param_dtype). Entry `rank`, NULL entries, and entries
+ *                  that already point at their own slot are skipped.
+ *   full_flat      device buffer of N*S elements; slot j = [j*S, (j+1)*S)
+ *                  receives shard_srcs[j] bit for bit.
+ *   views_out      host array of n_params device pointers (may be NULL):
+ *                  views_out[k] = full_flat + offsets[k]*elem_size; a tied
+ *                  parameter gets its owner's pointer. Shapes are the caller's.
+ * Errors as zs_shard_step; sources overlapping full_flat (other than their
+ * own slot) are ZS_ERR_INVAL.
+ * ------------------------------------------------------------------------- */
+zs_status zs_gather_assemble(const zs_plan* plan, int32_t rank, const void* const* shard_srcs,
+                             void* full_flat, zs_dtype param_dtype, void** views_out,
+                             void* cuda_stream);
+
+/* Diagnostics. */
+const char* zs_status_string(zs_status status);
+const char* zs_last_error(void);
+/* Synchronises `cuda_stream`, then reads and clears this device's error word
+ * (set by bounds-checked builds and bounded waits); ZS_ERR_TIMEOUT or
+ * ZS_ERR_RANGE if it was set, ZS_ERR_CUDA if the stream reports an error. */
+zs_status zs_check_device_error(void* cuda_stream);
+/* 1 = check device pointers against the driver's allocation records on each
+ * call (default), 0 = only NULL/alignment/range checks. Returns the old level. */
+int32_t zs_set_validation(int32_t level);
+/* Library version, "major.minor.patch". */
+const char* zs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZS_H */
