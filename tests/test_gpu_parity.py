@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import fsdp_sharded_mixed_gb300 as zs
-import oracle as orc
+import oracle
 import synth
 from gpu_util import (DEV, ZS_OF, assert_params_close, assert_state_close, dev_fill,
                       oracle_hp, to_dev, to_host)
@@ -43,8 +43,8 @@ def random_case(seed):
         numels[-1] = numels[0]
         ties[-1] = 0
     align = int(rng.choice([128, 128, 8, 1]))
-    gdt = orc.BF16 if rng.random() < 0.7 else orc.FP32
-    pdt = int(rng.choice([orc.BF16, orc.BF16, orc.FP24, orc.FP32]))
+    gdt = oracle.BF16 if rng.random() < 0.7 else oracle.FP32
+    pdt = int(rng.choice([oracle.BF16, oracle.BF16, oracle.FP24, oracle.FP32]))
     return rng, world, numels, ties, align, gdt, pdt
 
 
@@ -62,14 +62,14 @@ def test_random_small_cases(orc, seed):
     lo = int(rng.integers(0, max(1, S // 3)))
     hi = int(rng.integers(max(lo, 2 * S // 3), S + 1))
     hp = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
-    eb = orc.ELEM_BYTES[pdt]
+    eb = oracle.ELEM_BYTES[pdt]
     master0 = synth.fill(S, index0=rank * S, seed=seed, stream=synth.STREAM_MASTER,
                          sigma=0.02, p_limit=P)
     o_state = [master0.copy(), np.zeros(S, np.float32), np.zeros(S, np.float32)]
     o_full = np.zeros(P_pad * eb, np.uint8)
     bufs = [guarded(S * 4, o_state[0]), guarded(S * 4, o_state[1]), guarded(S * 4, o_state[2])]
     full_whole, full = guarded(P_pad * eb, o_full)
-    bf16 = gdt == orc.BF16
+    bf16 = gdt == oracle.BF16
     for t in (1, 2, 3):
         g_host = [synth.fill(S, index0=rank * S, seed=seed, rank=j, step=t, p_limit=P,
                              bf16=bf16) for j in range(N)]
@@ -172,7 +172,7 @@ def test_gpt2_small_buckets_ten_steps(orc):
     for name, d, ref in (("master", d_master, o_master), ("m", d_m, o_m), ("v", d_v, o_v)):
         assert assert_state_close(to_host(d, np.float32), ref, name) == 0
     got = to_host(d_full, np.uint16)
-    assert assert_params_close(got, o_full, orc.BF16) == 0
+    assert assert_params_close(got, o_full, oracle.BF16) == 0
     assert np.array_equal(got, o_full)
     plan.free()
 
@@ -217,7 +217,7 @@ def _full_size_sampled(orc, w, steps, rank, n_samples=60_000):
         assert assert_state_close(d[ti].cpu().numpy(), ref, name) == 0
     slot = d_full.narrow(0, rank * S, S)
     got = slot[ti].cpu().numpy().view(np.uint16)
-    assert assert_params_close(got, o_full[:K], orc.BF16) == 0
+    assert assert_params_close(got, o_full[:K], oracle.BF16) == 0
     # Every element: the slot holds the nearest-even bf16 of the master.
     ref_all = d_master.to(torch.bfloat16).view(torch.int16)
     assert bool((slot == ref_all).all())
@@ -248,7 +248,7 @@ def test_device_generator_matches_host():
             assert np.array_equal(to_host(d, h.dtype), h)
 
 
-@pytest.mark.parametrize("pdt", [orc.BF16, orc.FP24, orc.FP32])
+@pytest.mark.parametrize("pdt", [oracle.BF16, oracle.FP24, oracle.FP32])
 def test_gather_assemble(orc, pdt):
     """Every other rank's shard lands in its slot bit for bit; the own slot, NULL
     entries and sources already in place are skipped; views follow offsets."""
@@ -257,7 +257,7 @@ def test_gather_assemble(orc, pdt):
     N = 5
     plan = zs.zs_flatten_plan(numels, ties, world=N)
     S, P_pad = plan.S, plan.P_pad
-    eb = orc.ELEM_BYTES[pdt]
+    eb = oracle.ELEM_BYTES[pdt]
     rng = np.random.default_rng(pdt)
     shards = [rng.integers(0, 256, size=S * eb, dtype=np.uint8) for _ in range(N)]
     rank = 2
@@ -303,7 +303,7 @@ def test_nan_inf_propagate(orc):
     for name, dt, ref in zip(("master", "m", "v"), d, o):
         assert_state_close(to_host(dt, np.float32), ref, name)
     assert np.isnan(o[0][5]) and np.isnan(o[0][9])
-    assert_params_close(to_host(d_full, np.uint16), o_full, orc.BF16)
+    assert_params_close(to_host(d_full, np.uint16), o_full, oracle.BF16)
     plan.free()
 
 
