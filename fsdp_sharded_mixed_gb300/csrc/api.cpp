@@ -189,7 +189,18 @@ extern "C" zs_status zs_shard_step(const zs_plan* plan, int32_t rank, int64_t lo
   a.slot = static_cast<unsigned char*>(full_flat) + (uint64_t)rank * S * pb;
   a.lo = lo;
   a.hi = hi;
-  a.slot_vec_ok = ((uintptr_t)a.slot % (pb == 3 ? 8u : 16u)) == 0;
+  // The widest vector path every pointer allows: 32-byte accesses need all
+  // bases (and the slot's 16-element groups) 32-byte aligned; 16-byte
+  // accesses need the slot's 8-element groups aligned; else element by element.
+  bool all32 = ((uintptr_t)master | (uintptr_t)exp_avg | (uintptr_t)exp_avg_sq) % 32 == 0;
+  for (int32_t j = 0; j < N && all32; ++j) all32 = (uintptr_t)grad_slices[j] % 32 == 0;
+  const uintptr_t slot_addr = (uintptr_t)a.slot;
+  if (all32 && slot_addr % (pb == 3 ? 16u : 32u) == 0)
+    a.vec_width = 16;
+  else if (slot_addr % (pb == 3 ? 8u : 16u) == 0)
+    a.vec_width = 8;
+  else
+    a.vec_width = 0;
   a.s.b1 = (float)hp->beta1;
   a.s.b2 = (float)hp->beta2;
   a.s.omb1 = (float)(1.0 - hp->beta1);

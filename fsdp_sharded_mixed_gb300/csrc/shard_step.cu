@@ -10,12 +10,16 @@
 // low-precision parameter: g*N + 24 + p bytes per element and about N + 15
 // flops, so HBM bandwidth bounds it and no tensor-core work exists here.
 //
-// Layout of the work: the shard-local range [lo, hi) is cut into groups of 8
-// elements (16 bytes of bf16 per slice). A persistent grid walks the groups
-// with a grid stride; each group is one thread's 16-byte vector loads of every
-// slice and of the three states, the fp32 arithmetic, and 16-byte vector
-// stores. Elements before the first and after the last whole group (bucket
-// ranges start and end at tensor boundaries) are done one by one.
+// Layout of the work: the shard-local range [lo, hi) is cut into groups of GW
+// elements. A persistent grid walks the groups with a grid stride; a group is
+// one thread's vector loads of every slice and of the three states, the fp32
+// arithmetic, and vector stores. GW = 16 uses 32-byte accesses (one ld/st.v8
+// per 16 bf16 or 8 fp32 values, Blackwell's widest global access): the most
+// bytes per load instruction, and enough bytes in flight per SM at two
+// resident blocks. GW = 8 uses 16-byte accesses for callers whose pointers
+// are only 16-byte aligned. Elements before the first and after the last
+// whole group (bucket ranges start and end at tensor boundaries) are done one
+// by one, as is everything when the rank's slot is not vector-aligned.
 //
 // Arithmetic: every operation is an IEEE binary32 op rounded to nearest even
 // (the _rn intrinsics are never contracted into FMAs), in the order the
@@ -33,8 +37,6 @@ __device__ unsigned int g_error_word;
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kGroup = 8;   // elements per group
-constexpr int kBatch = 8;   // gradient slices loaded back to back
 
 enum ParamKind { kParamBf16 = 0, kParamFp32 = 1, kParamFp24 = 2 };
 
@@ -50,35 +52,93 @@ struct StepArgs {
   StepScalars s;
 };
 
-// ---- loads and stores ------------------------------------------------------
-// Gradient slices are read-only for the kernel's lifetime and read once.
-__device__ __forceinline__ uint4 ld_once(const void* p) {
-  uint4 r;
+// ---- global loads and stores -----------------------------------------------
+// Gradient slices are read-only for the kernel's lifetime and read once:
+// non-coherent path, no L1 allocation. States are read then overwritten by the
+// same thread, so they take the coherent path.
+__device__ __forceinline__ void ld16_nc(const void* p, uint32_t* r) {
   asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
       : "l"(p));
-  return r;
 }
-__device__ __forceinline__ float4 ld_state(const float* p) {
-  float4 r;
+__device__ __forceinline__ void ld32_nc(const void* p, uint32_t* r) {
+  asm("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "l"(p));
+}
+__device__ __forceinline__ void ld16_f(const float* p, float* r) {
   asm("ld.global.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
-      : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+      : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3])
       : "l"(p));
-  return r;
 }
-__device__ __forceinline__ void st_state(float* p, float4 x) {
-  asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(x.x), "f"(x.y),
-               "f"(x.z), "f"(x.w)
+__device__ __forceinline__ void ld32_f(const float* p, float* r) {
+  asm("ld.global.L1::no_allocate.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]),
+        "=f"(r[7])
+      : "l"(p));
+}
+__device__ __forceinline__ void st16_u(void* p, const uint32_t* w) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3])
                : "memory");
 }
-__device__ __forceinline__ void st_u32x4(void* p, uint32_t a, uint32_t b, uint32_t c,
-                                         uint32_t d) {
-  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
-               "r"(d)
+__device__ __forceinline__ void st32_u(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                : "memory");
 }
-__device__ __forceinline__ void st_u32x2(void* p, uint32_t a, uint32_t b) {
-  asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+__device__ __forceinline__ void st8_u(void* p, const uint32_t* w) {
+  asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(w[0]), "r"(w[1]) : "memory");
+}
+__device__ __forceinline__ void st16_f(float* p, const float* x) {
+  asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(x[0]), "f"(x[1]),
+               "f"(x[2]), "f"(x[3])
+               : "memory");
+}
+__device__ __forceinline__ void st32_f(float* p, const float* x) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(x[0]),
+               "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7])
+               : "memory");
+}
+
+// GW consecutive fp32 values (a group's worth of one state array).
+template <int GW>
+__device__ __forceinline__ void load_state(const float* p, float* x) {
+  if constexpr (GW == 16) {
+    ld32_f(p, x);
+    ld32_f(p + 8, x + 8);
+  } else {
+    ld16_f(p, x);
+    ld16_f(p + 4, x + 4);
+  }
+}
+template <int GW>
+__device__ __forceinline__ void store_state(float* p, const float* x) {
+  if constexpr (GW == 16) {
+    st32_f(p, x);
+    st32_f(p + 8, x + 8);
+  } else {
+    st16_f(p, x);
+    st16_f(p + 4, x + 4);
+  }
+}
+// GW gradient values of one slice as raw words: GW/2 words (bf16) or GW (fp32).
+template <int GW, bool BF16G>
+__device__ __forceinline__ void load_grad(const void* p, uint32_t* w) {
+  if constexpr (BF16G) {
+    if constexpr (GW == 16) ld32_nc(p, w);
+    else ld16_nc(p, w);
+  } else {
+    const unsigned char* b = static_cast<const unsigned char*>(p);
+    if constexpr (GW == 16) {
+      ld32_nc(b, w);
+      ld32_nc(b + 32, w + 8);
+    } else {
+      ld16_nc(b, w);
+      ld16_nc(b + 16, w + 4);
+    }
+  }
 }
 
 // ---- conversions -------------------------------------------------------------
@@ -121,88 +181,99 @@ __device__ __forceinline__ void adamw(const StepScalars& s, float g, float& p, f
   p = __fsub_rn(__fmul_rn(p, s.decay), __fmul_rn(s.lr, u));
 }
 
-// ---- one group of 8 elements -------------------------------------------------
-// acc[k] += slice_j[8g + k] for j ascending. NG > 0: N known at compile time.
-template <bool BF16G, int NG, int MAXN>
-__device__ __forceinline__ void reduce_group(const StepArgs<MAXN>& a, int64_t g, float acc[8]) {
-  constexpr int W = BF16G ? 1 : 2;  // 16-byte words per slice per group
+// ---- one group of GW elements --------------------------------------------------
+// acc[k] = (((0 + x_0) + x_1) + ...) over the slices, j ascending. The slices
+// are loaded a batch at a time so that a batch's loads are all in flight
+// together. NG > 0: N is a compile-time constant.
+template <int GW, bool BF16G, int NG, int MAXN>
+__device__ __forceinline__ void reduce_group(const StepArgs<MAXN>& a, int64_t g, float* acc) {
+  constexpr int W = BF16G ? GW / 2 : GW;            // 32-bit words per slice per group
+  // Slices per batch: up to 64 gradient words in flight when N is a
+  // compile-time constant, 32 for a runtime N (which keeps more state live).
+  constexpr int kWords = NG > 0 ? 64 : 32;
+  constexpr int KB = kWords / W >= 8 ? 8 : (kWords / W >= 1 ? kWords / W : 1);
+  constexpr int kStride = BF16G ? 2 * GW : 4 * GW;  // bytes per slice per group
   const int n = NG > 0 ? NG : a.world;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
-#pragma unroll(NG > 0 ? (NG + kBatch - 1) / kBatch : 1)
-  for (int j0 = 0; j0 < n; j0 += kBatch) {
-    uint4 raw[kBatch][W];
+  for (int k = 0; k < GW; ++k) acc[k] = 0.0f;
+#pragma unroll(NG > 0 ? (NG + KB - 1) / KB : 1)
+  for (int j0 = 0; j0 < n; j0 += KB) {
+    uint32_t raw[KB][W];
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
+    for (int b = 0; b < KB; ++b)
+      if (j0 + b < n)
+        load_grad<GW, BF16G>(static_cast<const unsigned char*>(a.grads[j0 + b]) + g * kStride,
+                             raw[b]);
+#pragma unroll
+    for (int b = 0; b < KB; ++b) {
       if (j0 + b < n) {
-        const unsigned char* base =
-            static_cast<const unsigned char*>(a.grads[j0 + b]) + g * (16 * W);
+        if constexpr (BF16G) {
 #pragma unroll
-        for (int w = 0; w < W; ++w) raw[b][w] = ld_once(base + 16 * w);
-      }
-    }
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      if (j0 + b < n) {
-        if (BF16G) {
-          const uint32_t q[4] = {raw[b][0].x, raw[b][0].y, raw[b][0].z, raw[b][0].w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            acc[2 * k] = __fadd_rn(acc[2 * k], bf16_lo(q[k]));
-            acc[2 * k + 1] = __fadd_rn(acc[2 * k + 1], bf16_hi(q[k]));
+          for (int k = 0; k < W; ++k) {
+            acc[2 * k] = __fadd_rn(acc[2 * k], bf16_lo(raw[b][k]));
+            acc[2 * k + 1] = __fadd_rn(acc[2 * k + 1], bf16_hi(raw[b][k]));
           }
         } else {
 #pragma unroll
-          for (int w = 0; w < W; ++w) {
-            acc[4 * w + 0] = __fadd_rn(acc[4 * w + 0], __uint_as_float(raw[b][w].x));
-            acc[4 * w + 1] = __fadd_rn(acc[4 * w + 1], __uint_as_float(raw[b][w].y));
-            acc[4 * w + 2] = __fadd_rn(acc[4 * w + 2], __uint_as_float(raw[b][w].z));
-            acc[4 * w + 3] = __fadd_rn(acc[4 * w + 3], __uint_as_float(raw[b][w].w));
-          }
+          for (int k = 0; k < W; ++k) acc[k] = __fadd_rn(acc[k], __uint_as_float(raw[b][k]));
         }
       }
     }
   }
 }
 
-template <int PD>
-__device__ __forceinline__ void store_params8(unsigned char* slot, int64_t g, const float p[8]) {
-  if (PD == kParamBf16) {
-    st_u32x4(slot + 16 * g, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
-             pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
-  } else if (PD == kParamFp32) {
-    st_state(reinterpret_cast<float*>(slot) + 8 * g, make_float4(p[0], p[1], p[2], p[3]));
-    st_state(reinterpret_cast<float*>(slot) + 8 * g + 4, make_float4(p[4], p[5], p[6], p[7]));
-  } else {
-    uint32_t q[8];
+template <int GW, int PD>
+__device__ __forceinline__ void store_params(unsigned char* slot, int64_t g, const float* p) {
+  if constexpr (PD == kParamBf16) {
+    uint32_t w[GW / 2];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) q[k] = to_fp24(p[k]);
-    unsigned char* d = slot + 24 * g;  // 8-byte aligned
-    st_u32x2(d, q[0] | (q[1] << 24), (q[1] >> 8) | (q[2] << 16));
-    st_u32x2(d + 8, (q[2] >> 16) | (q[3] << 8), q[4] | (q[5] << 24));
-    st_u32x2(d + 16, (q[5] >> 8) | (q[6] << 16), (q[6] >> 16) | (q[7] << 8));
+    for (int k = 0; k < GW / 2; ++k) w[k] = pack_bf16x2(p[2 * k], p[2 * k + 1]);
+    if constexpr (GW == 16) st32_u(slot + 32 * g, w);
+    else st16_u(slot + 16 * g, w);
+  } else if constexpr (PD == kParamFp32) {
+    store_state<GW>(reinterpret_cast<float*>(slot) + GW * g, p);
+  } else {
+    // Each run of 8 values is 24 bytes = six little-endian words.
+    unsigned char* d = slot + 3 * GW * g;
+#pragma unroll
+    for (int r = 0; r < GW / 8; ++r) {
+      uint32_t q[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) q[k] = to_fp24(p[8 * r + k]);
+      const uint32_t w[6] = {q[0] | (q[1] << 24), (q[1] >> 8) | (q[2] << 16),
+                             (q[2] >> 16) | (q[3] << 8), q[4] | (q[5] << 24),
+                             (q[5] >> 8) | (q[6] << 16), (q[6] >> 16) | (q[7] << 8)};
+      if constexpr (GW == 16) {
+        // 48 bytes per group from a 16-byte aligned start: 16 + 8 | 8 + 16.
+        if (r == 0) {
+          st16_u(d, w);
+          st8_u(d + 16, w + 4);
+        } else {
+          st8_u(d + 24, w);
+          st16_u(d + 32, w + 2);
+        }
+      } else {
+        st8_u(d, w);
+        st8_u(d + 8, w + 2);
+        st8_u(d + 16, w + 4);
+      }
+    }
   }
 }
 
-template <bool BF16G, int PD, int NG, int MAXN>
+template <int GW, bool BF16G, int PD, int NG, int MAXN>
 __device__ __forceinline__ void process_group(const StepArgs<MAXN>& a, int64_t g) {
-  const float4 p0 = ld_state(a.master + 8 * g), p1 = ld_state(a.master + 8 * g + 4);
-  const float4 m0 = ld_state(a.m + 8 * g), m1 = ld_state(a.m + 8 * g + 4);
-  const float4 v0 = ld_state(a.v + 8 * g), v1 = ld_state(a.v + 8 * g + 4);
-  float acc[8];
-  reduce_group<BF16G, NG>(a, g, acc);
-  float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-  float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-  float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  float p[GW], m[GW], v[GW], acc[GW];
+  load_state<GW>(a.master + GW * g, p);
+  load_state<GW>(a.m + GW * g, m);
+  load_state<GW>(a.v + GW * g, v);
+  reduce_group<GW, BF16G, NG>(a, g, acc);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) adamw(a.s, __fmul_rn(acc[k], a.s.invN), p[k], m[k], v[k]);
-  st_state(a.master + 8 * g, make_float4(p[0], p[1], p[2], p[3]));
-  st_state(a.master + 8 * g + 4, make_float4(p[4], p[5], p[6], p[7]));
-  st_state(a.m + 8 * g, make_float4(m[0], m[1], m[2], m[3]));
-  st_state(a.m + 8 * g + 4, make_float4(m[4], m[5], m[6], m[7]));
-  st_state(a.v + 8 * g, make_float4(v[0], v[1], v[2], v[3]));
-  st_state(a.v + 8 * g + 4, make_float4(v[4], v[5], v[6], v[7]));
-  store_params8<PD>(a.slot, g, p);
+  for (int k = 0; k < GW; ++k) adamw(a.s, __fmul_rn(acc[k], a.s.invN), p[k], m[k], v[k]);
+  store_state<GW>(a.master + GW * g, p);
+  store_state<GW>(a.m + GW * g, m);
+  store_state<GW>(a.v + GW * g, v);
+  store_params<GW, PD>(a.slot, g, p);
 }
 
 // One element, for the ragged head/tail and unaligned slots.
@@ -220,9 +291,9 @@ __device__ __forceinline__ void process_element(const StepArgs<MAXN>& a, int64_t
   a.master[i] = p;
   a.m[i] = m;
   a.v[i] = v;
-  if (PD == kParamBf16) {
+  if constexpr (PD == kParamBf16) {
     reinterpret_cast<uint16_t*>(a.slot)[i] = to_bf16(p);
-  } else if (PD == kParamFp32) {
+  } else if constexpr (PD == kParamFp32) {
     reinterpret_cast<float*>(a.slot)[i] = p;
   } else {
     const uint32_t q = to_fp24(p);
@@ -233,31 +304,35 @@ __device__ __forceinline__ void process_element(const StepArgs<MAXN>& a, int64_t
   }
 }
 
-template <bool BF16G, int PD, int NG, int MAXN, bool VEC>
-__global__ void __launch_bounds__(kThreads)
+// GW = 0: every element one by one. GW = 8 or 16: whole groups vectorised.
+template <int GW, bool BF16G, int PD, int NG, int MAXN>
+__global__ void __launch_bounds__(kThreads, 2)
     shard_step_kernel(const __grid_constant__ StepArgs<MAXN> a) {
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
-  if (!VEC) {
-    for (int64_t i = a.lo + tid; i < a.hi; i += stride) process_element<BF16G, PD>(a, i);
-    return;
+  int64_t g0 = 0, g1 = 0;
+  if constexpr (GW > 0) {
+    g0 = (a.lo + GW - 1) / GW;
+    g1 = a.hi / GW;
   }
-  int64_t g0 = (a.lo + kGroup - 1) / kGroup, g1 = a.hi / kGroup;
   if (g0 >= g1) {  // no whole group: everything is ragged
     for (int64_t i = a.lo + tid; i < a.hi; i += stride) process_element<BF16G, PD>(a, i);
     return;
   }
-  const int64_t head = g0 * kGroup - a.lo, tail = a.hi - g1 * kGroup;
-  if (tid < head) process_element<BF16G, PD>(a, a.lo + tid);
-  else if (tid < head + tail) process_element<BF16G, PD>(a, g1 * kGroup + (tid - head));
-  for (int64_t g = g0 + tid; g < g1; g += stride) process_group<BF16G, PD, NG>(a, g);
+  if constexpr (GW > 0) {
+    const int64_t head = g0 * GW - a.lo, tail = a.hi - g1 * GW;
+    if (tid < head) process_element<BF16G, PD>(a, a.lo + tid);
+    else if (tid < head + tail) process_element<BF16G, PD>(a, g1 * GW + (tid - head));
+    for (int64_t g = g0 + tid; g < g1; g += stride) process_group<GW, BF16G, PD, NG>(a, g);
+  }
 }
 
-template <bool BF16G, int PD, int NG, int MAXN, bool VEC>
+template <int GW, bool BF16G, int PD, int NG, int MAXN>
 cudaError_t launch_one(const ShardStepLaunch& in, cudaStream_t stream) {
-  // Resident blocks on the whole GPU for this instantiation, per device.
+  // Resident blocks on the whole GPU for this instantiation, per device; the
+  // grid is twice that, so the tail of one wave overlaps the next.
   static int max_blocks_by_dev[64];
-  auto kernel = shard_step_kernel<BF16G, PD, NG, MAXN, VEC>;
+  auto kernel = shard_step_kernel<GW, BF16G, PD, NG, MAXN>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -268,7 +343,7 @@ cudaError_t launch_one(const ShardStepLaunch& in, cudaStream_t stream) {
     if (e == cudaSuccess)
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
     if (e != cudaSuccess) return e;
-    max_blocks = sms * (per_sm > 0 ? per_sm : 1);
+    max_blocks = 2 * sms * (per_sm > 0 ? per_sm : 1);
   }
   StepArgs<MAXN> a;
   for (int j = 0; j < in.world; ++j) a.grads[j] = in.grads[j];
@@ -281,7 +356,7 @@ cudaError_t launch_one(const ShardStepLaunch& in, cudaStream_t stream) {
   a.hi = in.hi;
   a.world = in.world;
   a.s = in.s;
-  const int64_t units = VEC ? (in.hi - in.lo) / kGroup + 2 : (in.hi - in.lo);
+  const int64_t units = GW > 0 ? (in.hi - in.lo) / GW + 2 : (in.hi - in.lo);
   int64_t blocks = (units + kThreads - 1) / kThreads;
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
@@ -290,14 +365,17 @@ cudaError_t launch_one(const ShardStepLaunch& in, cudaStream_t stream) {
 }
 
 template <bool BF16G, int PD>
-cudaError_t dispatch_n(const ShardStepLaunch& a, cudaStream_t stream) {
-  if (!a.slot_vec_ok) return launch_one<BF16G, PD, 0, ZS_MAX_WORLD, false>(a, stream);
-  if constexpr (BF16G && PD == kParamBf16) {
-    if (a.world == 4) return launch_one<BF16G, PD, 4, 16, true>(a, stream);
-    if (a.world == 8) return launch_one<BF16G, PD, 8, 16, true>(a, stream);
+cudaError_t dispatch(const ShardStepLaunch& a, cudaStream_t stream) {
+  if (a.vec_width == 16) {
+    if constexpr (BF16G && PD == kParamBf16) {
+      if (a.world == 4) return launch_one<16, BF16G, PD, 4, 16>(a, stream);
+      if (a.world == 8) return launch_one<16, BF16G, PD, 8, 16>(a, stream);
+    }
+    if (a.world <= 16) return launch_one<16, BF16G, PD, 0, 16>(a, stream);
+    return launch_one<16, BF16G, PD, 0, ZS_MAX_WORLD>(a, stream);
   }
-  if (a.world <= 16) return launch_one<BF16G, PD, 0, 16, true>(a, stream);
-  return launch_one<BF16G, PD, 0, ZS_MAX_WORLD, true>(a, stream);
+  if (a.vec_width == 8) return launch_one<8, BF16G, PD, 0, ZS_MAX_WORLD>(a, stream);
+  return launch_one<0, BF16G, PD, 0, ZS_MAX_WORLD>(a, stream);
 }
 
 }  // namespace
@@ -306,11 +384,11 @@ cudaError_t launch_shard_step(const ShardStepLaunch& a, cudaStream_t stream) {
   const bool bf16g = a.grad_dtype == ZS_BF16;
   switch (a.param_dtype) {
     case ZS_BF16:
-      return bf16g ? dispatch_n<true, kParamBf16>(a, stream) : dispatch_n<false, kParamBf16>(a, stream);
+      return bf16g ? dispatch<true, kParamBf16>(a, stream) : dispatch<false, kParamBf16>(a, stream);
     case ZS_FP32:
-      return bf16g ? dispatch_n<true, kParamFp32>(a, stream) : dispatch_n<false, kParamFp32>(a, stream);
+      return bf16g ? dispatch<true, kParamFp32>(a, stream) : dispatch<false, kParamFp32>(a, stream);
     case ZS_FP24:
-      return bf16g ? dispatch_n<true, kParamFp24>(a, stream) : dispatch_n<false, kParamFp24>(a, stream);
+      return bf16g ? dispatch<true, kParamFp24>(a, stream) : dispatch<false, kParamFp24>(a, stream);
   }
   return cudaErrorInvalidValue;
 }

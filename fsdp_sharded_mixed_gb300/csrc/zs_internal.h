@@ -48,7 +48,8 @@ struct ShardStepLaunch {
   float* v;
   unsigned char* slot;  // full_flat + rank*S*elem_bytes
   int64_t lo, hi;
-  bool slot_vec_ok;     // slot + 8k elements is aligned for vector stores
+  int vec_width;        // elements per vector group: 16 (32-byte accesses),
+                        // 8 (16-byte accesses) or 0 (element by element)
   StepScalars s;
 };
 cudaError_t launch_shard_step(const ShardStepLaunch& a, cudaStream_t stream);

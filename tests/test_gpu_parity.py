@@ -18,18 +18,21 @@ pytestmark = pytest.mark.gpu
 CANARY = 0x5A
 
 
-def guarded(nbytes, fill=None):
-    """A device byte buffer with 256-byte guard bands of CANARY on both sides;
-    returns (whole, interior) where interior is 16-byte aligned."""
-    whole = torch.full((nbytes + 512,), CANARY, dtype=torch.uint8, device=DEV)
-    inner = whole.narrow(0, 256, nbytes)
+def guarded(nbytes, fill=None, front=256):
+    """A device byte buffer with guard bands of CANARY on both sides (``front``
+    bytes before, 256 after); returns (whole, interior). front = 256 gives a
+    32-byte aligned interior, 272 one that is only 16-byte aligned."""
+    whole = torch.full((front + nbytes + 256,), CANARY, dtype=torch.uint8, device=DEV)
+    inner = whole.narrow(0, front, nbytes)
     if fill is not None:
         inner.copy_(torch.from_numpy(np.ascontiguousarray(fill).view(np.uint8)).to(DEV))
+    whole.zs_front = front
     return whole, inner
 
 
 def guards_intact(whole):
-    g = torch.cat([whole[:256], whole[-256:]])
+    front = whole.zs_front
+    g = torch.cat([whole[:front], whole[whole.numel() - 256:]])
     return bool((g == CANARY).all())
 
 
@@ -67,13 +70,17 @@ def test_random_small_cases(orc, seed):
                          sigma=0.02, p_limit=P)
     o_state = [master0.copy(), np.zeros(S, np.float32), np.zeros(S, np.float32)]
     o_full = np.zeros(P_pad * eb, np.uint8)
-    bufs = [guarded(S * 4, o_state[0]), guarded(S * 4, o_state[1]), guarded(S * 4, o_state[2])]
-    full_whole, full = guarded(P_pad * eb, o_full)
+    # Some seeds place one buffer only 16-byte aligned: the 16-byte vector path.
+    fronts = [256] * (N + 4)
+    if seed % 3 == 1:
+        fronts[int(rng.integers(0, N + 4))] = 272
+    bufs = [guarded(S * 4, o_state[k], fronts[N + k]) for k in range(3)]
+    full_whole, full = guarded(P_pad * eb, o_full, fronts[N + 3])
     bf16 = gdt == oracle.BF16
     for t in (1, 2, 3):
         g_host = [synth.fill(S, index0=rank * S, seed=seed, rank=j, step=t, p_limit=P,
                              bf16=bf16) for j in range(N)]
-        g_dev = [guarded(g.nbytes, g) for g in g_host]
+        g_dev = [guarded(g.nbytes, g, fronts[j]) for j, g in enumerate(g_host)]
         zs.zs_shard_step(plan, rank, lo, hi, [g[1] for g in g_dev],
                          zs.ZS_BF16 if bf16 else zs.ZS_FP32, bufs[0][1], bufs[1][1],
                          bufs[2][1], full, ZS_OF[pdt], hp, t)
