@@ -300,29 +300,53 @@ def run_ours(args, w):
         step()
         torch.cuda.synchronize()
 
-    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+    # The timed region: K steps back to back between two events on the
+    # launching stream (or one replay of a CUDA graph holding the K launches).
+    graph = None
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=side, capture_error_mode="relaxed"):
+            gptr = side.cuda_stream
+            for _ in range(args.steps):
+                step_no[0] += 1
+                zs.zs_shard_step(plan, r, 0, S, grads, zs.ZS_BF16, master, m, v, full,
+                                 zs.ZS_BF16, hp, step_no[0], stream=gptr)
+        stream.wait_stream(side)
+        graph.replay()  # one untimed replay
     if gworld > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for k in range(args.steps):
-        events[k][0].record(stream)
-        step()
-        events[k][1].record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for _ in range(args.steps):
+            step()
     t1.record(stream)
     torch.cuda.synchronize()
     if gworld > 1:
         dist.barrier()
     clocks = sampler.stop()
     elapsed = t0.elapsed_time(t1) / 1e3
-    per_step = sorted(a.elapsed_time(b) for a, b in events)
-    launch_avg_s = sum(per_step) / len(per_step) / 1e3
+    launch_avg_s = elapsed / args.steps
     t_max = max_over_ranks(elapsed, dev)
     elems_all = sum_over_ranks(float(S) * args.steps, dev)
     value = elems_all / t_max
+
+    # Per-step spread, measured after the timed region (events around each step).
+    n_spread = min(args.steps, 50)
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n_spread)]
+    for a_ev, b_ev in events:
+        a_ev.record(stream)
+        step()
+        b_ev.record(stream)
+    torch.cuda.synchronize()
+    per_step = sorted(a_ev.elapsed_time(b_ev) for a_ev, b_ev in events)
 
     # End to end through the C ABI from pinned host memory: every step copies
     # the N incoming slices host->device and reads the updated slot back.
@@ -383,7 +407,10 @@ def run_ours(args, w):
             "hbm_gbs": bpe * value / gworld / 1e9,
             "step_ms": {"median": statistics.median(per_step),
                         "p10": per_step[len(per_step) // 10],
-                        "p90": per_step[(9 * len(per_step)) // 10]},
+                        "p90": per_step[(9 * len(per_step)) // 10],
+                        "note": f"{n_spread} steps with events around each, after the timed region"},
+            "timing": "cuda graph replay of the K steps" if graph is not None
+                      else "K direct launches between two events",
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks,
         }
@@ -402,6 +429,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="llama-7b")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--graph", action="store_true",
+                    help="time one replay of a CUDA graph holding the K launches")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
