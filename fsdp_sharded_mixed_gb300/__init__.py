@@ -34,7 +34,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-fmad=false", "-prec-div=true",
               "-prec-sqrt=true", "-ftz=false", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-I/usr/local/cuda/include"]
-CUDA_SOURCES = ["shard_step.cu", "gather.cu"]
+CUDA_SOURCES = ["shard_step.cu", "gather.cu", "clip.cu"]
 HOST_SOURCES = ["api.cpp", "plan.cpp"]
 
 
@@ -104,6 +104,12 @@ EXPORTS = {
     "zs_shard_step": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _P, _P, _P, ctypes.c_int,
                        ctypes.POINTER(AdamWHparams), _I64, _P], ctypes.c_int),
     "zs_gather_assemble": ([_P, _I32, _P, _P, ctypes.c_int, _P, _P], ctypes.c_int),
+    "zs_grad_norm_workspace_bytes": ([], _I64),
+    "zs_grad_sqnorm": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _I64, _P, _P], ctypes.c_int),
+    "zs_clip_coefficient": ([_P, _I32, ctypes.c_double, _P, _P, _P], ctypes.c_int),
+    "zs_shard_step_clipped": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _P, _P, _P,
+                               ctypes.c_int, ctypes.POINTER(AdamWHparams), _I64, _P, _P, _P],
+                              ctypes.c_int),
     "zs_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "zs_last_error": ([], ctypes.c_char_p),
     "zs_check_device_error": ([_P], ctypes.c_int),
@@ -226,6 +232,39 @@ def zs_shard_step(plan, rank, lo, hi, grad_slices, grad_dtype, master, exp_avg, 
     _check(lib().zs_shard_step(plan.handle, rank, lo, hi, ptrs, grad_dtype, _ptr(master),
                                _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(full_flat), param_dtype,
                                ctypes.byref(h), step, _stream(stream)))
+
+
+def zs_shard_step_clipped(plan, rank, lo, hi, grad_slices, grad_dtype, master, exp_avg,
+                          exp_avg_sq, full_flat, param_dtype, hp, step, coef=None, skip=None,
+                          stream=None):
+    """``zs_shard_step`` with a device clip coefficient and skip flag (tensors
+    or addresses of a device fp32 and a device int32; None = not used)."""
+    ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
+    h = AdamWHparams(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"])
+    _check(lib().zs_shard_step_clipped(plan.handle, rank, lo, hi, ptrs, grad_dtype, _ptr(master),
+                                       _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(full_flat),
+                                       param_dtype, ctypes.byref(h), step, _ptr(coef),
+                                       _ptr(skip), _stream(stream)))
+
+
+def zs_grad_norm_workspace_bytes():
+    return lib().zs_grad_norm_workspace_bytes()
+
+
+def zs_grad_sqnorm(plan, rank, lo, hi, grad_slices, grad_dtype, workspace, sqnorm_out,
+                   stream=None):
+    """Enqueue the shard's sum of squared mean gradients into the device
+    double ``sqnorm_out``; ``workspace`` is caller-owned device scratch."""
+    ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
+    nbytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") \
+        else zs_grad_norm_workspace_bytes()
+    _check(lib().zs_grad_sqnorm(plan.handle, rank, lo, hi, ptrs, grad_dtype, _ptr(workspace),
+                                nbytes, _ptr(sqnorm_out), _stream(stream)))
+
+
+def zs_clip_coefficient(rank_sqnorms, n, max_norm, coef_out, nonfinite_out, stream=None):
+    _check(lib().zs_clip_coefficient(_ptr(rank_sqnorms), n, max_norm, _ptr(coef_out),
+                                     _ptr(nonfinite_out), _stream(stream)))
 
 
 def zs_gather_assemble(plan, rank, shard_srcs, full_flat, param_dtype, stream=None):

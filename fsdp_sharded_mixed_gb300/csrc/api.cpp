@@ -126,13 +126,13 @@ int elem_bytes(zs_dtype dt) {
 
 }  // namespace zs
 
-extern "C" zs_status zs_shard_step(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
-                                   const void* const* grad_slices, zs_dtype grad_dtype,
-                                   float* master, float* exp_avg, float* exp_avg_sq,
-                                   void* full_flat, zs_dtype param_dtype,
-                                   const zs_adamw_hparams* hp, int64_t step,
-                                   void* cuda_stream) {
-  static const char* fn = "zs_shard_step";
+namespace {
+
+zs_status shard_step_impl(const char* fn, const zs_plan* plan, int32_t rank, int64_t lo,
+                          int64_t hi, const void* const* grad_slices, zs_dtype grad_dtype,
+                          float* master, float* exp_avg, float* exp_avg_sq, void* full_flat,
+                          zs_dtype param_dtype, const zs_adamw_hparams* hp, int64_t step,
+                          const float* coef, const int32_t* skip, void* cuda_stream) {
   zs::clear_error();
   if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
   const int32_t N = plan->world;
@@ -211,7 +211,125 @@ extern "C" zs_status zs_shard_step(const zs_plan* plan, int32_t rank, int64_t lo
   a.s.eps = (float)hp->eps;
   a.s.decay = (float)(1.0 - hp->lr * hp->weight_decay);
   a.s.invN = (float)(1.0 / (double)N);
+  a.coef = coef;
+  a.skip = skip;
   cudaError_t e = zs::launch_shard_step(a, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess)
+    return zs::fail(ZS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return ZS_OK;
+}
+
+// A device scalar the kernels read: aligned, device memory, in bounds.
+zs_status check_device_scalar(const void* p, int64_t bytes, const char* fn, const char* name) {
+  if (!p) return zs::fail(ZS_ERR_INVAL, "%s: %s is NULL", fn, name);
+  if ((uintptr_t)p % (uintptr_t)bytes != 0)
+    return zs::fail(ZS_ERR_ALIGN, "%s: %s is not %lld-byte aligned", fn, name, (long long)bytes);
+  return check_device_buffer(p, bytes, fn, name, 0);
+}
+
+}  // namespace
+
+extern "C" zs_status zs_shard_step(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                                   const void* const* grad_slices, zs_dtype grad_dtype,
+                                   float* master, float* exp_avg, float* exp_avg_sq,
+                                   void* full_flat, zs_dtype param_dtype,
+                                   const zs_adamw_hparams* hp, int64_t step,
+                                   void* cuda_stream) {
+  return shard_step_impl("zs_shard_step", plan, rank, lo, hi, grad_slices, grad_dtype, master,
+                         exp_avg, exp_avg_sq, full_flat, param_dtype, hp, step, nullptr, nullptr,
+                         cuda_stream);
+}
+
+extern "C" zs_status zs_shard_step_clipped(const zs_plan* plan, int32_t rank, int64_t lo,
+                                           int64_t hi, const void* const* grad_slices,
+                                           zs_dtype grad_dtype, float* master, float* exp_avg,
+                                           float* exp_avg_sq, void* full_flat,
+                                           zs_dtype param_dtype, const zs_adamw_hparams* hp,
+                                           int64_t step, const float* coef,
+                                           const int32_t* skip, void* cuda_stream) {
+  static const char* fn = "zs_shard_step_clipped";
+  zs::clear_error();
+  if (coef)
+    if (zs_status st = check_device_scalar(coef, 4, fn, "coef")) return st;
+  if (skip)
+    if (zs_status st = check_device_scalar(skip, 4, fn, "skip")) return st;
+  return shard_step_impl(fn, plan, rank, lo, hi, grad_slices, grad_dtype, master, exp_avg,
+                         exp_avg_sq, full_flat, param_dtype, hp, step, coef, skip, cuda_stream);
+}
+
+extern "C" int64_t zs_grad_norm_workspace_bytes(void) { return zs::kNormWorkspaceBytes; }
+
+extern "C" zs_status zs_grad_sqnorm(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                                    const void* const* grad_slices, zs_dtype grad_dtype,
+                                    void* workspace, int64_t workspace_bytes, double* sqnorm_out,
+                                    void* cuda_stream) {
+  static const char* fn = "zs_grad_sqnorm";
+  zs::clear_error();
+  if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
+  const int32_t N = plan->world;
+  const int64_t S = plan->S;
+  if (rank < 0 || rank >= N) return zs::fail(ZS_ERR_RANGE, "%s: rank %d not in [0, %d)", fn, rank, N);
+  if (lo < 0 || hi < lo || hi > S)
+    return zs::fail(ZS_ERR_RANGE, "%s: [lo, hi) = [%lld, %lld) not inside [0, %lld)", fn,
+                    (long long)lo, (long long)hi, (long long)S);
+  if (grad_dtype != ZS_BF16 && grad_dtype != ZS_FP32)
+    return zs::fail(ZS_ERR_INVAL, "%s: gradient dtype %d is not bf16 or fp32", fn, (int)grad_dtype);
+  if (!workspace || workspace_bytes < zs::kNormWorkspaceBytes)
+    return zs::fail(ZS_ERR_RANGE, "%s: workspace must hold %lld bytes", fn,
+                    (long long)zs::kNormWorkspaceBytes);
+  if (!aligned16(workspace)) return zs::fail(ZS_ERR_ALIGN, "%s: workspace is not 16-byte aligned", fn);
+  if (zs_status st = check_device_scalar(sqnorm_out, 8, fn, "sqnorm_out")) return st;
+  if (hi > lo && !grad_slices) return zs::fail(ZS_ERR_INVAL, "%s: grad_slices is NULL", fn);
+  const int gb = grad_dtype == ZS_BF16 ? 2 : 4;
+  std::vector<Range> ranges;
+  bool all32 = true;
+  for (int32_t j = 0; j < N && hi > lo; ++j) {
+    const void* g = grad_slices[j];
+    if (!g) return zs::fail(ZS_ERR_INVAL, "%s: grad_slices[%d] is NULL", fn, j);
+    if (!aligned16(g)) return zs::fail(ZS_ERR_ALIGN, "%s: grad_slices[%d] is not 16-byte aligned", fn, j);
+    all32 = all32 && (uintptr_t)g % 32 == 0;
+    ranges.push_back({(uintptr_t)g, (uintptr_t)g + (uint64_t)S * gb, "grad_slices", j, false});
+  }
+  ranges.push_back({(uintptr_t)workspace, (uintptr_t)workspace + (uint64_t)zs::kNormWorkspaceBytes,
+                    "workspace", 0, true});
+  ranges.push_back({(uintptr_t)sqnorm_out, (uintptr_t)sqnorm_out + 8, "sqnorm_out", 0, true});
+  if (zs_status st = check_overlaps(ranges, fn)) return st;
+  if (zs_status st = check_device_buffer(workspace, zs::kNormWorkspaceBytes, fn, "workspace", 0)) return st;
+  for (int32_t j = 0; j < N && hi > lo; ++j)
+    if (zs_status st = check_device_buffer(grad_slices[j], S * gb, fn, "grad_slices", j)) return st;
+  zs::NormLaunch a;
+  a.grads = grad_slices;
+  a.world = N;
+  a.grad_dtype = grad_dtype;
+  a.lo = lo;
+  a.hi = hi;
+  a.vec = all32;
+  a.invN = (float)(1.0 / (double)N);
+  a.partials = static_cast<double*>(workspace);
+  a.ticket = reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(workspace) +
+                                             zs::kNormTicketOffset);
+  a.out = sqnorm_out;
+  cudaError_t e = zs::launch_grad_sqnorm(a, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess)
+    return zs::fail(ZS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return ZS_OK;
+}
+
+extern "C" zs_status zs_clip_coefficient(const double* rank_sqnorms, int32_t n, double max_norm,
+                                         float* coef_out, int32_t* nonfinite_out,
+                                         void* cuda_stream) {
+  static const char* fn = "zs_clip_coefficient";
+  zs::clear_error();
+  if (n < 1 || n > ZS_MAX_WORLD) return zs::fail(ZS_ERR_RANGE, "%s: n %d outside 1..%d", fn, n, ZS_MAX_WORLD);
+  if (!std::isfinite(max_norm) || !(max_norm > 0))
+    return zs::fail(ZS_ERR_INVAL, "%s: max_norm must be finite and > 0 (got %g)", fn, max_norm);
+  if (!rank_sqnorms || (uintptr_t)rank_sqnorms % 8)
+    return zs::fail(ZS_ERR_ALIGN, "%s: rank_sqnorms must be 8-byte aligned device memory", fn);
+  if (zs_status st = check_device_buffer(rank_sqnorms, 8 * (int64_t)n, fn, "rank_sqnorms", 0)) return st;
+  if (zs_status st = check_device_scalar(coef_out, 4, fn, "coef_out")) return st;
+  if (zs_status st = check_device_scalar(nonfinite_out, 4, fn, "nonfinite_out")) return st;
+  cudaError_t e = zs::launch_clip_coef(rank_sqnorms, n, max_norm, coef_out, nonfinite_out,
+                                       static_cast<cudaStream_t>(cuda_stream));
   if (e != cudaSuccess)
     return zs::fail(ZS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return ZS_OK;

@@ -1,0 +1,209 @@
+// clip.cu — global-norm gradient clipping for the sharded step, and the
+// non-finite decision every rank shares.
+//
+// "从 Data Parallel 到 ZeRO/FSDP", "Gradient Accumulation 会改变生命周期": a
+// sharded step has to settle whether clipping uses the global norm or the
+// local shard's, and whether an overflow is decided by all ranks alike. Here:
+// the global L2 norm of the reduced (mean) gradient. Each rank sums the
+// squares of its shard's mean gradient (grad_sqnorm_kernel); the N partial
+// sums are added in rank order, the square root taken and the coefficient
+// min(1, max_norm / (norm + 1e-6)) formed in double and rounded to fp32
+// (clip_coef_kernel, the scalar AllReduce of a real system emulated on one
+// GPU); the step multiplies the mean gradient by it, and a non-finite norm
+// makes the step leave every buffer untouched.
+//
+// The norm pass reads the N slices once (g*N bytes per element). Squares are
+// formed in fp32 with their exact rounding residue (an FMA), summed per
+// 16-element group with a compensated (two-sum) fp32 accumulator, and folded
+// into a per-thread double; double work is one add per group, because GB300's
+// fp64 rate is far below its fp32 rate. The grid is a fixed 1024 blocks, each
+// block's partial goes to scratch memory, and the last block to finish adds
+// the partials in block order: the result does not depend on timing and is
+// the same on every run.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zs_internal.h"
+
+namespace zs {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kGW = 16;
+
+template <int MAXN>
+struct NormArgs {
+  const void* grads[MAXN];
+  int64_t lo, hi;
+  int world;
+  float invN;
+  double* partials;        // [kNormPartials]
+  unsigned int* ticket;    // zero on entry; the last block resets it
+  double* out;
+};
+
+__device__ __forceinline__ void ld32_nc(const void* p, uint32_t* r) {
+  asm("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "l"(p));
+}
+
+// Compensated accumulation of g*g: s + c carries the group's sum with the
+// rounding errors of the squares (exact residues) and of the additions.
+__device__ __forceinline__ void acc_square(float g, float& s, float& c) {
+  const float hi = __fmul_rn(g, g);
+  const float lo = __fmaf_rn(g, g, -hi);
+  const float t = __fadd_rn(s, hi);
+  const float bv = __fsub_rn(t, s);
+  const float av = __fsub_rn(t, bv);
+  const float err = __fadd_rn(__fsub_rn(s, av), __fsub_rn(hi, bv));
+  s = t;
+  c = __fadd_rn(c, __fadd_rn(err, lo));
+}
+
+template <bool BF16G, int MAXN>
+__device__ __forceinline__ float mean_grad(const NormArgs<MAXN>& a, int64_t i) {
+  float acc = 0.0f;
+  for (int j = 0; j < a.world; ++j) {
+    const float x = BF16G ? __uint_as_float(
+                                (uint32_t) static_cast<const uint16_t*>(a.grads[j])[i] << 16)
+                          : static_cast<const float*>(a.grads[j])[i];
+    acc = __fadd_rn(acc, x);
+  }
+  return __fmul_rn(acc, a.invN);
+}
+
+// VEC: 16-element groups with 32-byte loads (all slices 32-byte aligned);
+// otherwise element by element.
+template <bool BF16G, bool VEC, int MAXN>
+__global__ void __launch_bounds__(kThreads) grad_sqnorm_kernel(const __grid_constant__ NormArgs<MAXN> a) {
+  const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  double sum = 0.0;
+  int64_t g0 = 0, g1 = 0;
+  if (VEC) {
+    g0 = (a.lo + kGW - 1) / kGW;
+    g1 = a.hi / kGW;
+  }
+  if (g0 >= g1) {
+    for (int64_t i = a.lo + tid; i < a.hi; i += stride) {
+      const float g = mean_grad<BF16G>(a, i);
+      float s = 0.0f, c = 0.0f;
+      acc_square(g, s, c);
+      sum += (double)s + (double)c;
+    }
+  } else {
+    const int64_t head = g0 * kGW - a.lo, tail = a.hi - g1 * kGW;
+    if (tid < head + tail) {
+      const int64_t i = tid < head ? a.lo + tid : g1 * kGW + (tid - head);
+      const float g = mean_grad<BF16G>(a, i);
+      float s = 0.0f, c = 0.0f;
+      acc_square(g, s, c);
+      sum += (double)s + (double)c;
+    }
+    constexpr int W = BF16G ? kGW / 2 : kGW;
+    constexpr int kStride = BF16G ? 2 * kGW : 4 * kGW;
+    for (int64_t g = g0 + tid; g < g1; g += stride) {
+      float acc[kGW];
+#pragma unroll
+      for (int k = 0; k < kGW; ++k) acc[k] = 0.0f;
+      for (int j = 0; j < a.world; ++j) {
+        uint32_t raw[W];
+        const unsigned char* base = static_cast<const unsigned char*>(a.grads[j]) + g * kStride;
+        ld32_nc(base, raw);
+        if (!BF16G) ld32_nc(base + 32, raw + 8);
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          if (BF16G) {
+            acc[2 * k] = __fadd_rn(acc[2 * k], __uint_as_float(raw[k] << 16));
+            acc[2 * k + 1] = __fadd_rn(acc[2 * k + 1], __uint_as_float(raw[k] & 0xFFFF0000u));
+          } else {
+            acc[k] = __fadd_rn(acc[k], __uint_as_float(raw[k]));
+          }
+        }
+      }
+      float s = 0.0f, c = 0.0f;
+#pragma unroll
+      for (int k = 0; k < kGW; ++k) acc_square(__fmul_rn(acc[k], a.invN), s, c);
+      sum += (double)s + (double)c;
+    }
+  }
+  // Block sum in a fixed order: warp shuffle tree, then warp 0 over the warps.
+  __shared__ double warp_sums[kThreads / 32];
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_down_sync(0xFFFFFFFFu, sum, off);
+  if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = sum;
+  __syncthreads();
+  __shared__ bool last;
+  if (threadIdx.x == 0) {
+    double b = 0.0;
+    for (int w = 0; w < kThreads / 32; ++w) b += warp_sums[w];
+    a.partials[blockIdx.x] = b;
+    __threadfence();
+    last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last || threadIdx.x >= 32) return;
+  // The last block: lane l adds partials l, l+32, ... in order, then a tree.
+  __threadfence();
+  const volatile double* parts = a.partials;
+  double t = 0.0;
+  for (unsigned int b = threadIdx.x; b < gridDim.x; b += 32) t += parts[b];
+  for (int off = 16; off > 0; off >>= 1) t += __shfl_down_sync(0xFFFFFFFFu, t, off);
+  if (threadIdx.x == 0) {
+    *a.out = t;
+    *a.ticket = 0u;
+  }
+}
+
+__global__ void clip_coef_kernel(const double* rank_sqnorms, int n, double max_norm, float* coef,
+                                 int32_t* nonfinite) {
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  double total = 0.0;
+  for (int r = 0; r < n; ++r) total = total + rank_sqnorms[r];
+  const double norm = sqrt(total);
+  const bool bad = !isfinite(norm);
+  const double c = max_norm / (norm + 1e-6);
+  *nonfinite = bad ? 1 : 0;
+  *coef = bad ? 1.0f : (float)(c < 1.0 ? c : 1.0);
+}
+
+template <bool BF16G, bool VEC, int MAXN>
+cudaError_t launch_norm(const NormLaunch& in, cudaStream_t stream) {
+  NormArgs<MAXN> a;
+  for (int j = 0; j < MAXN; ++j) a.grads[j] = (in.grads && j < in.world) ? in.grads[j] : nullptr;
+  a.lo = in.lo;
+  a.hi = in.hi;
+  a.world = in.world;
+  a.invN = in.invN;
+  a.partials = in.partials;
+  a.ticket = in.ticket;
+  a.out = in.out;
+  cudaError_t e = cudaMemsetAsync(in.ticket, 0, sizeof(unsigned int), stream);
+  if (e != cudaSuccess) return e;
+  grad_sqnorm_kernel<BF16G, VEC, MAXN><<<kNormPartials, kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grad_sqnorm(const NormLaunch& a, cudaStream_t stream) {
+  const bool bf16g = a.grad_dtype == ZS_BF16;
+  if (a.world <= 16) {
+    if (a.vec) return bf16g ? launch_norm<true, true, 16>(a, stream) : launch_norm<false, true, 16>(a, stream);
+    return bf16g ? launch_norm<true, false, 16>(a, stream) : launch_norm<false, false, 16>(a, stream);
+  }
+  if (a.vec)
+    return bf16g ? launch_norm<true, true, ZS_MAX_WORLD>(a, stream)
+                 : launch_norm<false, true, ZS_MAX_WORLD>(a, stream);
+  return bf16g ? launch_norm<true, false, ZS_MAX_WORLD>(a, stream)
+               : launch_norm<false, false, ZS_MAX_WORLD>(a, stream);
+}
+
+cudaError_t launch_clip_coef(const double* rank_sqnorms, int n, double max_norm, float* coef,
+                             int32_t* nonfinite, cudaStream_t stream) {
+  clip_coef_kernel<<<1, 32, 0, stream>>>(rank_sqnorms, n, max_norm, coef, nonfinite);
+  return cudaGetLastError();
+}
+
+}  // namespace zs

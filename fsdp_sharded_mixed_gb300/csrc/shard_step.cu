@@ -49,6 +49,8 @@ struct StepArgs {
   unsigned char* slot;
   int64_t lo, hi;
   int world;
+  const float* coef;    // clip coefficient (device), or NULL
+  const int32_t* skip;  // shared non-finite decision (device), or NULL
   StepScalars s;
 };
 
@@ -261,15 +263,22 @@ __device__ __forceinline__ void store_params(unsigned char* slot, int64_t g, con
   }
 }
 
+// The mean gradient, times the clip coefficient when clipping.
+__device__ __forceinline__ float mean_grad(float acc, float invN, bool clip, float coef) {
+  const float g = __fmul_rn(acc, invN);
+  return clip ? __fmul_rn(g, coef) : g;
+}
+
 template <int GW, bool BF16G, int PD, int NG, int MAXN>
-__device__ __forceinline__ void process_group(const StepArgs<MAXN>& a, int64_t g) {
+__device__ __forceinline__ void process_group(const StepArgs<MAXN>& a, int64_t g, bool clip,
+                                              float coef) {
   float p[GW], m[GW], v[GW], acc[GW];
   load_state<GW>(a.master + GW * g, p);
   load_state<GW>(a.m + GW * g, m);
   load_state<GW>(a.v + GW * g, v);
   reduce_group<GW, BF16G, NG>(a, g, acc);
 #pragma unroll
-  for (int k = 0; k < GW; ++k) adamw(a.s, __fmul_rn(acc[k], a.s.invN), p[k], m[k], v[k]);
+  for (int k = 0; k < GW; ++k) adamw(a.s, mean_grad(acc[k], a.s.invN, clip, coef), p[k], m[k], v[k]);
   store_state<GW>(a.master + GW * g, p);
   store_state<GW>(a.m + GW * g, m);
   store_state<GW>(a.v + GW * g, v);
@@ -278,7 +287,8 @@ __device__ __forceinline__ void process_group(const StepArgs<MAXN>& a, int64_t g
 
 // One element, for the ragged head/tail and unaligned slots.
 template <bool BF16G, int PD, int MAXN>
-__device__ __forceinline__ void process_element(const StepArgs<MAXN>& a, int64_t i) {
+__device__ __forceinline__ void process_element(const StepArgs<MAXN>& a, int64_t i, bool clip,
+                                                float coef) {
   float acc = 0.0f;
   for (int j = 0; j < a.world; ++j) {
     const float x = BF16G ? __uint_as_float(
@@ -287,7 +297,7 @@ __device__ __forceinline__ void process_element(const StepArgs<MAXN>& a, int64_t
     acc = __fadd_rn(acc, x);
   }
   float p = a.master[i], m = a.m[i], v = a.v[i];
-  adamw(a.s, __fmul_rn(acc, a.s.invN), p, m, v);
+  adamw(a.s, mean_grad(acc, a.s.invN, clip, coef), p, m, v);
   a.master[i] = p;
   a.m[i] = m;
   a.v[i] = v;
@@ -308,6 +318,9 @@ __device__ __forceinline__ void process_element(const StepArgs<MAXN>& a, int64_t
 template <int GW, bool BF16G, int PD, int NG, int MAXN>
 __global__ void __launch_bounds__(kThreads, 2)
     shard_step_kernel(const __grid_constant__ StepArgs<MAXN> a) {
+  if (a.skip && *a.skip) return;  // the ranks' shared non-finite decision
+  const bool clip = a.coef != nullptr;
+  const float coef = clip ? *a.coef : 1.0f;
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   int64_t g0 = 0, g1 = 0;
@@ -316,14 +329,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     g1 = a.hi / GW;
   }
   if (g0 >= g1) {  // no whole group: everything is ragged
-    for (int64_t i = a.lo + tid; i < a.hi; i += stride) process_element<BF16G, PD>(a, i);
+    for (int64_t i = a.lo + tid; i < a.hi; i += stride)
+      process_element<BF16G, PD>(a, i, clip, coef);
     return;
   }
   if constexpr (GW > 0) {
     const int64_t head = g0 * GW - a.lo, tail = a.hi - g1 * GW;
-    if (tid < head) process_element<BF16G, PD>(a, a.lo + tid);
-    else if (tid < head + tail) process_element<BF16G, PD>(a, g1 * GW + (tid - head));
-    for (int64_t g = g0 + tid; g < g1; g += stride) process_group<GW, BF16G, PD, NG>(a, g);
+    if (tid < head) process_element<BF16G, PD>(a, a.lo + tid, clip, coef);
+    else if (tid < head + tail)
+      process_element<BF16G, PD>(a, g1 * GW + (tid - head), clip, coef);
+    for (int64_t g = g0 + tid; g < g1; g += stride)
+      process_group<GW, BF16G, PD, NG>(a, g, clip, coef);
   }
 }
 
@@ -355,6 +371,8 @@ cudaError_t launch_one(const ShardStepLaunch& in, cudaStream_t stream) {
   a.lo = in.lo;
   a.hi = in.hi;
   a.world = in.world;
+  a.coef = in.coef;
+  a.skip = in.skip;
   a.s = in.s;
   const int64_t units = GW > 0 ? (in.hi - in.lo) / GW + 2 : (in.hi - in.lo);
   int64_t blocks = (units + kThreads - 1) / kThreads;

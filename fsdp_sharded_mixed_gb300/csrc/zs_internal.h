@@ -50,6 +50,8 @@ struct ShardStepLaunch {
   int64_t lo, hi;
   int vec_width;        // elements per vector group: 16 (32-byte accesses),
                         // 8 (16-byte accesses) or 0 (element by element)
+  const float* coef;    // device fp32 clip coefficient, or NULL (no clipping)
+  const int32_t* skip;  // device flag: non-zero leaves every buffer as it is, or NULL
   StepScalars s;
 };
 cudaError_t launch_shard_step(const ShardStepLaunch& a, cudaStream_t stream);
@@ -61,6 +63,26 @@ struct GatherLaunch {
   int64_t slot_bytes;
 };
 cudaError_t launch_gather(const GatherLaunch& a, cudaStream_t stream);
+
+// Global-norm pass (clip.cu): per-block partial sums of squares in scratch
+// memory, reduced in block order by the last block.
+constexpr int kNormPartials = 1024;
+constexpr int64_t kNormTicketOffset = kNormPartials * 8;   // bytes
+constexpr int64_t kNormWorkspaceBytes = kNormTicketOffset + 256;
+struct NormLaunch {
+  const void* const* grads;
+  int32_t world;
+  zs_dtype grad_dtype;
+  int64_t lo, hi;
+  bool vec;             // all slices 32-byte aligned: 16-element vector groups
+  float invN;
+  double* partials;     // [kNormPartials]
+  unsigned int* ticket;
+  double* out;
+};
+cudaError_t launch_grad_sqnorm(const NormLaunch& a, cudaStream_t stream);
+cudaError_t launch_clip_coef(const double* rank_sqnorms, int n, double max_norm, float* coef,
+                             int32_t* nonfinite, cudaStream_t stream);
 
 // Device error word (set by bounds-checked builds and bounded waits).
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* word);

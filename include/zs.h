@@ -167,6 +167,55 @@ zs_status zs_gather_assemble(const zs_plan* plan, int32_t rank, const void* cons
                              void* full_flat, zs_dtype param_dtype, void** views_out,
                              void* cuda_stream);
 
+/* ---------------------------------------------------------------------------
+ * Global-norm gradient clipping and the shared non-finite decision.
+ * [DP-to-ZeRO] "Gradient Accumulation 会改变生命周期": a sharded step must
+ * settle whether clipping uses the global norm or the local shard's, and
+ * whether an overflow is decided by all ranks alike; its landing path checks
+ * clipping by comparing single-step updates. Reading: the global L2 norm of
+ * the reduced (mean) gradient; every rank skips the update when it is not
+ * finite. Per step:
+ *   1. each rank: zs_grad_sqnorm -> its shard's sum over i of g_i^2 (double);
+ *   2. zs_clip_coefficient over the N partial sums (added in rank order; the
+ *      scalar AllReduce of a real system) -> coef = fp32(min(1, max_norm /
+ *      (sqrt(total) + 1e-6))) and nonfinite = !isfinite(sqrt(total));
+ *   3. each rank: zs_shard_step_clipped with coef and nonfinite as `skip`.
+ * Nothing returns to the host in between.
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of scratch device memory zs_grad_sqnorm needs (1024 fp64 block
+ * partials and a ticket word; 8448). The caller allocates and owns it. */
+int64_t zs_grad_norm_workspace_bytes(void);
+
+/* Sum over shard-local i in [lo, hi) of g_i^2, g_i the step's fp32 mean of the
+ * N slices (same order and rounding as zs_shard_step), each square exact and
+ * the sum carried in double; written to the device double *sqnorm_out. The
+ * sum is reduced over a fixed 1024-block grid in a fixed order, so it is the
+ * same on every run (it may differ from a sequential sum in the last bits).
+ * workspace: 16-byte aligned device scratch of at least
+ * zs_grad_norm_workspace_bytes() bytes, used by one call at a time. Errors as
+ * zs_shard_step, plus ZS_ERR_RANGE for a short workspace. */
+zs_status zs_grad_sqnorm(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                         const void* const* grad_slices, zs_dtype grad_dtype, void* workspace,
+                         int64_t workspace_bytes, double* sqnorm_out, void* cuda_stream);
+
+/* rank_sqnorms: device double [n], the ranks' partial sums (1 <= n <= 1024).
+ * Writes the device fp32 *coef_out and the device int32 *nonfinite_out (1 when
+ * the global norm is Inf or NaN; coef is then 1). max_norm: finite, > 0. */
+zs_status zs_clip_coefficient(const double* rank_sqnorms, int32_t n, double max_norm,
+                              float* coef_out, int32_t* nonfinite_out, void* cuda_stream);
+
+/* zs_shard_step with g = (mean) * (*coef) when coef is not NULL, and no change
+ * to any buffer when skip is not NULL and *skip != 0. coef and skip are device
+ * pointers read by the kernel (4-byte aligned). With coef == NULL and skip ==
+ * NULL it is zs_shard_step. */
+zs_status zs_shard_step_clipped(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                                const void* const* grad_slices, zs_dtype grad_dtype,
+                                float* master, float* exp_avg, float* exp_avg_sq,
+                                void* full_flat, zs_dtype param_dtype,
+                                const zs_adamw_hparams* hp, int64_t step, const float* coef,
+                                const int32_t* skip, void* cuda_stream);
+
 /* Diagnostics. */
 const char* zs_status_string(zs_status status);
 const char* zs_last_error(void);

@@ -76,6 +76,13 @@ def load(path=LIB_PATH):
     L.oracle_ddp_step.argtypes = [_I32, _I64, _P, _I32, _P, _P, _P, _P, _I32, _D, _D, _D,
                                   _D, _D, _I64]
     L.oracle_ddp_step.restype = ctypes.c_int
+    L.oracle_grad_sqnorm.argtypes = [_I32, _I64, _I64, _I64, _P, _I32]
+    L.oracle_grad_sqnorm.restype = _D
+    L.oracle_clip_coef.argtypes = [_P, _I32, _D, _P, _P]
+    L.oracle_clip_coef.restype = None
+    L.oracle_shard_step_clipped.argtypes = [_I32, _I32, _I64, _I64, _I64, _P, _I32, _P, _P, _P,
+                                            _P, _I32, _D, _D, _D, _D, _D, _I64, _F, _I32]
+    L.oracle_shard_step_clipped.restype = ctypes.c_int
     L.oracle_gather.argtypes = [_I32, _I64, _I32, _P, _P]
     L.oracle_gather.restype = None
     L.oracle_bf16_rne.argtypes = [_F]
@@ -167,6 +174,30 @@ class Oracle:
                                     wd, t)
         if rc != 0:
             raise ValueError("oracle_ddp_step rejected the input")
+
+    # -- global-norm clipping ---------------------------------------------
+    def grad_sqnorm(self, *, world, S, lo, hi, grads):
+        gdt = BF16 if grads[0].dtype == np.uint16 else FP32
+        return self.L.oracle_grad_sqnorm(world, S, lo, hi, self._ptrs(grads), gdt)
+
+    def clip_coef(self, rank_sqnorms, max_norm):
+        a = np.ascontiguousarray(rank_sqnorms, dtype=np.float64)
+        coef = ctypes.c_float()
+        bad = ctypes.c_int32()
+        self.L.oracle_clip_coef(a.ctypes.data, a.size, max_norm, ctypes.byref(coef),
+                                ctypes.byref(bad))
+        return np.float32(coef.value), int(bad.value)
+
+    def shard_step_clipped(self, *, world, rank, S, lo, hi, grads, master, m, v, full_flat,
+                           coef, skip, param_dtype=BF16, lr=1e-3, beta1=0.9, beta2=0.999,
+                           eps=1e-8, wd=0.01, t=1):
+        gdt = BF16 if grads[0].dtype == np.uint16 else FP32
+        rc = self.L.oracle_shard_step_clipped(world, rank, S, lo, hi, self._ptrs(grads), gdt,
+                                              master.ctypes.data, m.ctypes.data, v.ctypes.data,
+                                              full_flat.ctypes.data, param_dtype, lr, beta1,
+                                              beta2, eps, wd, t, float(coef), int(skip))
+        if rc != 0:
+            raise ValueError("oracle_shard_step_clipped rejected the input")
 
     # -- O6 gather -------------------------------------------------------
     def gather(self, *, world, S, elem_size, shards, full_flat):

@@ -357,6 +357,73 @@ int oracle_shard_step(int32_t world, int32_t rank, int64_t S, int64_t lo, int64_
 }
 
 /* ---------------------------------------------------------------------------
+ * Gradient clipping on the global norm, with the non-finite decision shared by
+ * all ranks. [DP-to-ZeRO] "Gradient Accumulation 会改变生命周期" lists what a
+ * sharded step must settle: whether clipping uses the global norm or the local
+ * shard's, and whether overflow is decided by all ranks consistently; its
+ * landing path (step 9) checks clipping by comparing single-step updates.
+ * Readings: the global L2 norm of the reduced (mean) gradient over all P_pad
+ * elements; each rank contributes the sum of squares of its shard and the N
+ * partial sums are added in rank order (the emulated scalar AllReduce); the
+ * coefficient is min(1, max_norm / (norm + 1e-6)) in double, rounded to fp32,
+ * applied as g * coef after the mean; a non-finite norm (an Inf or NaN
+ * anywhere) makes every rank skip the update, leaving master, m, v and the
+ * parameter slot untouched.
+ * ------------------------------------------------------------------------- */
+
+/* Sum over i in [lo, hi), ascending, of g_i^2 in double, g_i being the step's
+ * fp32 mean gradient (the square of an fp32 value is exact in double). */
+double oracle_grad_sqnorm(int32_t world, int64_t S, int64_t lo, int64_t hi,
+                          const void* const* grads, int32_t grad_dtype) {
+  if (world < 1 || lo < 0 || hi < lo || hi > S) return -1.0;
+  float invN = (float)(1.0 / (double)world);
+  double sum = 0.0;
+  for (int64_t i = lo; i < hi; ++i) {
+    float acc = 0.0f;
+    for (int32_t j = 0; j < world; ++j) acc = acc + load_grad(grads[j], grad_dtype, i);
+    float g = acc * invN;
+    sum = sum + (double)g * (double)g;
+  }
+  return sum;
+}
+
+/* The N ranks' partial sums of squares -> the clip coefficient and the shared
+ * non-finite flag. */
+void oracle_clip_coef(const double* rank_sqnorms, int32_t n, double max_norm, float* coef,
+                      int32_t* nonfinite) {
+  double total = 0.0;
+  for (int32_t r = 0; r < n; ++r) total = total + rank_sqnorms[r];
+  double norm = std::sqrt(total);
+  *nonfinite = std::isfinite(norm) ? 0 : 1;
+  double c = max_norm / (norm + 1e-6);
+  *coef = *nonfinite ? 1.0f : (float)(c < 1.0 ? c : 1.0);
+}
+
+/* The shard step with the clip coefficient applied to the mean gradient and
+ * the shared skip decision. */
+int oracle_shard_step_clipped(int32_t world, int32_t rank, int64_t S, int64_t lo, int64_t hi,
+                              const void* const* grads, int32_t grad_dtype, float* master,
+                              float* m, float* v, void* full_flat, int32_t param_dtype,
+                              double lr, double beta1, double beta2, double eps, double wd,
+                              int64_t t, float coef, int32_t skip) {
+  if (world < 1 || rank < 0 || rank >= world || lo < 0 || hi < lo || hi > S || t < 1)
+    return -1;
+  if (!elem_bytes(param_dtype) || (grad_dtype != DT_BF16 && grad_dtype != DT_FP32))
+    return -1;
+  if (skip) return 0;
+  Scalars s = make_scalars(lr, beta1, beta2, eps, wd, t, world);
+  int64_t slot = (int64_t)rank * S;
+  for (int64_t i = lo; i < hi; ++i) {
+    float acc = 0.0f;
+    for (int32_t j = 0; j < world; ++j) acc = acc + load_grad(grads[j], grad_dtype, i);
+    float g = (acc * s.invN) * coef;
+    adamw_element(s, g, master[i], m[i], v[i]);
+    store_param(full_flat, param_dtype, slot + i, master[i]);
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------
  * O7. The unsharded data-parallel step every DDP replica runs ([DP-to-ZeRO]
  * "DDP 为什么单卡仍是 16P" and "Data Parallel 保证的数学语义"): AllReduce the
  * N local gradients to their mean over the whole flat buffer, run AdamW on

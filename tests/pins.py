@@ -618,10 +618,147 @@ def pin_bucket_invariance(o):
             assert np.array_equal(fw, fp)
 
 
+# --------------------------------------------------- global-norm clipping ----
+def pin_sqnorm_dyadic(o):
+    """Small dyadic slices: the sum of squares of the mean gradient is exact in
+    double, equal to the rational closed form."""
+    rng = np.random.default_rng(12)
+    for world in (1, 2, 4, 8):
+        ints = rng.integers(-64, 65, size=(world, 333))
+        vals = (ints * 2.0 ** -8).astype(np.float32)
+        grads = [to_bf16_exact(vals[j]) for j in range(world)]
+        got = o.grad_sqnorm(world=world, S=333, lo=0, hi=333, grads=grads)
+        exact = sum(Fraction(int(x), 256 * world) ** 2 for x in ints.sum(axis=0))
+        assert Fraction(got) == exact, world
+        lo, hi = 17, 300
+        part = o.grad_sqnorm(world=world, S=333, lo=lo, hi=hi, grads=grads)
+        assert Fraction(part) == sum(Fraction(int(x), 256 * world) ** 2
+                                     for x in ints.sum(axis=0)[lo:hi])
+
+
+def pin_clip_coef_closed_forms(o):
+    """min(1, max_norm / (norm + 1e-6)) in fp32; the partial sums add in rank
+    order; an infinite or NaN norm sets the shared skip flag."""
+    c, bad = o.clip_coef([9.0, 16.0], 1.0)
+    assert bad == 0 and c == np.float32(1.0 / (5.0 + 1e-6))
+    c, bad = o.clip_coef([9.0, 16.0], 100.0)
+    assert bad == 0 and c == np.float32(1.0)
+    c, bad = o.clip_coef([4.0, 0.0, 0.0], 1.0)
+    assert bad == 0 and c == np.float32(1.0 / (2.0 + 1e-6))
+    c, bad = o.clip_coef([0.0], 1.0)
+    assert bad == 0 and c == np.float32(1.0)
+    for rank_sq in ([float("inf"), 1.0], [1.0, float("nan")], [1e308, 1e308]):
+        c, bad = o.clip_coef(rank_sq, 1.0)
+        assert bad == 1 and c == np.float32(1.0), rank_sq
+    c, bad = o.clip_coef([1e300, 1e300], 1.0)
+    assert bad == 0 and c == np.float32(1.0 / (np.sqrt(2e300) + 1e-6))
+
+
+def _clip_inputs(n=2048, world=4, seed=31):
+    grads = [synth.fill(n, seed=seed, rank=j, step=1, bf16=True, outlier_frac=0.02,
+                        outlier_scale=50.0) for j in range(world)]
+    master = synth.fill(n, seed=seed, stream=synth.STREAM_MASTER, sigma=0.02)
+    return grads, master
+
+
+def pin_clip_unit_identity(o):
+    """coef = 1 and no skip is the unclipped step, bit for bit."""
+    grads, master = _clip_inputs()
+    n, world = master.size, len(grads)
+    a = [master.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)]
+    b = [master.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)]
+    fa = np.zeros(n * world, np.uint16)
+    fb = np.zeros(n * world, np.uint16)
+    for t in (1, 2):
+        o.shard_step(world=world, rank=0, S=n, lo=0, hi=n, grads=grads, master=a[0], m=a[1],
+                     v=a[2], full_flat=fa, t=t, **HP)
+        o.shard_step_clipped(world=world, rank=0, S=n, lo=0, hi=n, grads=grads, master=b[0],
+                             m=b[1], v=b[2], full_flat=fb, coef=1.0, skip=0, t=t, **HP)
+    for x, y in zip(a, b):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+    assert np.array_equal(fa, fb)
+
+
+def pin_clip_post_norm(o):
+    """After clipping to max_norm, the gradient the update sees has global
+    norm max_norm * norm / (norm + 1e-6) (observed as m with beta1 = 0)."""
+    grads, master = _clip_inputs()
+    n, world = master.size, len(grads)
+    sq = o.grad_sqnorm(world=world, S=n, lo=0, hi=n, grads=grads)
+    norm = np.sqrt(sq)
+    max_norm = 0.25 * norm
+    coef, bad = o.clip_coef([sq], max_norm)
+    assert bad == 0 and coef < 1
+    m = np.zeros(n, np.float32)
+    o.shard_step_clipped(world=world, rank=0, S=n, lo=0, hi=n, grads=grads, master=master.copy(),
+                         m=m, v=np.zeros(n, np.float32), full_flat=np.zeros(n * world, np.uint16),
+                         coef=coef, skip=0, t=1, lr=0.0, beta1=0.0, beta2=0.999, eps=1e-8,
+                         wd=0.0)
+    got = np.sqrt(np.sum(m.astype(np.float64) ** 2))
+    expect = max_norm * norm / (norm + 1e-6)
+    assert abs(got - expect) <= 4e-7 * expect, (got, expect)
+
+
+def pin_clip_skip(o):
+    """A skipped step leaves master, m, v and the parameter slot untouched."""
+    grads, master = _clip_inputs()
+    n, world = master.size, len(grads)
+    st = [master.copy(), np.full(n, 0.5, np.float32), np.full(n, 0.25, np.float32)]
+    full = np.full(n * world, 0x1234, np.uint16)
+    before = [x.copy() for x in st] + [full.copy()]
+    o.shard_step_clipped(world=world, rank=0, S=n, lo=0, hi=n, grads=grads, master=st[0],
+                         m=st[1], v=st[2], full_flat=full, coef=0.5, skip=1, t=3, **HP)
+    for x, y in zip(st + [full], before):
+        assert np.array_equal(x, y)
+
+
+def pin_clip_ddp_equivalence(o, w=TINY, steps=2):
+    """Clipping on the global norm: the sharded pipeline (each rank's partial
+    sum of squares, the coefficient over the N partials, N clipped shard steps,
+    gather) equals the unsharded clipped step over the whole flat buffer, bit
+    for bit, and both see the same coefficient."""
+    plan = o.plan(w.numels, w.tied_to, world=w.world, align=w.align)
+    P, P_pad, S, N = plan["P"], plan["P_pad"], plan["S"], w.world
+    master0 = synth.fill(P_pad, seed=w.seed, stream=synth.STREAM_MASTER, sigma=w.master_sigma,
+                         p_limit=P)
+    full_st = [master0.copy(), np.zeros(P_pad, np.float32), np.zeros(P_pad, np.float32)]
+    full_params = np.zeros(P_pad * N, np.uint16)   # rank-0 "slot" spans the whole buffer
+    sh = [[master0[r * S:(r + 1) * S].copy(), np.zeros(S, np.float32), np.zeros(S, np.float32)]
+          for r in range(N)]
+    max_norm = None
+    for t in range(1, steps + 1):
+        local = _local_grads(w, P_pad, P, t, N)
+        sq_full = o.grad_sqnorm(world=N, S=P_pad, lo=0, hi=P_pad, grads=local)
+        if max_norm is None:
+            max_norm = 0.5 * float(np.sqrt(sq_full))
+        c_full, bad_full = o.clip_coef([sq_full], max_norm)
+        o.shard_step_clipped(world=N, rank=0, S=P_pad, lo=0, hi=P_pad, grads=local,
+                             master=full_st[0], m=full_st[1], v=full_st[2], full_flat=full_params,
+                             coef=c_full, skip=bad_full, t=t, **HP)
+        slices = [[local[j][r * S:(r + 1) * S].copy() for j in range(N)] for r in range(N)]
+        partial = [o.grad_sqnorm(world=N, S=S, lo=0, hi=S, grads=slices[r]) for r in range(N)]
+        c_sh, bad_sh = o.clip_coef(partial, max_norm)
+        assert bad_sh == bad_full == 0 and c_sh == c_full and c_sh < 1, (c_sh, c_full)
+        fulls = []
+        for r in range(N):
+            f = np.zeros(P_pad, np.uint16)
+            o.shard_step_clipped(world=N, rank=r, S=S, lo=0, hi=S, grads=slices[r],
+                                 master=sh[r][0], m=sh[r][1], v=sh[r][2], full_flat=f,
+                                 coef=c_sh, skip=bad_sh, t=t, **HP)
+            fulls.append(f[r * S:(r + 1) * S].copy())
+        gathered = np.zeros(P_pad, np.uint16)
+        o.gather(world=N, S=S, elem_size=2, shards=fulls, full_flat=gathered)
+        assert np.array_equal(gathered, full_params[:P_pad]), f"params differ at t={t}"
+        for k in range(3):
+            assert np.array_equal(np.concatenate([x[k] for x in sh]).view(np.uint32),
+                                  full_st[k].view(np.uint32)), f"state {k} differs at t={t}"
+
+
 ALL_PINS = [
     pin_sign_law, pin_zero_grad, pin_constant_grad, pin_eps_placement, pin_lr0_wd0,
     pin_fp64_bound, pin_bias_correction_t2, pin_reduce_dyadic, pin_reduce_order,
     pin_reduce_mean, pin_cast_sampled, pin_param_store, pin_plan_bruteforce,
     pin_plan_buckets, pin_plan_workloads, pin_ledger_pages, pin_ddp_equivalence,
-    pin_bucket_invariance,
+    pin_bucket_invariance, pin_sqnorm_dyadic, pin_clip_coef_closed_forms,
+    pin_clip_unit_identity, pin_clip_post_norm, pin_clip_skip, pin_clip_ddp_equivalence,
 ]

@@ -52,6 +52,14 @@ MUTANTS = [
      "static_cast<uint8_t*>(full_flat) + (size_t)j * S * elem_size, shards[j],",
      "static_cast<uint8_t*>(full_flat) + (size_t)j * S, shards[j],"),
     ("DDP sum, not mean", "mean[i] = acc * s.invN;", "mean[i] = acc;"),
+    ("norm of the sum, not the mean", "float g = acc * invN;\n    sum = sum + (double)g * (double)g;",
+     "float g = acc;\n    sum = sum + (double)g * (double)g;"),
+    ("norm without square root", "double norm = std::sqrt(total);", "double norm = total;"),
+    ("coefficient not clamped", "*coef = *nonfinite ? 1.0f : (float)(c < 1.0 ? c : 1.0);",
+     "*coef = *nonfinite ? 1.0f : (float)c;"),
+    ("non-finite never flagged", "*nonfinite = std::isfinite(norm) ? 0 : 1;", "*nonfinite = 0;"),
+    ("skip ignored", "  if (skip) return 0;", "  if (false) return 0;"),
+    ("coefficient ignored", "float g = (acc * s.invN) * coef;", "float g = acc * s.invN;"),
 ]
 
 
