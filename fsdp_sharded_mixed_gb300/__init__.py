@@ -106,6 +106,7 @@ EXPORTS = {
     "zs_gather_assemble": ([_P, _I32, _P, _P, ctypes.c_int, _P, _P], ctypes.c_int),
     "zs_grad_norm_workspace_bytes": ([], _I64),
     "zs_grad_sqnorm": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _I64, _P, _P], ctypes.c_int),
+    "zs_grad_sqnorm_noalloc": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _P], ctypes.c_int),
     "zs_clip_coefficient": ([_P, _I32, ctypes.c_double, _P, _P, _P], ctypes.c_int),
     "zs_shard_step_clipped": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _P, _P, _P,
                                ctypes.c_int, ctypes.POINTER(AdamWHparams), _I64, _P, _P, _P],
@@ -260,6 +261,16 @@ def zs_grad_sqnorm(plan, rank, lo, hi, grad_slices, grad_dtype, workspace, sqnor
         else zs_grad_norm_workspace_bytes()
     _check(lib().zs_grad_sqnorm(plan.handle, rank, lo, hi, ptrs, grad_dtype, _ptr(workspace),
                                 nbytes, _ptr(sqnorm_out), _stream(stream)))
+
+
+def zs_grad_sqnorm_noalloc(plan, rank, lo, hi, grad_slices, grad_dtype, sqnorm_out,
+                           stream=None):
+    """``zs_grad_sqnorm`` for callers that cannot allocate device memory: the
+    scratch is the library's own static device array (see include/zs.h for
+    the first-call set-up and for why overlapping calls must not be issued)."""
+    ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
+    _check(lib().zs_grad_sqnorm_noalloc(plan.handle, rank, lo, hi, ptrs, grad_dtype,
+                                        _ptr(sqnorm_out), _stream(stream)))
 
 
 def zs_clip_coefficient(rank_sqnorms, n, max_norm, coef_out, nonfinite_out, stream=None):

@@ -315,6 +315,58 @@ extern "C" zs_status zs_grad_sqnorm(const zs_plan* plan, int32_t rank, int64_t l
   return ZS_OK;
 }
 
+extern "C" zs_status zs_grad_sqnorm_noalloc(const zs_plan* plan, int32_t rank, int64_t lo,
+                                            int64_t hi, const void* const* grad_slices,
+                                            zs_dtype grad_dtype, double* sqnorm_out,
+                                            void* cuda_stream) {
+  static const char* fn = "zs_grad_sqnorm_noalloc";
+  zs::clear_error();
+  if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
+  const int32_t N = plan->world;
+  const int64_t S = plan->S;
+  if (rank < 0 || rank >= N) return zs::fail(ZS_ERR_RANGE, "%s: rank %d not in [0, %d)", fn, rank, N);
+  if (lo < 0 || hi < lo || hi > S)
+    return zs::fail(ZS_ERR_RANGE, "%s: [lo, hi) = [%lld, %lld) not inside [0, %lld)", fn,
+                    (long long)lo, (long long)hi, (long long)S);
+  if (grad_dtype != ZS_BF16 && grad_dtype != ZS_FP32)
+    return zs::fail(ZS_ERR_INVAL, "%s: gradient dtype %d is not bf16 or fp32", fn, (int)grad_dtype);
+  // The scratch this call needs must fit the library's static array.
+  if (zs::kNormWorkspaceBytes > zs::kNoAllocScratchBytes)
+    return zs::fail(ZS_ERR_RANGE, "%s: needs %lld bytes of scratch, the static array holds %lld",
+                    fn, (long long)zs::kNormWorkspaceBytes, (long long)zs::kNoAllocScratchBytes);
+  if (zs_status st = check_device_scalar(sqnorm_out, 8, fn, "sqnorm_out")) return st;
+  if (hi > lo && !grad_slices) return zs::fail(ZS_ERR_INVAL, "%s: grad_slices is NULL", fn);
+  const int gb = grad_dtype == ZS_BF16 ? 2 : 4;
+  std::vector<Range> ranges;
+  bool all32 = true;
+  for (int32_t j = 0; j < N && hi > lo; ++j) {
+    const void* g = grad_slices[j];
+    if (!g) return zs::fail(ZS_ERR_INVAL, "%s: grad_slices[%d] is NULL", fn, j);
+    if (!aligned16(g)) return zs::fail(ZS_ERR_ALIGN, "%s: grad_slices[%d] is not 16-byte aligned", fn, j);
+    all32 = all32 && (uintptr_t)g % 32 == 0;
+    ranges.push_back({(uintptr_t)g, (uintptr_t)g + (uint64_t)S * gb, "grad_slices", j, false});
+  }
+  ranges.push_back({(uintptr_t)sqnorm_out, (uintptr_t)sqnorm_out + 8, "sqnorm_out", 0, true});
+  if (zs_status st = check_overlaps(ranges, fn)) return st;
+  for (int32_t j = 0; j < N && hi > lo; ++j)
+    if (zs_status st = check_device_buffer(grad_slices[j], S * gb, fn, "grad_slices", j)) return st;
+  zs::NormLaunch a;
+  a.grads = grad_slices;
+  a.world = N;
+  a.grad_dtype = grad_dtype;
+  a.lo = lo;
+  a.hi = hi;
+  a.vec = all32;
+  a.invN = (float)(1.0 / (double)N);
+  a.partials = nullptr;  // set to the static array by the launcher
+  a.ticket = nullptr;
+  a.out = sqnorm_out;
+  cudaError_t e = zs::launch_grad_sqnorm_noalloc(a, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess)
+    return zs::fail(ZS_ERR_CUDA, "%s: set-up or launch failed: %s", fn, cudaGetErrorString(e));
+  return ZS_OK;
+}
+
 extern "C" zs_status zs_clip_coefficient(const double* rank_sqnorms, int32_t n, double max_norm,
                                          float* coef_out, int32_t* nonfinite_out,
                                          void* cuda_stream) {

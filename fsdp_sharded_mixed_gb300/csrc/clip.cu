@@ -23,6 +23,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "zs_internal.h"
 
 namespace zs {
@@ -204,6 +206,45 @@ cudaError_t launch_clip_coef(const double* rank_sqnorms, int n, double max_norm,
                              int32_t* nonfinite, cudaStream_t stream) {
   clip_coef_kernel<<<1, 32, 0, stream>>>(rank_sqnorms, n, max_norm, coef, nonfinite);
   return cudaGetLastError();
+}
+
+}  // namespace zs
+
+// ---- The norm pass without caller scratch ------------------------------------
+// For callers that cannot allocate device memory, the scratch of one norm pass
+// (the 1024 block partials and the ticket word) also exists as a file-scope
+// device array. Every GPU that loads this library holds these 8448 bytes until
+// the process exits. All calls share it, so calls that overlap on the GPU
+// race; the ticket is cleared before each launch and the partials are written
+// before they are read, so nothing of an earlier call leaks into a later one.
+namespace zs {
+
+static __device__ __align__(256) unsigned char g_norm_scratch[kNoAllocScratchBytes];
+
+cudaError_t launch_grad_sqnorm_noalloc(const NormLaunch& in, cudaStream_t stream) {
+  // The array's device address, looked up once per device with that device
+  // current (the first call on a device does this set-up).
+  static std::mutex mu;
+  static void* addr_by_dev[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr_by_dev[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_norm_scratch);
+      if (e != cudaSuccess) return e;
+      addr_by_dev[dev] = p;
+    }
+    base = addr_by_dev[dev];
+  }
+  NormLaunch a = in;
+  a.partials = static_cast<double*>(base);
+  a.ticket = reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(base) + kNormTicketOffset);
+  return launch_grad_sqnorm(a, stream);
 }
 
 }  // namespace zs

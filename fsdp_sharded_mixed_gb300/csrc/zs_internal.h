@@ -81,6 +81,10 @@ struct NormLaunch {
   double* out;
 };
 cudaError_t launch_grad_sqnorm(const NormLaunch& a, cudaStream_t stream);
+// The same norm pass with its scratch in a file-scope device array of
+// kNoAllocScratchBytes (clip.cu); callers check kNormWorkspaceBytes fits.
+constexpr int64_t kNoAllocScratchBytes = 8448;
+cudaError_t launch_grad_sqnorm_noalloc(const NormLaunch& a, cudaStream_t stream);
 cudaError_t launch_clip_coef(const double* rank_sqnorms, int n, double max_norm, float* coef,
                              int32_t* nonfinite, cudaStream_t stream);
 

@@ -199,6 +199,28 @@ zs_status zs_grad_sqnorm(const zs_plan* plan, int32_t rank, int64_t lo, int64_t 
                          const void* const* grad_slices, zs_dtype grad_dtype, void* workspace,
                          int64_t workspace_bytes, double* sqnorm_out, void* cuda_stream);
 
+/* zs_grad_sqnorm for callers that cannot allocate device memory. The pages
+ * have no counterpart to this call; it exists for this library's users. Some
+ * callers cannot hand over scratch memory: code whose process has given the
+ * whole device to another allocator that it cannot reach (a plug-in inside a
+ * host application, say), or code that must still compute the gradient norm
+ * after the device has run out of memory, to decide whether to skip the step
+ * or to record why a rank is failing, when a cudaMalloc would itself fail.
+ * This variant keeps the norm pass's scratch (1024 fp64 partials and a ticket
+ * word, 8448 bytes, the most one call needs whatever the input size) in a
+ * static device array of the library, held on every GPU that loads it until
+ * the process exits; a call whose scratch would not fit is refused with
+ * ZS_ERR_RANGE. It calls no allocator. The caller still passes the inputs and
+ * the output, as for zs_grad_sqnorm, and gets the same value. The first call on
+ * a device looks the array up (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture. All calls share the one
+ * array: calls that overlap on the GPU (on different streams, or from several
+ * threads) race and must not be issued; calls in order on one stream are
+ * safe, each clearing what must start at zero. */
+zs_status zs_grad_sqnorm_noalloc(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                                 const void* const* grad_slices, zs_dtype grad_dtype,
+                                 double* sqnorm_out, void* cuda_stream);
+
 /* rank_sqnorms: device double [n], the ranks' partial sums (1 <= n <= 1024).
  * Writes the device fp32 *coef_out and the device int32 *nonfinite_out (1 when
  * the global norm is Inf or NaN; coef is then 1). max_norm: finite, > 0. */
