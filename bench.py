@@ -240,7 +240,6 @@ def workload_config(w, plan):
 
 
 def run_ours(args, w):
-    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -254,12 +253,16 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
+    Ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
     plan = zs.zs_flatten_plan(w.numels, w.tied_to, world=w.world, align_elems=w.align)
     N, S, P = plan.world, plan.S, plan.P
     r = emulated_rank(grank, N)
     hp = w.hparams
     bpe = bytes_per_elem(N)
+    clip = args.pipeline == "clip"
+    norm_bpe = 2 * N  # the norm pass reads the N bf16 slices once
+    pipe_bpe = bpe + (norm_bpe if clip else 0)
 
     # Inputs resident in HBM: one set of incoming slices, master from the
     # generator, zero moments, the full AllGather buffer.
@@ -275,15 +278,46 @@ def run_ours(args, w):
     m = torch.zeros(S, dtype=torch.float32, device=dev)
     v = torch.zeros(S, dtype=torch.float32, device=dev)
     full = torch.zeros(plan.P_pad, dtype=torch.int16, device=dev)
+
+    # Clipping: this rank's partial sum of squares, the N partials (the other
+    # ranks' as if every shard had this one's norm: the scalar AllReduce of a
+    # real system), the coefficient and skip flag, all on the device.
+    ws = parts = coef = bad = None
+    max_norm = 1.0
+    if clip:
+        ws = torch.empty(zs.zs_grad_norm_workspace_bytes(), dtype=torch.uint8, device=dev)
+        parts = torch.zeros(N, dtype=torch.float64, device=dev)
+        coef = torch.zeros(1, dtype=torch.float32, device=dev)
+        bad = torch.zeros(1, dtype=torch.int32, device=dev)
+        zs.zs_grad_sqnorm(plan, r, 0, S, grads, zs.ZS_BF16, ws, parts.narrow(0, r, 1),
+                          stream=sptr)
+        torch.cuda.synchronize()
+        own = float(parts[r].item())
+        parts.fill_(own)
+        max_norm = 0.5 * (N * own) ** 0.5  # so that the step really clips
     torch.cuda.synchronize()
 
     step_no = [0]
 
-    def step():
+    def step(sp=sptr, lo=0, hi=S, marks=None):
         step_no[0] += 1
-        zs.zs_shard_step(plan, r, 0, S, grads, zs.ZS_BF16, master, m, v, full, zs.ZS_BF16, hp,
-                         step_no[0], stream=sptr)
+        if clip:
+            if marks:
+                marks[0].record(torch.cuda.current_stream())
+            zs.zs_grad_sqnorm(plan, r, lo, hi, grads, zs.ZS_BF16, ws, parts.narrow(0, r, 1),
+                              stream=sp)
+            zs.zs_clip_coefficient(parts, N, max_norm, coef, bad, stream=sp)
+            if marks:
+                marks[1].record(torch.cuda.current_stream())
+            zs.zs_shard_step_clipped(plan, r, lo, hi, grads, zs.ZS_BF16, master, m, v, full,
+                                     zs.ZS_BF16, hp, step_no[0], coef=coef, skip=bad, stream=sp)
+            if marks:
+                marks[2].record(torch.cuda.current_stream())
+        else:
+            zs.zs_shard_step(plan, r, lo, hi, grads, zs.ZS_BF16, master, m, v, full,
+                             zs.ZS_BF16, hp, step_no[0], stream=sp)
 
+    launches_per_step = 3 if clip else 1
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -301,46 +335,57 @@ def run_ours(args, w):
         torch.cuda.synchronize()
 
     # The timed region: K steps back to back between two events on the
-    # launching stream (or one replay of a CUDA graph holding the K launches).
+    # launching stream (or one replay of a CUDA graph holding the K steps).
+    # For the clip pipeline, events also mark each step's kernels so each
+    # kernel's own average duration is known.
     graph = None
     if args.graph:
         graph = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         with torch.cuda.graph(graph, stream=side, capture_error_mode="relaxed"):
-            gptr = side.cuda_stream
             for _ in range(args.steps):
-                step_no[0] += 1
-                zs.zs_shard_step(plan, r, 0, S, grads, zs.ZS_BF16, master, m, v, full,
-                                 zs.ZS_BF16, hp, step_no[0], stream=gptr)
+                step(sp=side.cuda_stream)
         stream.wait_stream(side)
         graph.replay()  # one untimed replay
+    marks = [[Ev(), Ev(), Ev()] for _ in range(args.steps)] if (clip and graph is None) else None
     if gworld > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
+    t0, t1 = Ev(), Ev()
     t0.record(stream)
     if graph is not None:
         graph.replay()
     else:
-        for _ in range(args.steps):
-            step()
+        for k in range(args.steps):
+            step(marks=marks[k] if marks else None)
     t1.record(stream)
     torch.cuda.synchronize()
     if gworld > 1:
         dist.barrier()
     clocks = sampler.stop()
     elapsed = t0.elapsed_time(t1) / 1e3
-    launch_avg_s = elapsed / args.steps
+    if marks:
+        norm_s = sum(a.elapsed_time(b) for a, b, _ in marks) / 1e3 / args.steps
+        step_s = sum(b.elapsed_time(c) for _, b, c in marks) / 1e3 / args.steps
+    elif clip:
+        # A graph replay gives no per-kernel split: time each part in a
+        # separate pass of direct launches.
+        split = [[Ev(), Ev(), Ev()] for _ in range(min(args.steps, 50))]
+        for mk in split:
+            step(marks=mk)
+        torch.cuda.synchronize()
+        norm_s = sum(a.elapsed_time(b) for a, b, _ in split) / 1e3 / len(split)
+        step_s = sum(b.elapsed_time(c) for _, b, c in split) / 1e3 / len(split)
+    else:
+        norm_s, step_s = None, elapsed / args.steps
     t_max = max_over_ranks(elapsed, dev)
     elems_all = sum_over_ranks(float(S) * args.steps, dev)
     value = elems_all / t_max
 
     # Per-step spread, measured after the timed region (events around each step).
     n_spread = min(args.steps, 50)
-    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(n_spread)]
+    events = [(Ev(), Ev()) for _ in range(n_spread)]
     for a_ev, b_ev in events:
         a_ev.record(stream)
         step()
@@ -349,47 +394,87 @@ def run_ours(args, w):
     per_step = sorted(a_ev.elapsed_time(b_ev) for a_ev, b_ev in events)
 
     # End to end through the C ABI from pinned host memory: every step copies
-    # the N incoming slices host->device and reads the updated slot back.
+    # the N incoming slices host->device and reads the updated slot back. The
+    # shard goes in chunks through the [lo, hi) range of the call, so the copy
+    # of chunk c+1, the step on chunk c and the read-back of chunk c-1 overlap
+    # (how bucketed ReduceScatter output meets the optimizer in a real job).
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not clip:
         h_grads = [torch.empty(S, dtype=torch.int16, pin_memory=True) for _ in range(N)]
         for hg, g in zip(h_grads, grads):
             hg.copy_(g)
         h_out = torch.empty(S, dtype=torch.int16, pin_memory=True)
         slot = full.narrow(0, r * S, S)
+        nch = max(1, args.e2e_chunks)
+        bounds = [min(S, (S * c // nch) // 16 * 16) for c in range(nch)] + [S]
+        s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(nch)]
+        ev_cmp = [torch.cuda.Event() for _ in range(nch)]
+        ev_out = [torch.cuda.Event() for _ in range(nch)]
+        for c in range(nch):  # nothing outstanding yet
+            ev_cmp[c].record(stream)
+            ev_out[c].record(stream)
 
         def e2e_step():
-            for hg, g in zip(h_grads, grads):
-                g.copy_(hg, non_blocking=True)
-            step()
-            h_out.copy_(slot, non_blocking=True)
+            step_no[0] += 1
+            for c in range(nch):
+                lo, hi = bounds[c], bounds[c + 1]
+                if hi <= lo:
+                    continue
+                s_in.wait_event(ev_cmp[c])      # last step's kernel has read chunk c
+                with torch.cuda.stream(s_in):
+                    for hg, g in zip(h_grads, grads):
+                        g[lo:hi].copy_(hg[lo:hi], non_blocking=True)
+                ev_in[c].record(s_in)
+                s_cmp.wait_event(ev_in[c])
+                s_cmp.wait_event(ev_out[c])     # last step's read-back of chunk c is done
+                zs.zs_shard_step(plan, r, lo, hi, grads, zs.ZS_BF16, master, m, v, full,
+                                 zs.ZS_BF16, hp, step_no[0], stream=s_cmp.cuda_stream)
+                ev_cmp[c].record(s_cmp)
+                s_out.wait_event(ev_cmp[c])
+                with torch.cuda.stream(s_out):
+                    h_out[lo:hi].copy_(slot[lo:hi], non_blocking=True)
+                ev_out[c].record(s_out)
 
+        for s_ in (s_in, s_cmp, s_out):
+            s_.wait_stream(stream)
         e2e_step()
         torch.cuda.synchronize()
         if gworld > 1:
             dist.barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a, b = Ev(), Ev()
         a.record(stream)
+        for s_ in (s_in, s_cmp, s_out):
+            s_.wait_stream(stream)
         for _ in range(args.e2e_steps):
             e2e_step()
+        for s_ in (s_in, s_cmp, s_out):
+            stream.wait_stream(s_)
         b.record(stream)
         torch.cuda.synchronize()
         e2e_t = max_over_ranks(a.elapsed_time(b) / 1e3, dev)
         e2e_elems = sum_over_ranks(float(S) * args.e2e_steps, dev)
         e2e = {"value": e2e_elems / e2e_t, "unit": UNIT, "h2d_bytes_per_step": 2 * N * S,
                "d2h_bytes_per_step": 2 * S, "steps": args.e2e_steps,
-               "ms_per_step": 1e3 * e2e_t / args.e2e_steps}
+               "ms_per_step": 1e3 * e2e_t / args.e2e_steps, "chunks": nch,
+               "h2d_gbs": 2 * N * S * args.e2e_steps / e2e_t / 1e9}
         del h_grads, h_out
 
     if grank == 0:
         peak, peak_kind = measured_peak()
-        achieved = bpe * S / launch_avg_s / 1e9
+        achieved = bpe * S / step_s / 1e9
         traffic_pe = committed_traffic(w.key)
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "peak_source": peak_kind,
                     "traffic": None if traffic_pe is None else traffic_pe * S,
                     "algorithmic_bytes": bpe * S, "kernel": "shard_step_kernel",
                     "kernel_sha": kernel_sha()}
+        kernels = {"shard_step_kernel": {"ms": 1e3 * step_s, "gbs": achieved,
+                                         "frac": achieved / peak}}
+        if norm_s is not None:
+            g = norm_bpe * S / norm_s / 1e9
+            kernels["grad_sqnorm_kernel+clip_coef_kernel"] = {"ms": 1e3 * norm_s, "gbs": g,
+                                                              "frac": g / peak}
         cpu = None
         if not args.no_cpu_baseline and gworld == 1:
             rate, secs, cores, n = oracle_sample_rate(w, S, P, r, args.cpu_sample_elems,
@@ -403,17 +488,19 @@ def run_ours(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": dict(workload_config(w, plan),
                                                 parallelism=f"replicas{gworld}",
-                                                emulated_rank_gpu0=r),
-            "hbm_gbs": bpe * value / gworld / 1e9,
+                                                emulated_rank_gpu0=r, pipeline=args.pipeline),
+            "hbm_gbs": pipe_bpe * value / gworld / 1e9,
             "step_ms": {"median": statistics.median(per_step),
                         "p10": per_step[len(per_step) // 10],
                         "p90": per_step[(9 * len(per_step)) // 10],
                         "note": f"{n_spread} steps with events around each, after the timed region"},
             "timing": "cuda graph replay of the K steps" if graph is not None
                       else "K direct launches between two events",
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps, "clocks": clocks,
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
         }
+        if clip:
+            line["config"]["clip_max_norm"] = max_norm
         print(json.dumps(line), flush=True)
     del grads, master, m, v, full
     plan.free()
@@ -431,7 +518,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--graph", action="store_true",
                     help="time one replay of a CUDA graph holding the K launches")
+    ap.add_argument("--pipeline", choices=["step", "clip"], default="step",
+                    help="step: the fused shard step; clip: global-norm pass + clip "
+                         "coefficient + clipped step")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-chunks", type=int, default=16)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-elems", type=int, default=32 * 1024 * 1024)

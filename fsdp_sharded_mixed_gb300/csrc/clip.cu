@@ -16,10 +16,12 @@
 // formed in fp32 with their exact rounding residue (an FMA), summed per
 // 16-element group with a compensated (two-sum) fp32 accumulator, and folded
 // into a per-thread double; double work is one add per group, because GB300's
-// fp64 rate is far below its fp32 rate. The grid is a fixed 1024 blocks, each
-// block's partial goes to scratch memory, and the last block to finish adds
-// the partials in block order: the result does not depend on timing and is
-// the same on every run.
+// fp64 rate is far below its fp32 rate. A batch of slices is loaded before it
+// is summed, so its loads are in flight together. The grid is a fixed 1216
+// blocks (8 per SM of a 152-SM GB300: whole waves at 1, 2, 4 or 8 resident
+// blocks per SM); each block's partial goes to scratch memory and the last
+// block to finish adds the partials in block order: the result does not depend
+// on timing or on the GPU, and is the same on every run.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -79,7 +81,7 @@ __device__ __forceinline__ float mean_grad(const NormArgs<MAXN>& a, int64_t i) {
 // VEC: 16-element groups with 32-byte loads (all slices 32-byte aligned);
 // otherwise element by element.
 template <bool BF16G, bool VEC, int MAXN>
-__global__ void __launch_bounds__(kThreads) grad_sqnorm_kernel(const __grid_constant__ NormArgs<MAXN> a) {
+__global__ void __launch_bounds__(kThreads, 2) grad_sqnorm_kernel(const __grid_constant__ NormArgs<MAXN> a) {
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   double sum = 0.0;
@@ -104,24 +106,36 @@ __global__ void __launch_bounds__(kThreads) grad_sqnorm_kernel(const __grid_cons
       acc_square(g, s, c);
       sum += (double)s + (double)c;
     }
-    constexpr int W = BF16G ? kGW / 2 : kGW;
+    constexpr int W = BF16G ? kGW / 2 : kGW;          // 32-bit words per slice per group
+    constexpr int KB = 64 / W;                        // slices loaded back to back
     constexpr int kStride = BF16G ? 2 * kGW : 4 * kGW;
     for (int64_t g = g0 + tid; g < g1; g += stride) {
       float acc[kGW];
 #pragma unroll
       for (int k = 0; k < kGW; ++k) acc[k] = 0.0f;
-      for (int j = 0; j < a.world; ++j) {
-        uint32_t raw[W];
-        const unsigned char* base = static_cast<const unsigned char*>(a.grads[j]) + g * kStride;
-        ld32_nc(base, raw);
-        if (!BF16G) ld32_nc(base + 32, raw + 8);
+      for (int j0 = 0; j0 < a.world; j0 += KB) {
+        uint32_t raw[KB][W];
 #pragma unroll
-        for (int k = 0; k < W; ++k) {
-          if (BF16G) {
-            acc[2 * k] = __fadd_rn(acc[2 * k], __uint_as_float(raw[k] << 16));
-            acc[2 * k + 1] = __fadd_rn(acc[2 * k + 1], __uint_as_float(raw[k] & 0xFFFF0000u));
-          } else {
-            acc[k] = __fadd_rn(acc[k], __uint_as_float(raw[k]));
+        for (int b = 0; b < KB; ++b) {
+          if (j0 + b < a.world) {
+            const unsigned char* base =
+                static_cast<const unsigned char*>(a.grads[j0 + b]) + g * kStride;
+            ld32_nc(base, raw[b]);
+            if (!BF16G) ld32_nc(base + 32, raw[b] + 8);
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < KB; ++b) {
+          if (j0 + b < a.world) {
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+              if (BF16G) {
+                acc[2 * k] = __fadd_rn(acc[2 * k], __uint_as_float(raw[b][k] << 16));
+                acc[2 * k + 1] = __fadd_rn(acc[2 * k + 1], __uint_as_float(raw[b][k] & 0xFFFF0000u));
+              } else {
+                acc[k] = __fadd_rn(acc[k], __uint_as_float(raw[b][k]));
+              }
+            }
           }
         }
       }
@@ -212,8 +226,8 @@ cudaError_t launch_clip_coef(const double* rank_sqnorms, int n, double max_norm,
 
 // ---- The norm pass without caller scratch ------------------------------------
 // For callers that cannot allocate device memory, the scratch of one norm pass
-// (the 1024 block partials and the ticket word) also exists as a file-scope
-// device array. Every GPU that loads this library holds these 8448 bytes until
+// (the 1216 block partials and the ticket word) also exists as a file-scope
+// device array. Every GPU that loads this library holds these 9984 bytes until
 // the process exits. All calls share it, so calls that overlap on the GPU
 // race; the ticket is cleared before each launch and the partials are written
 // before they are read, so nothing of an earlier call leaks into a later one.

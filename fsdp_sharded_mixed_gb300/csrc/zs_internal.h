@@ -66,7 +66,7 @@ cudaError_t launch_gather(const GatherLaunch& a, cudaStream_t stream);
 
 // Global-norm pass (clip.cu): per-block partial sums of squares in scratch
 // memory, reduced in block order by the last block.
-constexpr int kNormPartials = 1024;
+constexpr int kNormPartials = 1216;  // 8 x 152 SMs
 constexpr int64_t kNormTicketOffset = kNormPartials * 8;   // bytes
 constexpr int64_t kNormWorkspaceBytes = kNormTicketOffset + 256;
 struct NormLaunch {
@@ -83,7 +83,7 @@ struct NormLaunch {
 cudaError_t launch_grad_sqnorm(const NormLaunch& a, cudaStream_t stream);
 // The same norm pass with its scratch in a file-scope device array of
 // kNoAllocScratchBytes (clip.cu); callers check kNormWorkspaceBytes fits.
-constexpr int64_t kNoAllocScratchBytes = 8448;
+constexpr int64_t kNoAllocScratchBytes = 9984;
 cudaError_t launch_grad_sqnorm_noalloc(const NormLaunch& a, cudaStream_t stream);
 cudaError_t launch_clip_coef(const double* rank_sqnorms, int n, double max_norm, float* coef,
                              int32_t* nonfinite, cudaStream_t stream);

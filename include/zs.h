@@ -183,14 +183,14 @@ zs_status zs_gather_assemble(const zs_plan* plan, int32_t rank, const void* cons
  * Nothing returns to the host in between.
  * ------------------------------------------------------------------------- */
 
-/* Bytes of scratch device memory zs_grad_sqnorm needs (1024 fp64 block
- * partials and a ticket word; 8448). The caller allocates and owns it. */
+/* Bytes of scratch device memory zs_grad_sqnorm needs (1216 fp64 block
+ * partials and a ticket word; 9984). The caller allocates and owns it. */
 int64_t zs_grad_norm_workspace_bytes(void);
 
 /* Sum over shard-local i in [lo, hi) of g_i^2, g_i the step's fp32 mean of the
  * N slices (same order and rounding as zs_shard_step), each square exact and
  * the sum carried in double; written to the device double *sqnorm_out. The
- * sum is reduced over a fixed 1024-block grid in a fixed order, so it is the
+ * sum is reduced over a fixed 1216-block grid in a fixed order, so it is the
  * same on every run (it may differ from a sequential sum in the last bits).
  * workspace: 16-byte aligned device scratch of at least
  * zs_grad_norm_workspace_bytes() bytes, used by one call at a time. Errors as
@@ -206,8 +206,8 @@ zs_status zs_grad_sqnorm(const zs_plan* plan, int32_t rank, int64_t lo, int64_t 
  * host application, say), or code that must still compute the gradient norm
  * after the device has run out of memory, to decide whether to skip the step
  * or to record why a rank is failing, when a cudaMalloc would itself fail.
- * This variant keeps the norm pass's scratch (1024 fp64 partials and a ticket
- * word, 8448 bytes, the most one call needs whatever the input size) in a
+ * This variant keeps the norm pass's scratch (1216 fp64 partials and a ticket
+ * word, 9984 bytes, the most one call needs whatever the input size) in a
  * static device array of the library, held on every GPU that loads it until
  * the process exits; a call whose scratch would not fit is refused with
  * ZS_ERR_RANGE. It calls no allocator. The caller still passes the inputs and
