@@ -260,9 +260,10 @@ def run_ours(args, w):
     r = emulated_rank(grank, N)
     hp = w.hparams
     bpe = bytes_per_elem(N)
-    clip = args.pipeline == "clip"
     norm_bpe = 2 * N  # the norm pass reads the N bf16 slices once
-    pipe_bpe = bpe + (norm_bpe if clip else 0)
+    clip = args.pipeline == "clip"
+    accum_mode = args.pipeline == "accum"
+    G = max(1, args.micro_steps)
 
     # Inputs resident in HBM: one set of incoming slices, master from the
     # generator, zero moments, the full AllGather buffer.
@@ -282,7 +283,7 @@ def run_ours(args, w):
     # Clipping: this rank's partial sum of squares, the N partials (the other
     # ranks' as if every shard had this one's norm: the scalar AllReduce of a
     # real system), the coefficient and skip flag, all on the device.
-    ws = parts = coef = bad = None
+    ws = parts = coef = bad = acc_buf = None
     max_norm = 1.0
     if clip:
         ws = torch.empty(zs.zs_grad_norm_workspace_bytes(), dtype=torch.uint8, device=dev)
@@ -295,29 +296,57 @@ def run_ours(args, w):
         own = float(parts[r].item())
         parts.fill_(own)
         max_norm = 0.5 * (N * own) ** 0.5  # so that the step really clips
+    if accum_mode:
+        acc_buf = torch.zeros(S, dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
 
     step_no = [0]
 
-    def step(sp=sptr, lo=0, hi=S, marks=None):
-        step_no[0] += 1
-        if clip:
-            if marks:
-                marks[0].record(torch.cuda.current_stream())
-            zs.zs_grad_sqnorm(plan, r, lo, hi, grads, zs.ZS_BF16, ws, parts.narrow(0, r, 1),
-                              stream=sp)
-            zs.zs_clip_coefficient(parts, N, max_norm, coef, bad, stream=sp)
-            if marks:
-                marks[1].record(torch.cuda.current_stream())
-            zs.zs_shard_step_clipped(plan, r, lo, hi, grads, zs.ZS_BF16, master, m, v, full,
-                                     zs.ZS_BF16, hp, step_no[0], coef=coef, skip=bad, stream=sp)
-            if marks:
-                marks[2].record(torch.cuda.current_stream())
-        else:
-            zs.zs_shard_step(plan, r, lo, hi, grads, zs.ZS_BF16, master, m, v, full,
-                             zs.ZS_BF16, hp, step_no[0], stream=sp)
+    # The parts of one optimizer step: (name, enqueue(stream), algorithmic bytes/elem).
+    def part_step(sp):
+        zs.zs_shard_step(plan, r, 0, S, grads, zs.ZS_BF16, master, m, v, full, zs.ZS_BF16, hp,
+                         step_no[0], stream=sp)
 
-    launches_per_step = 3 if clip else 1
+    def part_norm(sp):
+        zs.zs_grad_sqnorm(plan, r, 0, S, grads, zs.ZS_BF16, ws, parts.narrow(0, r, 1), stream=sp)
+        zs.zs_clip_coefficient(parts, N, max_norm, coef, bad, stream=sp)
+
+    def part_clipped(sp):
+        zs.zs_shard_step_clipped(plan, r, 0, S, grads, zs.ZS_BF16, master, m, v, full,
+                                 zs.ZS_BF16, hp, step_no[0], coef=coef, skip=bad, stream=sp)
+
+    def part_accumulate(sp):
+        for k in range(G - 1):
+            zs.zs_grad_accumulate(plan, r, 0, S, grads, zs.ZS_BF16, acc_buf, k == 0, stream=sp)
+
+    def part_accumulated(sp):
+        zs.zs_shard_step_accumulated(plan, r, 0, S, grads, zs.ZS_BF16, acc_buf, G, master, m, v,
+                                     full, zs.ZS_BF16, hp, step_no[0], stream=sp)
+
+    if clip:
+        pipeline = [("grad_sqnorm_kernel+clip_coef_kernel", part_norm, norm_bpe),
+                    ("shard_step_kernel", part_clipped, bpe)]
+        launches_per_step = 3
+    elif accum_mode:
+        acc_bytes = (2 * N + 4) + (G - 2) * (2 * N + 8) if G > 1 else 0
+        pipeline = ([("accumulate_kernel", part_accumulate, acc_bytes)] if G > 1 else []) + \
+                   [("shard_step_kernel", part_accumulated, bpe + 4)]
+        launches_per_step = G
+    else:
+        pipeline = [("shard_step_kernel", part_step, bpe)]
+        launches_per_step = 1
+    pipe_bpe = sum(b for _, _, b in pipeline)
+
+    def step(sp=sptr, marks=None):
+        step_no[0] += 1
+        cur = torch.cuda.current_stream()
+        for k, (_, fn, _) in enumerate(pipeline):
+            if marks:
+                marks[k].record(cur)
+            fn(sp)
+        if marks:
+            marks[-1].record(cur)
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -348,7 +377,10 @@ def run_ours(args, w):
                 step(sp=side.cuda_stream)
         stream.wait_stream(side)
         graph.replay()  # one untimed replay
-    marks = [[Ev(), Ev(), Ev()] for _ in range(args.steps)] if (clip and graph is None) else None
+    multi = len(pipeline) > 1
+    nmk = len(pipeline) + 1
+    marks = [[Ev() for _ in range(nmk)] for _ in range(args.steps)] if (multi and graph is None) \
+        else None
     if gworld > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -365,20 +397,19 @@ def run_ours(args, w):
         dist.barrier()
     clocks = sampler.stop()
     elapsed = t0.elapsed_time(t1) / 1e3
-    if marks:
-        norm_s = sum(a.elapsed_time(b) for a, b, _ in marks) / 1e3 / args.steps
-        step_s = sum(b.elapsed_time(c) for _, b, c in marks) / 1e3 / args.steps
-    elif clip:
-        # A graph replay gives no per-kernel split: time each part in a
-        # separate pass of direct launches.
-        split = [[Ev(), Ev(), Ev()] for _ in range(min(args.steps, 50))]
-        for mk in split:
+    if multi and marks is None:
+        # A graph replay gives no per-part split: time each part in a separate
+        # pass of direct launches.
+        marks = [[Ev() for _ in range(nmk)] for _ in range(min(args.steps, 50))]
+        for mk in marks:
             step(marks=mk)
         torch.cuda.synchronize()
-        norm_s = sum(a.elapsed_time(b) for a, b, _ in split) / 1e3 / len(split)
-        step_s = sum(b.elapsed_time(c) for _, b, c in split) / 1e3 / len(split)
+    if multi:
+        part_s = [sum(mk[k].elapsed_time(mk[k + 1]) for mk in marks) / 1e3 / len(marks)
+                  for k in range(len(pipeline))]
     else:
-        norm_s, step_s = None, elapsed / args.steps
+        part_s = [elapsed / args.steps]
+    step_s = part_s[-1]
     t_max = max_over_ranks(elapsed, dev)
     elems_all = sum_over_ranks(float(S) * args.steps, dev)
     value = elems_all / t_max
@@ -399,7 +430,7 @@ def run_ours(args, w):
     # of chunk c+1, the step on chunk c and the read-back of chunk c-1 overlap
     # (how bucketed ReduceScatter output meets the optimizer in a real job).
     e2e = None
-    if not args.no_e2e and not clip:
+    if not args.no_e2e and args.pipeline == "step":
         h_grads = [torch.empty(S, dtype=torch.int16, pin_memory=True) for _ in range(N)]
         for hg, g in zip(h_grads, grads):
             hg.copy_(g)
@@ -462,19 +493,19 @@ def run_ours(args, w):
 
     if grank == 0:
         peak, peak_kind = measured_peak()
-        achieved = bpe * S / step_s / 1e9
+        step_bpe = pipeline[-1][2]
+        achieved = step_bpe * S / step_s / 1e9
         traffic_pe = committed_traffic(w.key)
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "peak_source": peak_kind,
                     "traffic": None if traffic_pe is None else traffic_pe * S,
-                    "algorithmic_bytes": bpe * S, "kernel": "shard_step_kernel",
+                    "algorithmic_bytes": step_bpe * S, "kernel": "shard_step_kernel",
                     "kernel_sha": kernel_sha()}
-        kernels = {"shard_step_kernel": {"ms": 1e3 * step_s, "gbs": achieved,
-                                         "frac": achieved / peak}}
-        if norm_s is not None:
-            g = norm_bpe * S / norm_s / 1e9
-            kernels["grad_sqnorm_kernel+clip_coef_kernel"] = {"ms": 1e3 * norm_s, "gbs": g,
-                                                              "frac": g / peak}
+        kernels = {}
+        for (name, _, b), t in zip(pipeline, part_s):
+            gbs = b * S / t / 1e9
+            kernels[name] = {"ms": 1e3 * t, "gbs": gbs, "frac": gbs / peak,
+                             "bytes_per_elem": b}
         cpu = None
         if not args.no_cpu_baseline and gworld == 1:
             rate, secs, cores, n = oracle_sample_rate(w, S, P, r, args.cpu_sample_elems,
@@ -501,6 +532,8 @@ def run_ours(args, w):
         }
         if clip:
             line["config"]["clip_max_norm"] = max_norm
+        if accum_mode:
+            line["config"]["micro_steps"] = G
         print(json.dumps(line), flush=True)
     del grads, master, m, v, full
     plan.free()
@@ -518,9 +551,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--graph", action="store_true",
                     help="time one replay of a CUDA graph holding the K launches")
-    ap.add_argument("--pipeline", choices=["step", "clip"], default="step",
+    ap.add_argument("--pipeline", choices=["step", "clip", "accum"], default="step",
                     help="step: the fused shard step; clip: global-norm pass + clip "
-                         "coefficient + clipped step")
+                         "coefficient + clipped step; accum: G-1 accumulations + the "
+                         "accumulated step")
+    ap.add_argument("--micro-steps", type=int, default=4,
+                    help="G, micro-batches per optimizer step for --pipeline accum")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-chunks", type=int, default=16)
     ap.add_argument("--no-e2e", action="store_true")

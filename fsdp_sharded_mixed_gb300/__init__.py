@@ -34,7 +34,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-fmad=false", "-prec-div=true",
               "-prec-sqrt=true", "-ftz=false", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-I/usr/local/cuda/include"]
-CUDA_SOURCES = ["shard_step.cu", "gather.cu", "clip.cu"]
+CUDA_SOURCES = ["shard_step.cu", "gather.cu", "clip.cu", "accum.cu"]
 HOST_SOURCES = ["api.cpp", "plan.cpp"]
 
 
@@ -111,6 +111,10 @@ EXPORTS = {
     "zs_shard_step_clipped": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _P, _P, _P,
                                ctypes.c_int, ctypes.POINTER(AdamWHparams), _I64, _P, _P, _P],
                               ctypes.c_int),
+    "zs_grad_accumulate": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _I32, _P], ctypes.c_int),
+    "zs_shard_step_accumulated": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _I32, _P, _P, _P,
+                                   _P, ctypes.c_int, ctypes.POINTER(AdamWHparams), _I64, _P],
+                                  ctypes.c_int),
     "zs_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "zs_last_error": ([], ctypes.c_char_p),
     "zs_check_device_error": ([_P], ctypes.c_int),
@@ -246,6 +250,25 @@ def zs_shard_step_clipped(plan, rank, lo, hi, grad_slices, grad_dtype, master, e
                                        _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(full_flat),
                                        param_dtype, ctypes.byref(h), step, _ptr(coef),
                                        _ptr(skip), _stream(stream)))
+
+
+def zs_grad_accumulate(plan, rank, lo, hi, grad_slices, grad_dtype, accum, first, stream=None):
+    """Enqueue accum = (first ? 0 : accum) + mean of the slices (fp32 [S])."""
+    ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
+    _check(lib().zs_grad_accumulate(plan.handle, rank, lo, hi, ptrs, grad_dtype, _ptr(accum),
+                                    1 if first else 0, _stream(stream)))
+
+
+def zs_shard_step_accumulated(plan, rank, lo, hi, grad_slices, grad_dtype, accum, micro_steps,
+                              master, exp_avg, exp_avg_sq, full_flat, param_dtype, hp, step,
+                              stream=None):
+    """The step on ((accum + mean of the slices) / micro_steps)."""
+    ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
+    h = AdamWHparams(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"])
+    _check(lib().zs_shard_step_accumulated(plan.handle, rank, lo, hi, ptrs, grad_dtype,
+                                           _ptr(accum), micro_steps, _ptr(master),
+                                           _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(full_flat),
+                                           param_dtype, ctypes.byref(h), step, _stream(stream)))
 
 
 def zs_grad_norm_workspace_bytes():

@@ -132,7 +132,8 @@ zs_status shard_step_impl(const char* fn, const zs_plan* plan, int32_t rank, int
                           int64_t hi, const void* const* grad_slices, zs_dtype grad_dtype,
                           float* master, float* exp_avg, float* exp_avg_sq, void* full_flat,
                           zs_dtype param_dtype, const zs_adamw_hparams* hp, int64_t step,
-                          const float* coef, const int32_t* skip, void* cuda_stream) {
+                          const float* coef, const int32_t* skip, const float* accum,
+                          int32_t micro_steps, void* cuda_stream) {
   zs::clear_error();
   if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
   const int32_t N = plan->world;
@@ -172,11 +173,17 @@ zs_status shard_step_impl(const char* fn, const zs_plan* plan, int32_t rank, int
     if (!aligned16(outs[k])) return zs::fail(ZS_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, names[k]);
     ranges.push_back({(uintptr_t)outs[k], (uintptr_t)outs[k] + (uint64_t)out_bytes[k], names[k], 0, true});
   }
+  if (accum) {
+    if (!aligned16(accum)) return zs::fail(ZS_ERR_ALIGN, "%s: accum is not 16-byte aligned", fn);
+    ranges.push_back({(uintptr_t)accum, (uintptr_t)accum + (uint64_t)S * 4, "accum", 0, false});
+  }
   if (zs_status st = check_overlaps(ranges, fn)) return st;
   for (int32_t j = 0; j < N; ++j)
     if (zs_status st = check_device_buffer(grad_slices[j], S * gb, fn, "grad_slices", j)) return st;
   for (int k = 0; k < 4; ++k)
     if (zs_status st = check_device_buffer(outs[k], out_bytes[k], fn, names[k], 0)) return st;
+  if (accum)
+    if (zs_status st = check_device_buffer(accum, S * 4, fn, "accum", 0)) return st;
 
   zs::ShardStepLaunch a;
   a.grads = grad_slices;
@@ -192,7 +199,8 @@ zs_status shard_step_impl(const char* fn, const zs_plan* plan, int32_t rank, int
   // The widest vector path every pointer allows: 32-byte accesses need all
   // bases (and the slot's 16-element groups) 32-byte aligned; 16-byte
   // accesses need the slot's 8-element groups aligned; else element by element.
-  bool all32 = ((uintptr_t)master | (uintptr_t)exp_avg | (uintptr_t)exp_avg_sq) % 32 == 0;
+  bool all32 = ((uintptr_t)master | (uintptr_t)exp_avg | (uintptr_t)exp_avg_sq |
+                (uintptr_t)accum) % 32 == 0;
   for (int32_t j = 0; j < N && all32; ++j) all32 = (uintptr_t)grad_slices[j] % 32 == 0;
   const uintptr_t slot_addr = (uintptr_t)a.slot;
   if (all32 && slot_addr % (pb == 3 ? 16u : 32u) == 0)
@@ -213,7 +221,10 @@ zs_status shard_step_impl(const char* fn, const zs_plan* plan, int32_t rank, int
   a.s.invN = (float)(1.0 / (double)N);
   a.coef = coef;
   a.skip = skip;
-  cudaError_t e = zs::launch_shard_step(a, static_cast<cudaStream_t>(cuda_stream));
+  a.accum = accum;
+  a.invG = (float)(1.0 / (double)(micro_steps > 0 ? micro_steps : 1));
+  cudaError_t e = accum ? zs::launch_shard_step_accumulated(a, static_cast<cudaStream_t>(cuda_stream))
+                        : zs::launch_shard_step(a, static_cast<cudaStream_t>(cuda_stream));
   if (e != cudaSuccess)
     return zs::fail(ZS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return ZS_OK;
@@ -237,7 +248,7 @@ extern "C" zs_status zs_shard_step(const zs_plan* plan, int32_t rank, int64_t lo
                                    void* cuda_stream) {
   return shard_step_impl("zs_shard_step", plan, rank, lo, hi, grad_slices, grad_dtype, master,
                          exp_avg, exp_avg_sq, full_flat, param_dtype, hp, step, nullptr, nullptr,
-                         cuda_stream);
+                         nullptr, 1, cuda_stream);
 }
 
 extern "C" zs_status zs_shard_step_clipped(const zs_plan* plan, int32_t rank, int64_t lo,
@@ -254,7 +265,77 @@ extern "C" zs_status zs_shard_step_clipped(const zs_plan* plan, int32_t rank, in
   if (skip)
     if (zs_status st = check_device_scalar(skip, 4, fn, "skip")) return st;
   return shard_step_impl(fn, plan, rank, lo, hi, grad_slices, grad_dtype, master, exp_avg,
-                         exp_avg_sq, full_flat, param_dtype, hp, step, coef, skip, cuda_stream);
+                         exp_avg_sq, full_flat, param_dtype, hp, step, coef, skip, nullptr, 1,
+                         cuda_stream);
+}
+
+extern "C" zs_status zs_shard_step_accumulated(const zs_plan* plan, int32_t rank, int64_t lo,
+                                               int64_t hi, const void* const* grad_slices,
+                                               zs_dtype grad_dtype, const float* accum,
+                                               int32_t micro_steps, float* master,
+                                               float* exp_avg, float* exp_avg_sq,
+                                               void* full_flat, zs_dtype param_dtype,
+                                               const zs_adamw_hparams* hp, int64_t step,
+                                               void* cuda_stream) {
+  static const char* fn = "zs_shard_step_accumulated";
+  zs::clear_error();
+  if (micro_steps < 1)
+    return zs::fail(ZS_ERR_RANGE, "%s: micro_steps %d < 1", fn, micro_steps);
+  if (!accum && hi > lo) return zs::fail(ZS_ERR_INVAL, "%s: accum is NULL", fn);
+  return shard_step_impl(fn, plan, rank, lo, hi, grad_slices, grad_dtype, master, exp_avg,
+                         exp_avg_sq, full_flat, param_dtype, hp, step, nullptr, nullptr, accum,
+                         micro_steps, cuda_stream);
+}
+
+extern "C" zs_status zs_grad_accumulate(const zs_plan* plan, int32_t rank, int64_t lo,
+                                        int64_t hi, const void* const* grad_slices,
+                                        zs_dtype grad_dtype, float* accum, int32_t first,
+                                        void* cuda_stream) {
+  static const char* fn = "zs_grad_accumulate";
+  zs::clear_error();
+  if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
+  const int32_t N = plan->world;
+  const int64_t S = plan->S;
+  if (rank < 0 || rank >= N) return zs::fail(ZS_ERR_RANGE, "%s: rank %d not in [0, %d)", fn, rank, N);
+  if (lo < 0 || hi < lo || hi > S)
+    return zs::fail(ZS_ERR_RANGE, "%s: [lo, hi) = [%lld, %lld) not inside [0, %lld)", fn,
+                    (long long)lo, (long long)hi, (long long)S);
+  if (grad_dtype != ZS_BF16 && grad_dtype != ZS_FP32)
+    return zs::fail(ZS_ERR_INVAL, "%s: gradient dtype %d is not bf16 or fp32", fn, (int)grad_dtype);
+  if (lo == hi) return ZS_OK;
+  if (!grad_slices || !accum) return zs::fail(ZS_ERR_INVAL, "%s: NULL buffer", fn);
+  if (!aligned16(accum)) return zs::fail(ZS_ERR_ALIGN, "%s: accum is not 16-byte aligned", fn);
+  const int gb = grad_dtype == ZS_BF16 ? 2 : 4;
+  std::vector<Range> ranges;
+  bool all32 = (uintptr_t)accum % 32 == 0;
+  for (int32_t j = 0; j < N; ++j) {
+    const void* g = grad_slices[j];
+    if (!g) return zs::fail(ZS_ERR_INVAL, "%s: grad_slices[%d] is NULL", fn, j);
+    if (!aligned16(g)) return zs::fail(ZS_ERR_ALIGN, "%s: grad_slices[%d] is not 16-byte aligned", fn, j);
+    all32 = all32 && (uintptr_t)g % 32 == 0;
+    ranges.push_back({(uintptr_t)g, (uintptr_t)g + (uint64_t)S * gb, "grad_slices", j, false});
+  }
+  ranges.push_back({(uintptr_t)accum, (uintptr_t)accum + (uint64_t)S * 4, "accum", 0, true});
+  if (zs_status st = check_overlaps(ranges, fn)) return st;
+  for (int32_t j = 0; j < N; ++j)
+    if (zs_status st = check_device_buffer(grad_slices[j], S * gb, fn, "grad_slices", j)) return st;
+  if (zs_status st = check_device_buffer(accum, S * 4, fn, "accum", 0)) return st;
+  zs::ShardStepLaunch a = {};
+  a.grads = grad_slices;
+  a.world = N;
+  a.grad_dtype = grad_dtype;
+  a.param_dtype = ZS_BF16;
+  a.lo = lo;
+  a.hi = hi;
+  a.vec_width = all32 ? 16 : 8;
+  a.accum = accum;
+  a.invG = 1.0f;
+  a.s.invN = (float)(1.0 / (double)N);
+  cudaError_t e = zs::launch_grad_accumulate(a, first ? 1 : 0,
+                                             static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess)
+    return zs::fail(ZS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return ZS_OK;
 }
 
 extern "C" int64_t zs_grad_norm_workspace_bytes(void) { return zs::kNormWorkspaceBytes; }

@@ -52,9 +52,15 @@ struct ShardStepLaunch {
                         // 8 (16-byte accesses) or 0 (element by element)
   const float* coef;    // device fp32 clip coefficient, or NULL (no clipping)
   const int32_t* skip;  // device flag: non-zero leaves every buffer as it is, or NULL
+  const float* accum;   // fp32 [S] micro-step accumulator (accumulation kernels), or NULL
+  float invG;           // fp32(1/G) for the accumulated step
   StepScalars s;
 };
 cudaError_t launch_shard_step(const ShardStepLaunch& a, cudaStream_t stream);
+// Gradient accumulation (accum.cu): accum = (first ? 0 : accum) + mean, and the
+// step on ((accum + mean) * invG).
+cudaError_t launch_grad_accumulate(const ShardStepLaunch& a, int first, cudaStream_t stream);
+cudaError_t launch_shard_step_accumulated(const ShardStepLaunch& a, cudaStream_t stream);
 
 struct GatherLaunch {
   const unsigned char* const* srcs;  // host array of N pointers (NULL = skip)

@@ -238,7 +238,40 @@ zs_status zs_shard_step_clipped(const zs_plan* plan, int32_t rank, int64_t lo, i
                                 const zs_adamw_hparams* hp, int64_t step, const float* coef,
                                 const int32_t* skip, void* cuda_stream);
 
-/* Diagnostics. */
+/* ---------------------------------------------------------------------------
+ * Gradient accumulation on the shard (G micro-batches per optimizer step).
+ * [DP-to-ZeRO] "Gradient Accumulation 会改变生命周期": whether each micro-step
+ * ReduceScatters, whether to accumulate on the shard or the full tensor, and
+ * whether the loss is divided by G must be decided; [Dissection] §7 (gradient
+ * accumulation). Reading: every micro-step ReduceScatters (ZeRO-2/3: no rank
+ * holds a full gradient); the mean of the micro-step's N slices is added into
+ * an fp32 accumulator of the shard; the last micro-step's slices go straight
+ * into the step, which uses ((accumulator + mean) * fp32(1/G)), the average
+ * over the G micro-batches (equivalently, the loss divided by G).
+ *   micro-steps 1 .. G-1: zs_grad_accumulate (first = 1 on micro-step 1, which
+ *                         overwrites the accumulator instead of adding);
+ *   micro-step G:         zs_shard_step_accumulated.
+ * ------------------------------------------------------------------------- */
+
+/* accum[i] = (first ? 0 : accum[i]) + mean_j x_j[i] for shard-local i in
+ * [lo, hi), the mean formed as zs_shard_step forms it (fp32, j ascending,
+ * times fp32(1/N)). accum: device fp32 [S], element 0 of the shard, must not
+ * overlap the slices. Errors as zs_shard_step. */
+zs_status zs_grad_accumulate(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                             const void* const* grad_slices, zs_dtype grad_dtype, float* accum,
+                             int32_t first, void* cuda_stream);
+
+/* zs_shard_step on g = (accum[i] + mean_j x_j[i]) * fp32(1/micro_steps), with
+ * accum (device fp32 [S], read only) holding the sum of the earlier
+ * micro-steps' means. micro_steps >= 1; accum must not overlap any output. */
+zs_status zs_shard_step_accumulated(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                                    const void* const* grad_slices, zs_dtype grad_dtype,
+                                    const float* accum, int32_t micro_steps, float* master,
+                                    float* exp_avg, float* exp_avg_sq, void* full_flat,
+                                    zs_dtype param_dtype, const zs_adamw_hparams* hp,
+                                    int64_t step, void* cuda_stream);
+
+/* Diagnostics. *//* Diagnostics. */
 const char* zs_status_string(zs_status status);
 const char* zs_last_error(void);
 /* Synchronises `cuda_stream`, then reads and clears this device's error word

@@ -83,6 +83,11 @@ def load(path=LIB_PATH):
     L.oracle_shard_step_clipped.argtypes = [_I32, _I32, _I64, _I64, _I64, _P, _I32, _P, _P, _P,
                                             _P, _I32, _D, _D, _D, _D, _D, _I64, _F, _I32]
     L.oracle_shard_step_clipped.restype = ctypes.c_int
+    L.oracle_grad_accumulate.argtypes = [_I32, _I64, _I64, _I64, _P, _I32, _P, _I32]
+    L.oracle_grad_accumulate.restype = ctypes.c_int
+    L.oracle_shard_step_accumulated.argtypes = [_I32, _I32, _I64, _I64, _I64, _P, _I32, _P, _I32,
+                                                _P, _P, _P, _P, _I32, _D, _D, _D, _D, _D, _I64]
+    L.oracle_shard_step_accumulated.restype = ctypes.c_int
     L.oracle_gather.argtypes = [_I32, _I64, _I32, _P, _P]
     L.oracle_gather.restype = None
     L.oracle_bf16_rne.argtypes = [_F]
@@ -198,6 +203,27 @@ class Oracle:
                                               beta2, eps, wd, t, float(coef), int(skip))
         if rc != 0:
             raise ValueError("oracle_shard_step_clipped rejected the input")
+
+    # -- gradient accumulation ------------------------------------------
+    def grad_accumulate(self, *, world, S, lo, hi, grads, accum, first):
+        gdt = BF16 if grads[0].dtype == np.uint16 else FP32
+        assert accum.dtype == np.float32 and accum.size >= S
+        rc = self.L.oracle_grad_accumulate(world, S, lo, hi, self._ptrs(grads), gdt,
+                                           accum.ctypes.data, 1 if first else 0)
+        if rc != 0:
+            raise ValueError("oracle_grad_accumulate rejected the input")
+
+    def shard_step_accumulated(self, *, world, rank, S, lo, hi, grads, accum, micro_steps,
+                               master, m, v, full_flat, param_dtype=BF16, lr=1e-3, beta1=0.9,
+                               beta2=0.999, eps=1e-8, wd=0.01, t=1):
+        gdt = BF16 if grads[0].dtype == np.uint16 else FP32
+        rc = self.L.oracle_shard_step_accumulated(world, rank, S, lo, hi, self._ptrs(grads), gdt,
+                                                  accum.ctypes.data, micro_steps,
+                                                  master.ctypes.data, m.ctypes.data,
+                                                  v.ctypes.data, full_flat.ctypes.data,
+                                                  param_dtype, lr, beta1, beta2, eps, wd, t)
+        if rc != 0:
+            raise ValueError("oracle_shard_step_accumulated rejected the input")
 
     # -- O6 gather -------------------------------------------------------
     def gather(self, *, world, S, elem_size, shards, full_flat):

@@ -424,6 +424,55 @@ int oracle_shard_step_clipped(int32_t world, int32_t rank, int64_t S, int64_t lo
 }
 
 /* ---------------------------------------------------------------------------
+ * Gradient accumulation on the shard. [DP-to-ZeRO] "Gradient Accumulation 会
+ * 改变生命周期": with G micro-batches per optimizer step one must decide whether
+ * each micro-step ReduceScatters, whether to accumulate on the shard or on the
+ * full tensor, and whether the loss is divided by G. Readings: every micro-step
+ * ReduceScatters and its mean gradient is added into an fp32 accumulator of
+ * this rank's shard (a_1 = 0 + mean_1, a_k = a_{k-1} + mean_k); the last
+ * micro-step's slices go straight into the update with
+ * g = (a_{G-1} + mean_G) * fp32(1/G), the average over the micro-batches.
+ * ------------------------------------------------------------------------- */
+int oracle_grad_accumulate(int32_t world, int64_t S, int64_t lo, int64_t hi,
+                           const void* const* grads, int32_t grad_dtype, float* accum,
+                           int32_t first) {
+  if (world < 1 || lo < 0 || hi < lo || hi > S) return -1;
+  float invN = (float)(1.0 / (double)world);
+  for (int64_t i = lo; i < hi; ++i) {
+    float acc = 0.0f;
+    for (int32_t j = 0; j < world; ++j) acc = acc + load_grad(grads[j], grad_dtype, i);
+    float mean = acc * invN;
+    accum[i] = (first ? 0.0f : accum[i]) + mean;
+  }
+  return 0;
+}
+
+int oracle_shard_step_accumulated(int32_t world, int32_t rank, int64_t S, int64_t lo,
+                                  int64_t hi, const void* const* grads, int32_t grad_dtype,
+                                  const float* accum, int32_t micro_steps, float* master,
+                                  float* m, float* v, void* full_flat, int32_t param_dtype,
+                                  double lr, double beta1, double beta2, double eps, double wd,
+                                  int64_t t) {
+  if (world < 1 || rank < 0 || rank >= world || lo < 0 || hi < lo || hi > S || t < 1 ||
+      micro_steps < 1)
+    return -1;
+  if (!elem_bytes(param_dtype) || (grad_dtype != DT_BF16 && grad_dtype != DT_FP32))
+    return -1;
+  Scalars s = make_scalars(lr, beta1, beta2, eps, wd, t, world);
+  float invG = (float)(1.0 / (double)micro_steps);
+  int64_t slot = (int64_t)rank * S;
+  for (int64_t i = lo; i < hi; ++i) {
+    float acc = 0.0f;
+    for (int32_t j = 0; j < world; ++j) acc = acc + load_grad(grads[j], grad_dtype, i);
+    float mean = acc * s.invN;
+    float g = (accum[i] + mean) * invG;
+    adamw_element(s, g, master[i], m[i], v[i]);
+    store_param(full_flat, param_dtype, slot + i, master[i]);
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------
  * O7. The unsharded data-parallel step every DDP replica runs ([DP-to-ZeRO]
  * "DDP 为什么单卡仍是 16P" and "Data Parallel 保证的数学语义"): AllReduce the
  * N local gradients to their mean over the whole flat buffer, run AdamW on

@@ -754,6 +754,133 @@ def pin_clip_ddp_equivalence(o, w=TINY, steps=2):
                                   full_st[k].view(np.uint32)), f"state {k} differs at t={t}"
 
 
+# ------------------------------------------------- gradient accumulation ----
+def _accum_run(o, micro, world, S, master, hp=HP, t=1, stale=None):
+    """Run G = len(micro) micro-steps (each a list of N slices) through the
+    accumulator and the accumulated step; return (master, m, v, params)."""
+    G = len(micro)
+    acc = np.full(S, np.nan, np.float32) if stale is None else stale.copy()
+    for k in range(G - 1):
+        o.grad_accumulate(world=world, S=S, lo=0, hi=S, grads=micro[k], accum=acc, first=k == 0)
+    if G == 1:
+        acc = np.zeros(S, np.float32)
+    st = [master.copy(), np.zeros(S, np.float32), np.zeros(S, np.float32)]
+    full = np.zeros(S * world, np.uint16)
+    o.shard_step_accumulated(world=world, rank=0, S=S, lo=0, hi=S, grads=micro[G - 1],
+                             accum=acc, micro_steps=G, master=st[0], m=st[1], v=st[2],
+                             full_flat=full, t=t, **hp)
+    return st + [full]
+
+
+def pin_accum_single_microstep_identity(o):
+    """G = 1 with a zero accumulator is the plain step, bit for bit."""
+    grads, master = _clip_inputs(n=1500, world=4, seed=41)
+    a = _accum_run(o, [grads], 4, 1500, master)
+    b = [master.copy(), np.zeros(1500, np.float32), np.zeros(1500, np.float32)]
+    fb = np.zeros(1500 * 4, np.uint16)
+    o.shard_step(world=4, rank=0, S=1500, lo=0, hi=1500, grads=grads, master=b[0], m=b[1],
+                 v=b[2], full_flat=fb, t=1, **HP)
+    for x, y in zip(a, b + [fb]):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+def pin_accum_dyadic(o):
+    """Dyadic micro-batches: the gradient the update sees is the exact average
+    over the G micro-batches and the N ranks (exact for G a power of two,
+    within one fp32 rounding of the exact value otherwise); observed as m with
+    beta1 = 0."""
+    rng = np.random.default_rng(8)
+    world, S = 4, 257
+    for G in (2, 3, 4, 5, 8):
+        ints = rng.integers(-32, 33, size=(G, world, S))
+        micro = [[to_bf16_exact((ints[k, j] * 2.0 ** -8).astype(np.float32)) for j in range(world)]
+                 for k in range(G)]
+        st = _accum_run(o, micro, world, S, np.zeros(S, np.float32),
+                        hp=dict(lr=0.0, beta1=0.0, beta2=0.999, eps=1e-8, wd=0.0))
+        g = st[1]
+        exact = [Fraction(int(x), 256 * world * G) for x in ints.sum(axis=(0, 1))]
+        for got, ex in zip(g, exact):
+            if G & (G - 1) == 0:
+                assert Fraction(float(got)) == ex, G
+            else:
+                ulp = abs(float(np.spacing(np.float32(float(ex)))))
+                assert abs(Fraction(float(got)) - ex) <= Fraction(ulp), G
+
+
+def pin_accum_equals_merged(o):
+    """G = 2 micro-batches of N = 2 slices, dyadic: the same update as one step
+    over the 4 slices together (the mean over micro-batches and ranks)."""
+    rng = np.random.default_rng(9)
+    S = 300
+    ints = rng.integers(-16, 17, size=(4, S))
+    sl = [to_bf16_exact((ints[j] * 2.0 ** -6).astype(np.float32)) for j in range(4)]
+    master = synth.fill(S, seed=9, stream=synth.STREAM_MASTER, sigma=0.02)
+    a = _accum_run(o, [sl[:2], sl[2:]], 2, S, master)
+    b = [master.copy(), np.zeros(S, np.float32), np.zeros(S, np.float32)]
+    fb = np.zeros(S * 4, np.uint16)
+    o.shard_step(world=4, rank=0, S=S, lo=0, hi=S, grads=sl, master=b[0], m=b[1], v=b[2],
+                 full_flat=fb, t=1, **HP)
+    for x, y in zip(a[:3], b):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+    assert np.array_equal(a[3][:S], fb[:S])
+
+
+def pin_accum_first_overwrites(o):
+    """The first micro-step overwrites the accumulator: stale contents (NaN,
+    leftovers of the previous optimizer step) never reach the update."""
+    grads, master = _clip_inputs(n=800, world=2, seed=43)
+    g2, _ = _clip_inputs(n=800, world=2, seed=44)
+    clean = _accum_run(o, [grads, g2], 2, 800, master, stale=np.zeros(800, np.float32))
+    dirty = _accum_run(o, [grads, g2], 2, 800, master, stale=np.full(800, np.nan, np.float32))
+    for x, y in zip(clean, dirty):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+    assert np.isfinite(clean[0]).all()
+
+
+def pin_accum_ddp_equivalence(o, w=TINY, G=3, steps=2):
+    """G micro-steps per optimizer step: the N ranks' accumulators and steps,
+    gathered, equal the unsharded accumulation and step over the whole flat
+    buffer, bit for bit."""
+    plan = o.plan(w.numels, w.tied_to, world=w.world, align=w.align)
+    P, P_pad, S, N = plan["P"], plan["P_pad"], plan["S"], w.world
+    master0 = synth.fill(P_pad, seed=w.seed, stream=synth.STREAM_MASTER, sigma=w.master_sigma,
+                         p_limit=P)
+    full_st = [master0.copy(), np.zeros(P_pad, np.float32), np.zeros(P_pad, np.float32)]
+    full_acc = np.zeros(P_pad, np.float32)
+    full_params = np.zeros(P_pad * N, np.uint16)
+    sh = [[master0[r * S:(r + 1) * S].copy(), np.zeros(S, np.float32), np.zeros(S, np.float32)]
+          for r in range(N)]
+    sh_acc = [np.zeros(S, np.float32) for _ in range(N)]
+    for t in range(1, steps + 1):
+        for k in range(G):
+            local = [synth.fill(P_pad, seed=w.seed, rank=j, step=1000 * t + k, sigma=w.grad_sigma,
+                                p_limit=P, bf16=True) for j in range(N)]
+            slices = [[local[j][r * S:(r + 1) * S].copy() for j in range(N)] for r in range(N)]
+            if k < G - 1:
+                o.grad_accumulate(world=N, S=P_pad, lo=0, hi=P_pad, grads=local, accum=full_acc,
+                                  first=k == 0)
+                for r in range(N):
+                    o.grad_accumulate(world=N, S=S, lo=0, hi=S, grads=slices[r], accum=sh_acc[r],
+                                      first=k == 0)
+                continue
+            o.shard_step_accumulated(world=N, rank=0, S=P_pad, lo=0, hi=P_pad, grads=local,
+                                     accum=full_acc, micro_steps=G, master=full_st[0],
+                                     m=full_st[1], v=full_st[2], full_flat=full_params, t=t, **HP)
+            fulls = []
+            for r in range(N):
+                f = np.zeros(P_pad, np.uint16)
+                o.shard_step_accumulated(world=N, rank=r, S=S, lo=0, hi=S, grads=slices[r],
+                                         accum=sh_acc[r], micro_steps=G, master=sh[r][0],
+                                         m=sh[r][1], v=sh[r][2], full_flat=f, t=t, **HP)
+                fulls.append(f[r * S:(r + 1) * S].copy())
+            gathered = np.zeros(P_pad, np.uint16)
+            o.gather(world=N, S=S, elem_size=2, shards=fulls, full_flat=gathered)
+            assert np.array_equal(gathered, full_params[:P_pad]), f"params differ at t={t}"
+            for i in range(3):
+                assert np.array_equal(np.concatenate([x[i] for x in sh]).view(np.uint32),
+                                      full_st[i].view(np.uint32)), f"state {i} differs at t={t}"
+
+
 ALL_PINS = [
     pin_sign_law, pin_zero_grad, pin_constant_grad, pin_eps_placement, pin_lr0_wd0,
     pin_fp64_bound, pin_bias_correction_t2, pin_reduce_dyadic, pin_reduce_order,
@@ -761,4 +888,6 @@ ALL_PINS = [
     pin_plan_buckets, pin_plan_workloads, pin_ledger_pages, pin_ddp_equivalence,
     pin_bucket_invariance, pin_sqnorm_dyadic, pin_clip_coef_closed_forms,
     pin_clip_unit_identity, pin_clip_post_norm, pin_clip_skip, pin_clip_ddp_equivalence,
+    pin_accum_single_microstep_identity, pin_accum_dyadic, pin_accum_equals_merged,
+    pin_accum_first_overwrites, pin_accum_ddp_equivalence,
 ]

@@ -60,6 +60,14 @@ MUTANTS = [
     ("non-finite never flagged", "*nonfinite = std::isfinite(norm) ? 0 : 1;", "*nonfinite = 0;"),
     ("skip ignored", "  if (skip) return 0;", "  if (false) return 0;"),
     ("coefficient ignored", "float g = (acc * s.invN) * coef;", "float g = acc * s.invN;"),
+    ("accumulator overwritten every micro-step",
+     "accum[i] = (first ? 0.0f : accum[i]) + mean;", "accum[i] = 0.0f + mean;"),
+    ("first micro-step adds stale contents",
+     "accum[i] = (first ? 0.0f : accum[i]) + mean;", "accum[i] = accum[i] + mean;"),
+    ("accumulated gradient not divided by G", "float g = (accum[i] + mean) * invG;",
+     "float g = accum[i] + mean;"),
+    ("accumulator ignored by the step", "float g = (accum[i] + mean) * invG;",
+     "float g = mean * invG;"),
 ]
 
 
