@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int64_t g = g0 + tid; g < g1; g += stride) {
       float prev[GW], acc[GW];
       if (!first) load_state<GW>(accum + GW * g, prev);
-      reduce_group<GW, BF16G, 0>(a, g, acc);
+      reduce_group<GW, BF16G>(a, g, acc);
 #pragma unroll
       for (int k = 0; k < GW; ++k)
         acc[k] = __fadd_rn(first ? 0.0f : prev[k], __fmul_rn(acc[k], a.s.invN));
