@@ -471,6 +471,18 @@ def run_ours(args, w):
             s_.wait_stream(stream)
         e2e_step()
         torch.cuda.synchronize()
+        # The host link as it is right now: the same bytes host->device as one
+        # copy per slice, no step, no read-back (the link is shared with other
+        # tenants of the machine and dips periodically).
+        link = []
+        for _ in range(args.e2e_steps):
+            a, b = Ev(), Ev()
+            a.record(stream)
+            for hg, g in zip(h_grads, grads):
+                g.copy_(hg, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            link.append(2 * N * S / (a.elapsed_time(b) / 1e3) / 1e9)
         if gworld > 1:
             dist.barrier()
         a, b = Ev(), Ev()
@@ -488,7 +500,11 @@ def run_ours(args, w):
         e2e = {"value": e2e_elems / e2e_t, "unit": UNIT, "h2d_bytes_per_step": 2 * N * S,
                "d2h_bytes_per_step": 2 * S, "steps": args.e2e_steps,
                "ms_per_step": 1e3 * e2e_t / args.e2e_steps, "chunks": nch,
-               "h2d_gbs": 2 * N * S * args.e2e_steps / e2e_t / 1e9}
+               "h2d_gbs": 2 * N * S * args.e2e_steps / e2e_t / 1e9,
+               "link_h2d_gbs": {"median": statistics.median(link), "min": min(link),
+                                "max": max(link),
+                                "note": "plain host->device copies of the same bytes, "
+                                        "timed just before; the host link is shared"}}
         del h_grads, h_out
 
     if grank == 0:
@@ -557,8 +573,8 @@ def main(argv=None):
                          "accumulated step")
     ap.add_argument("--micro-steps", type=int, default=4,
                     help="G, micro-batches per optimizer step for --pipeline accum")
-    ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--e2e-chunks", type=int, default=16)
+    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-chunks", type=int, default=32)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-elems", type=int, default=32 * 1024 * 1024)
