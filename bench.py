@@ -38,7 +38,8 @@ if ROOT not in sys.path:
 METRIC = "shard-step elements/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "elements/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCE = os.path.join(ROOT, "fsdp_sharded_mixed_gb300", "csrc", "shard_step.cu")
+KERNEL_SOURCES = [os.path.join(ROOT, "fsdp_sharded_mixed_gb300", "csrc", f)
+                  for f in ("shard_step.cu", "step_kernel.cuh")]
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "shard_step_traffic.txt")
 
 
@@ -80,8 +81,12 @@ def sum_over_ranks(value, device=None):
 
 
 def kernel_sha():
-    with open(KERNEL_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256[:16] over the sources of the step kernel."""
+    h = hashlib.sha256()
+    for path in KERNEL_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def committed_traffic(workload_key):
