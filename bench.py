@@ -328,7 +328,46 @@ def run_ours(args, w):
         zs.zs_shard_step_accumulated(plan, r, 0, S, grads, zs.ZS_BF16, acc_buf, G, master, m, v,
                                      full, zs.ZS_BF16, hp, step_no[0], stream=sp)
 
-    if clip:
+    units = []
+    up_dims = {}
+    if args.pipeline == "unshard":
+        # FSDP2's gather side over the whole model: per wrap unit a row-sharded
+        # plan, the rank-major AllGather buffer (filled once from the
+        # generator), and the unit's full parameters, written by the copy-out.
+        from synth.workloads import wrap_units
+        for idx in wrap_units(w):
+            local_of = {g_: k for k, g_ in enumerate(idx)}
+            ps = [w.params[i] for i in idx]
+            ties_u = [local_of[p.tied_to] if p.tied_to >= 0 else -1 for p in ps]
+            up = zs.zs_rows_plan([p.shape[0] for p in ps], [p.numel for p in ps], ties_u, world=N,
+                                 align_elems=w.align)
+            gbuf = torch.empty(up.P_pad, dtype=torch.int16, device=dev)
+            synth.fill_device(gbuf.data_ptr(), up.P_pad, seed=w.seed, rank=len(units), step=1,
+                              sigma=w.grad_sigma, bf16=True, cuda_stream=sptr)
+            outs = [torch.empty(p.numel, dtype=torch.int16, device=dev) if t < 0 else None
+                    for p, t in zip(ps, ties_u)]
+            units.append((up, gbuf, outs))
+            up_dims[id(up)] = [p.shape[0] for p in ps]
+        torch.cuda.synchronize()
+
+    def _segments(up, outs):
+        c, _ = zs.zs_plan_rows(up)
+        return sum(-(-d // ci) for d, ci, o in zip(up_dims[id(up)], c, outs)
+                   if o is not None and d > 0)
+
+    def part_unshard(sp):
+        for up, gbuf, outs in units:
+            zs.zs_unshard(up, gbuf, zs.ZS_BF16, outs, stream=sp)
+
+    if args.pipeline == "unshard":
+        # bytes per shard element of the workload's plan: every parameter
+        # element read once from the gathered buffer and written once.
+        unit_bytes = 4 * sum(p.numel for p in w.params if p.tied_to < 0)
+        pipeline = [("segment_copy_kernel", part_unshard, unit_bytes / S)]
+        launches_per_step = 0
+        for up, _, outs in units:   # one launch per 256 (parameter, rank) row segments
+            launches_per_step += -(-_segments(up, outs) // 256)
+    elif clip:
         pipeline = [("grad_sqnorm_kernel+clip_coef_kernel", part_norm, norm_bpe),
                     ("shard_step_kernel", part_clipped, bpe)]
         launches_per_step = 3
@@ -516,11 +555,12 @@ def run_ours(args, w):
         peak, peak_kind = measured_peak()
         step_bpe = pipeline[-1][2]
         achieved = step_bpe * S / step_s / 1e9
+        kname = pipeline[-1][0]
         traffic_pe = committed_traffic(w.key)
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "peak_source": peak_kind,
                     "traffic": None if traffic_pe is None else traffic_pe * S,
-                    "algorithmic_bytes": step_bpe * S, "kernel": "shard_step_kernel",
+                    "algorithmic_bytes": step_bpe * S, "kernel": kname,
                     "kernel_sha": kernel_sha()}
         kernels = {}
         for (name, _, b), t in zip(pipeline, part_s):
@@ -572,10 +612,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--graph", action="store_true",
                     help="time one replay of a CUDA graph holding the K launches")
-    ap.add_argument("--pipeline", choices=["step", "clip", "accum"], default="step",
+    ap.add_argument("--pipeline", choices=["step", "clip", "accum", "unshard"], default="step",
                     help="step: the fused shard step; clip: global-norm pass + clip "
                          "coefficient + clipped step; accum: G-1 accumulations + the "
-                         "accumulated step")
+                         "accumulated step; unshard: FSDP2 copy-out of every wrap unit's "
+                         "gathered parameters")
     ap.add_argument("--micro-steps", type=int, default=4,
                     help="G, micro-batches per optimizer step for --pipeline accum")
     ap.add_argument("--e2e-steps", type=int, default=8)

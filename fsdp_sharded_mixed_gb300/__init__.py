@@ -34,7 +34,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-fmad=false", "-prec-div=true",
               "-prec-sqrt=true", "-ftz=false", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-I/usr/local/cuda/include"]
-CUDA_SOURCES = ["shard_step.cu", "gather.cu", "clip.cu", "accum.cu"]
+CUDA_SOURCES = ["shard_step.cu", "gather.cu", "clip.cu", "accum.cu", "rows.cu"]
 HOST_SOURCES = ["api.cpp", "plan.cpp"]
 
 
@@ -115,6 +115,10 @@ EXPORTS = {
     "zs_shard_step_accumulated": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _I32, _P, _P, _P,
                                    _P, ctypes.c_int, ctypes.POINTER(AdamWHparams), _I64, _P],
                                   ctypes.c_int),
+    "zs_rows_plan": ([_P, _P, _P, _I32, _I32, _I64, _P], ctypes.c_int),
+    "zs_plan_rows": ([_P, _P, _P, _I32], ctypes.c_int),
+    "zs_unshard": ([_P, _P, ctypes.c_int, _P, _P], ctypes.c_int),
+    "zs_shard_rows": ([_P, _I32, _P, ctypes.c_int, _P, _P], ctypes.c_int),
     "zs_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "zs_last_error": ([], ctypes.c_char_p),
     "zs_check_device_error": ([_P], ctypes.c_int),
@@ -194,6 +198,34 @@ def zs_flatten_plan(numels, tied_to=None, world=1, align_elems=128, bucket_elems
     _check(lib().zs_flatten_plan(arr, ties, n, world, align_elems, bucket_elems,
                                  ctypes.byref(out)))
     return Plan(out.value, n)
+
+
+def zs_rows_plan(dim0, numels, tied_to=None, world=1, align_elems=128):
+    """Per-parameter row sharding (FSDP2 Shard(0)); see include/zs.h."""
+    n = len(numels)
+    d = (ctypes.c_int64 * max(n, 1))(*dim0)
+    arr = (ctypes.c_int64 * max(n, 1))(*numels)
+    ties = None if tied_to is None else (ctypes.c_int32 * max(n, 1))(*tied_to)
+    out = ctypes.c_void_p()
+    _check(lib().zs_rows_plan(d, arr, ties, n, world, align_elems, ctypes.byref(out)))
+    return Plan(out.value, n)
+
+
+def zs_plan_rows(plan):
+    c = (ctypes.c_int64 * max(plan.n_params, 1))()
+    w = (ctypes.c_int64 * max(plan.n_params, 1))()
+    _check(lib().zs_plan_rows(plan.handle, c, w, plan.n_params))
+    return list(c)[:plan.n_params], list(w)[:plan.n_params]
+
+
+def zs_unshard(plan, gathered, dtype, params_out, stream=None):
+    ptrs = (ctypes.c_void_p * max(len(params_out), 1))(*[_ptr(p) for p in params_out])
+    _check(lib().zs_unshard(plan.handle, _ptr(gathered), dtype, ptrs, _stream(stream)))
+
+
+def zs_shard_rows(plan, rank, params_in, dtype, local_out, stream=None):
+    ptrs = (ctypes.c_void_p * max(len(params_in), 1))(*[_ptr(p) for p in params_in])
+    _check(lib().zs_shard_rows(plan.handle, rank, ptrs, dtype, _ptr(local_out), _stream(stream)))
 
 
 def zs_plan_info(plan):

@@ -511,9 +511,138 @@ extern "C" zs_status zs_gather_assemble(const zs_plan* plan, int32_t rank,
     if (e != cudaSuccess)
       return zs::fail(ZS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   }
-  if (views_out)
+  if (views_out) {
+    if (plan->layout != zs::kLayoutFlat)
+      return zs::fail(ZS_ERR_UNSUPPORTED,
+                      "%s: a row-sharded plan's gathered buffer is rank-major; zs_unshard copies "
+                      "it out into parameters (views_out must be NULL)", fn);
     for (int32_t k = 0; k < plan->n_params; ++k)
       views_out[k] = dst + (uint64_t)plan->offsets[k] * pb;
+  }
+  return ZS_OK;
+}
+
+namespace {
+
+// Rows [r*c, min((r+1)*c, d)) of a parameter with d rows of w elements.
+int64_t valid_rows(const zs_plan* p, int32_t i, int32_t r) {
+  const int64_t c = p->rows_per_rank[i], d = p->dim0[i];
+  const int64_t lo = (int64_t)r * c;
+  if (lo >= d) return 0;
+  return (lo + c <= d ? c : d - lo);
+}
+
+zs_status check_rows_params(const zs_plan* plan, const void* const* params, int pb, bool output,
+                            const char* fn, std::vector<Range>* ranges) {
+  if (!params && plan->n_params > 0) return zs::fail(ZS_ERR_INVAL, "%s: parameter list is NULL", fn);
+  for (int32_t i = 0; i < plan->n_params; ++i) {
+    if (plan->owner[i] != i || plan->numels[i] == 0) continue;
+    const void* q = params[i];
+    if (!q) return zs::fail(ZS_ERR_INVAL, "%s: params[%d] is NULL", fn, i);
+    if ((uintptr_t)q % (uintptr_t)pb)
+      return zs::fail(ZS_ERR_ALIGN, "%s: params[%d] is not %d-byte aligned", fn, i, pb);
+    const int64_t bytes = plan->numels[i] * pb;
+    ranges->push_back({(uintptr_t)q, (uintptr_t)q + (uint64_t)bytes, "params", i, output});
+    if (zs_status st = check_device_buffer(q, bytes, fn, "params", i)) return st;
+  }
+  return ZS_OK;
+}
+
+}  // namespace
+
+extern "C" zs_status zs_unshard(const zs_plan* plan, const void* gathered, zs_dtype dtype,
+                                void* const* params_out, void* cuda_stream) {
+  static const char* fn = "zs_unshard";
+  zs::clear_error();
+  if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
+  if (plan->layout != zs::kLayoutRows)
+    return zs::fail(ZS_ERR_UNSUPPORTED, "%s: a flat plan's gathered buffer already is the "
+                    "parameters (use the views of zs_gather_assemble)", fn);
+  const int pb = zs::elem_bytes(dtype);
+  if (!pb) return zs::fail(ZS_ERR_INVAL, "%s: unknown dtype %d", fn, (int)dtype);
+  const int32_t N = plan->world;
+  const int64_t S = plan->S;
+  if (!gathered && S > 0) return zs::fail(ZS_ERR_INVAL, "%s: gathered is NULL", fn);
+  if ((uintptr_t)gathered % 16) return zs::fail(ZS_ERR_ALIGN, "%s: gathered is not 16-byte aligned", fn);
+  std::vector<Range> ranges;
+  const int64_t gbytes = (int64_t)N * S * pb;
+  ranges.push_back({(uintptr_t)gathered, (uintptr_t)gathered + (uint64_t)gbytes, "gathered", 0, false});
+  if (zs_status st = check_rows_params(plan, (const void* const*)params_out, pb, true, fn, &ranges)) return st;
+  if (zs_status st = check_overlaps(ranges, fn)) return st;
+  if (zs_status st = check_device_buffer(gathered, gbytes, fn, "gathered", 0)) return st;
+  std::vector<zs::RowSegment> segs;
+  const unsigned char* g = static_cast<const unsigned char*>(gathered);
+  for (int32_t i = 0; i < plan->n_params; ++i) {
+    if (plan->owner[i] != i) continue;
+    const int64_t w = plan->row_elems[i], c = plan->rows_per_rank[i];
+    for (int32_t r = 0; r < N; ++r) {
+      const int64_t rows = valid_rows(plan, i, r);
+      if (rows == 0) continue;
+      zs::RowSegment sg;
+      sg.src = g + ((uint64_t)r * S + plan->offsets[i]) * pb;
+      sg.dst = static_cast<unsigned char*>(params_out[i]) + (uint64_t)r * c * w * pb;
+      sg.copy_bytes = rows * w * pb;
+      sg.zero_bytes = 0;
+      segs.push_back(sg);
+    }
+  }
+  if (segs.empty()) return ZS_OK;
+  cudaError_t e = zs::launch_segment_copy(segs.data(), (int)segs.size(),
+                                          static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess)
+    return zs::fail(ZS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return ZS_OK;
+}
+
+extern "C" zs_status zs_shard_rows(const zs_plan* plan, int32_t rank, const void* const* params_in,
+                                   zs_dtype dtype, void* local_out, void* cuda_stream) {
+  static const char* fn = "zs_shard_rows";
+  zs::clear_error();
+  if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
+  if (plan->layout != zs::kLayoutRows)
+    return zs::fail(ZS_ERR_UNSUPPORTED, "%s: not a row-sharded plan", fn);
+  const int pb = zs::elem_bytes(dtype);
+  if (!pb) return zs::fail(ZS_ERR_INVAL, "%s: unknown dtype %d", fn, (int)dtype);
+  const int32_t N = plan->world;
+  const int64_t S = plan->S;
+  if (rank < 0 || rank >= N) return zs::fail(ZS_ERR_RANGE, "%s: rank %d not in [0, %d)", fn, rank, N);
+  if (S == 0) return ZS_OK;
+  if (!local_out) return zs::fail(ZS_ERR_INVAL, "%s: local_out is NULL", fn);
+  if ((uintptr_t)local_out % 16) return zs::fail(ZS_ERR_ALIGN, "%s: local_out is not 16-byte aligned", fn);
+  std::vector<Range> ranges;
+  ranges.push_back({(uintptr_t)local_out, (uintptr_t)local_out + (uint64_t)S * pb, "local_out", 0, true});
+  if (zs_status st = check_rows_params(plan, params_in, pb, false, fn, &ranges)) return st;
+  if (zs_status st = check_overlaps(ranges, fn)) return st;
+  if (zs_status st = check_device_buffer(local_out, S * pb, fn, "local_out", 0)) return st;
+  std::vector<zs::RowSegment> segs;
+  unsigned char* out = static_cast<unsigned char*>(local_out);
+  int64_t used = 0;
+  for (int32_t i = 0; i < plan->n_params; ++i) {
+    if (plan->owner[i] != i) continue;
+    const int64_t w = plan->row_elems[i], c = plan->rows_per_rank[i];
+    const int64_t rows = valid_rows(plan, i, rank);
+    zs::RowSegment sg;
+    sg.src = rows ? static_cast<const unsigned char*>(params_in[i]) + (uint64_t)rank * c * w * pb
+                  : nullptr;
+    sg.dst = out + (uint64_t)plan->offsets[i] * pb;
+    sg.copy_bytes = rows * w * pb;
+    sg.zero_bytes = (c - rows) * w * pb;
+    used = plan->offsets[i] + c * w;
+    if (sg.copy_bytes + sg.zero_bytes > 0) segs.push_back(sg);
+  }
+  if (S > used) {
+    zs::RowSegment pad;
+    pad.src = nullptr;
+    pad.dst = out + (uint64_t)used * pb;
+    pad.copy_bytes = 0;
+    pad.zero_bytes = (S - used) * pb;
+    segs.push_back(pad);
+  }
+  if (segs.empty()) return ZS_OK;
+  cudaError_t e = zs::launch_segment_copy(segs.data(), (int)segs.size(),
+                                          static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess)
+    return zs::fail(ZS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return ZS_OK;
 }
 

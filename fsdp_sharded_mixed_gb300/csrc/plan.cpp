@@ -59,6 +59,7 @@ extern "C" zs_status zs_flatten_plan(const int64_t* numels, const int32_t* tied_
     delete p;
     return zs::fail(ZS_ERR_NOMEM, "zs_flatten_plan: out of host memory");
   }
+  p->layout = zs::kLayoutFlat;
   p->world = world;
   p->n_params = n_params;
   p->align = align_elems;
@@ -207,5 +208,121 @@ extern "C" zs_status zs_plan_free(zs_plan* plan) {
   }
   plan->magic = 0;
   delete plan;
+  return ZS_OK;
+}
+
+// The per-parameter row layout of FSDP2 ("从 Data Parallel 到 ZeRO/FSDP", "ZeRO 与
+// FSDP 的关系": fully_shard keeps per-parameter sharded state): parameter i is
+// cut along dim 0 into N chunks of c_i = ceil(dim0_i / N) rows; rank r holds
+// rows [r*c_i, min((r+1)*c_i, dim0_i)) (possibly none), padded to c_i rows.
+// A rank's local buffer is its padded chunks back to back in registration
+// order (tied parameters once), padded at the end to a multiple of
+// align_elems: S = that length. The AllGather of the N local buffers is the
+// rank-major [N][S] buffer that zs_unshard copies out into parameters.
+extern "C" zs_status zs_rows_plan(const int64_t* dim0, const int64_t* numels,
+                                  const int32_t* tied_to, int32_t n_params, int32_t world,
+                                  int64_t align_elems, zs_plan** out) {
+  zs::clear_error();
+  if (!out) return zs::fail(ZS_ERR_INVAL, "zs_rows_plan: out is NULL");
+  *out = nullptr;
+  if (n_params < 0) return zs::fail(ZS_ERR_INVAL, "zs_rows_plan: n_params < 0");
+  if (n_params > 0 && (!numels || !dim0))
+    return zs::fail(ZS_ERR_INVAL, "zs_rows_plan: numels or dim0 is NULL");
+  if (world < 1 || world > ZS_MAX_WORLD)
+    return zs::fail(ZS_ERR_RANGE, "zs_rows_plan: world %d outside 1..%d", world, ZS_MAX_WORLD);
+  if (align_elems < 1 || align_elems > (int64_t(1) << 32))
+    return zs::fail(ZS_ERR_RANGE, "zs_rows_plan: align_elems %lld out of range",
+                    (long long)align_elems);
+  zs_plan* p = new (std::nothrow) zs_plan();
+  if (!p) return zs::fail(ZS_ERR_NOMEM, "zs_rows_plan: out of host memory");
+  try {
+    p->numels.assign(numels, numels + n_params);
+    p->dim0.assign(dim0, dim0 + n_params);
+    p->offsets.assign(n_params, 0);
+    p->owner.assign(n_params, 0);
+    p->row_elems.assign(n_params, 0);
+    p->rows_per_rank.assign(n_params, 0);
+  } catch (...) {
+    delete p;
+    return zs::fail(ZS_ERR_NOMEM, "zs_rows_plan: out of host memory");
+  }
+  p->layout = zs::kLayoutRows;
+  p->world = world;
+  p->n_params = n_params;
+  p->align = align_elems;
+  p->bucket_elems = 0;
+  int64_t local = 0, total = 0;
+  for (int32_t i = 0; i < n_params; ++i) {
+    const int64_t n = numels[i], d = dim0[i];
+    if (n < 0 || d < 0 || (d == 0 && n != 0) || (d > 0 && n % d != 0)) {
+      delete p;
+      return zs::fail(ZS_ERR_INVAL, "zs_rows_plan: param %d has %lld elements in %lld rows", i,
+                      (long long)n, (long long)d);
+    }
+    const int32_t t = tied_to ? tied_to[i] : -1;
+    if (t >= 0) {
+      if (t >= i) {
+        delete p;
+        return zs::fail(ZS_ERR_INVAL, "zs_rows_plan: tied_to[%d] = %d is not an earlier param", i, t);
+      }
+      const int32_t root = p->owner[t];
+      if (numels[root] != n || dim0[root] != d) {
+        delete p;
+        return zs::fail(ZS_ERR_INVAL, "zs_rows_plan: tied param %d differs from its owner %d", i, root);
+      }
+      p->owner[i] = root;
+      p->offsets[i] = p->offsets[root];
+      p->row_elems[i] = p->row_elems[root];
+      p->rows_per_rank[i] = p->rows_per_rank[root];
+      continue;
+    }
+    p->owner[i] = i;
+    p->row_elems[i] = d > 0 ? n / d : 0;
+    p->rows_per_rank[i] = (d + world - 1) / world;
+    const int64_t seg = p->rows_per_rank[i] * p->row_elems[i];
+    if (add_overflows(local, seg) || add_overflows(total, n)) {
+      delete p;
+      return zs::fail(ZS_ERR_RANGE, "zs_rows_plan: sizes overflow int64");
+    }
+    p->offsets[i] = local;
+    local += seg;
+    total += n;
+  }
+  if (add_overflows(local, align_elems - 1)) {
+    delete p;
+    return zs::fail(ZS_ERR_RANGE, "zs_rows_plan: padded size overflows int64");
+  }
+  p->S = (local + align_elems - 1) / align_elems * align_elems;
+  p->P = total;
+  p->P_pad = p->S * world;
+  try {
+    p->bucket_lo.push_back(0);
+    p->bucket_hi.push_back(p->P_pad);
+  } catch (...) {
+    delete p;
+    return zs::fail(ZS_ERR_NOMEM, "zs_rows_plan: out of host memory");
+  }
+  p->magic = zs::kPlanMagic;
+  {
+    std::lock_guard<std::mutex> lock(g_live_mu);
+    live_plans().insert(p);
+  }
+  *out = p;
+  return ZS_OK;
+}
+
+extern "C" zs_status zs_plan_rows(const zs_plan* plan, int64_t* rows_per_rank,
+                                  int64_t* row_elems, int32_t n_params) {
+  zs::clear_error();
+  if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "zs_plan_rows: not a live plan");
+  if (plan->layout != zs::kLayoutRows)
+    return zs::fail(ZS_ERR_UNSUPPORTED, "zs_plan_rows: not a row-sharded plan");
+  if (n_params != plan->n_params)
+    return zs::fail(ZS_ERR_RANGE, "zs_plan_rows: plan has %d params, caller passed %d",
+                    plan->n_params, n_params);
+  for (int32_t i = 0; i < n_params; ++i) {
+    if (rows_per_rank) rows_per_rank[i] = plan->rows_per_rank[i];
+    if (row_elems) row_elems[i] = plan->row_elems[i];
+  }
   return ZS_OK;
 }

@@ -11,6 +11,7 @@
 
 struct zs_plan {
   uint64_t magic;
+  int32_t layout;      // kLayoutFlat (one flat buffer cut into N pieces) or kLayoutRows
   int32_t world;
   int32_t n_params;
   int64_t align;
@@ -20,10 +21,16 @@ struct zs_plan {
   std::vector<int64_t> offsets;
   std::vector<int32_t> owner;
   std::vector<int64_t> bucket_lo, bucket_hi;
+  // kLayoutRows: dim0[i] rows of row_elems[i] elements; rows_per_rank[i] =
+  // ceil(dim0 / N); offsets[i] = the parameter's segment offset inside every
+  // rank's local buffer (S elements, the segments back to back, padded).
+  std::vector<int64_t> dim0, row_elems, rows_per_rank;
 };
 
 namespace zs {
 
+constexpr int32_t kLayoutFlat = 0;
+constexpr int32_t kLayoutRows = 1;
 constexpr uint64_t kPlanMagic = 0x7A735F706C616E31ull;  // "zs_plan1"
 
 // Thread-local error detail; returns `st` so call sites can `return fail(...)`.
@@ -93,6 +100,17 @@ constexpr int64_t kNoAllocScratchBytes = 9984;
 cudaError_t launch_grad_sqnorm_noalloc(const NormLaunch& a, cudaStream_t stream);
 cudaError_t launch_clip_coef(const double* rank_sqnorms, int n, double max_norm, float* coef,
                              int32_t* nonfinite, cudaStream_t stream);
+
+// Segment copies of the row-sharded layout (rows.cu): copy_bytes from src to
+// dst, then zero_bytes of zeros after them at dst.
+struct RowSegment {
+  const unsigned char* src;
+  unsigned char* dst;
+  int64_t copy_bytes;
+  int64_t zero_bytes;
+};
+constexpr int kMaxSegs = 256;
+cudaError_t launch_segment_copy(const RowSegment* segs, int n, cudaStream_t stream);
 
 // Device error word (set by bounds-checked builds and bounded waits).
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* word);

@@ -271,7 +271,43 @@ zs_status zs_shard_step_accumulated(const zs_plan* plan, int32_t rank, int64_t l
                                     zs_dtype param_dtype, const zs_adamw_hparams* hp,
                                     int64_t step, void* cuda_stream);
 
-/* Diagnostics. *//* Diagnostics. */
+/* ---------------------------------------------------------------------------
+ * Per-parameter row sharding (FSDP2) and the gather side of a wrap unit.
+ * [DP-to-ZeRO] "ZeRO 与 FSDP 的关系": FSDP2's fully_shard keeps per-parameter
+ * sharded state and unshards before forward/backward, reshards after;
+ * [Lifecycle] "The parameter lifecycle, one module at a time" and "Reshard
+ * policy": AllGather before a module's compute, then reshard to 1/N, retain,
+ * or (an integer reshard_after_forward) reshard to a smaller world.
+ * Layout of a row-sharded plan: parameter i (dim0 rows of numel/dim0
+ * elements) is cut along dim 0 into N chunks of c_i = ceil(dim0/N) rows;
+ * rank r holds rows [r*c_i, min((r+1)*c_i, dim0)) (possibly none) padded with
+ * zero rows to c_i; a rank's local buffer is its padded chunks back to back in
+ * registration order (tied parameters once), zero-padded at the end to a
+ * multiple of align_elems: S elements. zs_plan_info reports S, P (the unique
+ * elements) and P_pad = N*S, the rank-major AllGather buffer. zs_shard_step
+ * and zs_gather_assemble work on these plans unchanged (S is a rank's shard);
+ * the gathered buffer is copied out into parameters by zs_unshard.
+ * ------------------------------------------------------------------------- */
+zs_status zs_rows_plan(const int64_t* dim0, const int64_t* numels, const int32_t* tied_to,
+                       int32_t n_params, int32_t world, int64_t align_elems, zs_plan** out);
+/* rows_per_rank[i] = c_i and row_elems[i] = numel/dim0 (either may be NULL);
+ * zs_plan_offsets gives each parameter's segment offset in a local buffer. */
+zs_status zs_plan_rows(const zs_plan* plan, int64_t* rows_per_rank, int64_t* row_elems,
+                       int32_t n_params);
+/* Copy-out of the AllGather: gathered = [N][S] elements of dtype, rank-major;
+ * params_out[i] = device pointer to parameter i's full tensor (numel_i
+ * elements, contiguous; entries of tied parameters are ignored). Writes every
+ * row of every owner parameter. Row-sharded plans only (ZS_ERR_UNSUPPORTED
+ * otherwise). */
+zs_status zs_unshard(const zs_plan* plan, const void* gathered, zs_dtype dtype,
+                     void* const* params_out, void* cuda_stream);
+/* Copy-in / reshard: rank `rank`'s local buffer (S elements of dtype) from the
+ * full parameters, padding zeroed. With a plan made for a smaller world M this
+ * is reshard_after_forward = M. Row-sharded plans only. */
+zs_status zs_shard_rows(const zs_plan* plan, int32_t rank, const void* const* params_in,
+                        zs_dtype dtype, void* local_out, void* cuda_stream);
+
+/* Diagnostics. *//* Diagnostics. *//* Diagnostics. */
 const char* zs_status_string(zs_status status);
 const char* zs_last_error(void);
 /* Synchronises `cuda_stream`, then reads and clears this device's error word

@@ -88,6 +88,12 @@ def load(path=LIB_PATH):
     L.oracle_shard_step_accumulated.argtypes = [_I32, _I32, _I64, _I64, _I64, _P, _I32, _P, _I32,
                                                 _P, _P, _P, _P, _I32, _D, _D, _D, _D, _D, _I64]
     L.oracle_shard_step_accumulated.restype = ctypes.c_int
+    L.oracle_rows_plan.argtypes = [_P, _P, _P, _I32, _I32, _I64, _P, _P, _P, _P]
+    L.oracle_rows_plan.restype = ctypes.c_int
+    L.oracle_unshard.argtypes = [_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _P, _P]
+    L.oracle_unshard.restype = None
+    L.oracle_shard_rows.argtypes = [_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _P, _P]
+    L.oracle_shard_rows.restype = None
     L.oracle_gather.argtypes = [_I32, _I64, _I32, _P, _P]
     L.oracle_gather.restype = None
     L.oracle_bf16_rne.argtypes = [_F]
@@ -224,6 +230,39 @@ class Oracle:
                                                   param_dtype, lr, beta1, beta2, eps, wd, t)
         if rc != 0:
             raise ValueError("oracle_shard_step_accumulated rejected the input")
+
+    # -- per-parameter row sharding (FSDP2) ------------------------------
+    def rows_plan(self, dim0, numels, tied_to=None, world=1, align=128):
+        n = len(numels)
+        d = np.ascontiguousarray(dim0, dtype=np.int64)
+        ne = np.ascontiguousarray(numels, dtype=np.int64)
+        tied = None if tied_to is None else np.ascontiguousarray(tied_to, dtype=np.int32)
+        off = np.zeros(max(n, 1), np.int64)
+        c = np.zeros(max(n, 1), np.int64)
+        w = np.zeros(max(n, 1), np.int64)
+        S = ctypes.c_int64()
+        rc = self.L.oracle_rows_plan(d.ctypes.data, ne.ctypes.data,
+                                     tied.ctypes.data if tied is not None else None, n, world,
+                                     align, off.ctypes.data, c.ctypes.data, w.ctypes.data,
+                                     ctypes.byref(S))
+        if rc != 0:
+            raise ValueError("oracle_rows_plan rejected the input")
+        return dict(S=S.value, offsets=off[:n].copy(), rows_per_rank=c[:n].copy(),
+                    row_elems=w[:n].copy(), dim0=d, tied=tied, world=world, n=n)
+
+    def unshard(self, rp, gathered, elem_size, params):
+        self.L.oracle_unshard(rp["dim0"].ctypes.data, rp["offsets"].ctypes.data,
+                              rp["rows_per_rank"].ctypes.data, rp["row_elems"].ctypes.data,
+                              rp["tied"].ctypes.data if rp["tied"] is not None else None, rp["n"],
+                              rp["world"], rp["S"], elem_size, gathered.ctypes.data,
+                              self._ptrs(params))
+
+    def shard_rows(self, rp, rank, elem_size, params, local):
+        self.L.oracle_shard_rows(rp["dim0"].ctypes.data, rp["offsets"].ctypes.data,
+                                 rp["rows_per_rank"].ctypes.data, rp["row_elems"].ctypes.data,
+                                 rp["tied"].ctypes.data if rp["tied"] is not None else None,
+                                 rp["n"], rank, rp["S"], elem_size, self._ptrs(params),
+                                 local.ctypes.data)
 
     # -- O6 gather -------------------------------------------------------
     def gather(self, *, world, S, elem_size, shards, full_flat):

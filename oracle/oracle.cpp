@@ -473,6 +473,87 @@ int oracle_shard_step_accumulated(int32_t world, int32_t rank, int64_t S, int64_
 }
 
 /* ---------------------------------------------------------------------------
+ * Per-parameter row sharding (FSDP2) and the gather side of a wrap unit.
+ * [DP-to-ZeRO] "ZeRO 与 FSDP 的关系": FSDP2 keeps per-parameter sharded state;
+ * [Lifecycle] "The parameter lifecycle, one module at a time": AllGather the
+ * module's parameters before its compute, reshard after (to 1/N, or, with an
+ * integer reshard_after_forward, to a smaller world); [Dissection] §7: a
+ * 768-element layer norm over 64 ranks gives 12-element shards.
+ * Readings: each parameter is cut along dim 0 into chunks of c = ceil(dim0/N)
+ * rows, rank r holding rows [r*c, min((r+1)*c, dim0)) (none when r*c >= dim0),
+ * padded with zero rows to c; a rank's local buffer is its padded chunks back
+ * to back in registration order (tied parameters once), padded with zeros to a
+ * multiple of align; the AllGather output is the N local buffers rank-major.
+ * ------------------------------------------------------------------------- */
+int oracle_rows_plan(const int64_t* dim0, const int64_t* numels, const int32_t* tied_to,
+                     int32_t n_params, int32_t world, int64_t align, int64_t* offsets,
+                     int64_t* rows_per_rank, int64_t* row_elems, int64_t* S_out) {
+  if (world < 1 || align < 1 || n_params < 0) return -1;
+  int64_t local = 0;
+  for (int32_t i = 0; i < n_params; ++i) {
+    if (numels[i] < 0 || dim0[i] < 0 || (dim0[i] == 0 && numels[i] != 0) ||
+        (dim0[i] > 0 && numels[i] % dim0[i] != 0))
+      return -1;
+    int32_t k = tied_to ? tied_to[i] : -1;
+    if (k >= 0) {
+      if (k >= i) return -1;
+      offsets[i] = offsets[k];
+      rows_per_rank[i] = rows_per_rank[k];
+      row_elems[i] = row_elems[k];
+      continue;
+    }
+    row_elems[i] = dim0[i] > 0 ? numels[i] / dim0[i] : 0;
+    rows_per_rank[i] = (dim0[i] + world - 1) / world;
+    offsets[i] = local;
+    local += rows_per_rank[i] * row_elems[i];
+  }
+  *S_out = (local + align - 1) / align * align;
+  return 0;
+}
+
+/* Rows of parameter i that rank r holds. */
+static int64_t rows_held(int64_t dim0, int64_t c, int32_t r) {
+  int64_t first = (int64_t)r * c;
+  if (first >= dim0) return 0;
+  return first + c <= dim0 ? c : dim0 - first;
+}
+
+/* The copy-out: gathered [N][S] -> each owner parameter's full tensor. */
+void oracle_unshard(const int64_t* dim0, const int64_t* offsets, const int64_t* rows_per_rank,
+                    const int64_t* row_elems, const int32_t* tied_to, int32_t n_params,
+                    int32_t world, int64_t S, int32_t elem_size, const void* gathered,
+                    void* const* params) {
+  for (int32_t i = 0; i < n_params; ++i) {
+    if (tied_to && tied_to[i] >= 0) continue;
+    int64_t row_bytes = row_elems[i] * elem_size;
+    for (int32_t r = 0; r < world; ++r) {
+      int64_t rows = rows_held(dim0[i], rows_per_rank[i], r);
+      const uint8_t* src = static_cast<const uint8_t*>(gathered) +
+                           ((size_t)r * S + offsets[i]) * elem_size;
+      uint8_t* dst = static_cast<uint8_t*>(params[i]) + (size_t)r * rows_per_rank[i] * row_bytes;
+      std::memcpy(dst, src, (size_t)(rows * row_bytes));
+    }
+  }
+}
+
+/* The copy-in / reshard: rank r's local buffer from the full parameters. */
+void oracle_shard_rows(const int64_t* dim0, const int64_t* offsets, const int64_t* rows_per_rank,
+                       const int64_t* row_elems, const int32_t* tied_to, int32_t n_params,
+                       int32_t rank, int64_t S, int32_t elem_size, const void* const* params,
+                       void* local) {
+  std::memset(local, 0, (size_t)S * elem_size);
+  for (int32_t i = 0; i < n_params; ++i) {
+    if (tied_to && tied_to[i] >= 0) continue;
+    int64_t row_bytes = row_elems[i] * elem_size;
+    int64_t rows = rows_held(dim0[i], rows_per_rank[i], rank);
+    const uint8_t* src = static_cast<const uint8_t*>(params[i]) +
+                         (size_t)rank * rows_per_rank[i] * row_bytes;
+    uint8_t* dst = static_cast<uint8_t*>(local) + (size_t)offsets[i] * elem_size;
+    std::memcpy(dst, src, (size_t)(rows * row_bytes));
+  }
+}
+
+/* ---------------------------------------------------------------------------
  * O7. The unsharded data-parallel step every DDP replica runs ([DP-to-ZeRO]
  * "DDP 为什么单卡仍是 16P" and "Data Parallel 保证的数学语义"): AllReduce the
  * N local gradients to their mean over the whole flat buffer, run AdamW on

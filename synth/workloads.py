@@ -151,6 +151,21 @@ SWEEP_GRAD_BYTES = [2, 4]
 SWEEP_PARAM_BYTES = [2, 3, 4]
 
 
+def wrap_units(w):
+    """FSDP wrap units of a workload's parameter list: one unit per transformer
+    block (the repeating architectural unit) and a root unit holding the rest
+    (embeddings, final norm, head; a tied head stays with its embedding).
+    Returns lists of indices into ``w.params``."""
+    blocks, root = {}, []
+    for i, p in enumerate(w.params):
+        parts = p.name.split(".")
+        if parts[0] in ("layers", "h") and len(parts) > 1 and parts[1].isdigit():
+            blocks.setdefault(int(parts[1]), []).append(i)
+        else:
+            root.append(i)
+    return [blocks[k] for k in sorted(blocks)] + [root]
+
+
 def sweep_workload(S, world):
     """A one-tensor parameter list whose padded flat buffer is world*S."""
     return Workload(f"sweep-S{S}-N{world}", f"sweep shard {S} x N={world}",

@@ -527,8 +527,8 @@ def pin_ledger_pages(o):
     check("zero3_dp8_bytes_per_param", bpp(3, 8))
     check("zero3_dp8_7B_GB", 7e9 * bpp(3, 8) / 1e9)
     check("lifecycle_zero3_per_param", bpp(3, 8) * 8)
-    # The 70B ZeRO-3 sentence: its own formula gives 140 GB per rank; the
-    # printed 17.5 GB each is the bf16 parameter shard alone.
+    # The 70B ZeRO-3 figures: the page's own formula gives 140 GB per rank;
+    # its per-card 17.5 GB is the bf16 parameter shard alone.
     assert abs(70e9 * bpp(3, 8) / 1e9 - 140.0) < 1e-9
     check("zero3_dp8_70B_params_GB", 70e9 * 2 / 8 / 1e9)
     plan = o.plan(QWEN25_3B.numels, QWEN25_3B.tied_to, world=4)
@@ -881,6 +881,185 @@ def pin_accum_ddp_equivalence(o, w=TINY, G=3, steps=2):
                                       full_st[i].view(np.uint32)), f"state {i} differs at t={t}"
 
 
+# ------------------------------------------- per-parameter row sharding ----
+def _rows_case_bits(rng, rp, numels, elem):
+    """Random bit patterns for each owner parameter (uint8 views)."""
+    out = []
+    for i, n in enumerate(numels):
+        tied = rp["tied"] is not None and rp["tied"][i] >= 0
+        out.append(None if tied else rng.integers(0, 256, size=n * elem, dtype=np.uint8))
+    return out
+
+
+def pin_rows_bruteforce(o):
+    """All lists of up to 2 parameters (dim0 0..5, 1..3 elements per row, with
+    and without a tie), N in 1..5, align in {1, 4}: c = ceil(dim0/N), the N
+    chunks tile the rows exactly once (empty chunks for high ranks), S is the
+    least multiple of align holding the chunks, and shard -> gather -> unshard
+    is the identity on random bits with zero padding."""
+    rng = np.random.default_rng(5)
+    shapes = [(d, w) for d in range(0, 6) for w in range(1, 4)]
+    for k in (1, 2):
+        for combo in itertools.product(shapes, repeat=k):
+            ties_opts = [None]
+            if k == 2 and combo[0] == combo[1]:
+                ties_opts.append([-1, 0])
+            for ties in ties_opts:
+                dim0 = [d for d, _ in combo]
+                numels = [d * w for d, w in combo]
+                for world in range(1, 6):
+                    for align in (1, 4):
+                        _check_rows_case(o, rng, dim0, numels, ties, world, align)
+
+
+def _check_rows_case(o, rng, dim0, numels, ties, world, align, elem=2):
+    rp = o.rows_plan(dim0, numels, ties, world=world, align=align)
+    used = 0
+    for i, (d, n) in enumerate(zip(dim0, numels)):
+        if ties is not None and ties[i] >= 0:
+            assert rp["offsets"][i] == rp["offsets"][ties[i]]
+            continue
+        c = rp["rows_per_rank"][i]
+        assert c == -(-d // world)
+        covered = []
+        for r in range(world):
+            lo, hi = r * c, min((r + 1) * c, d)
+            covered += list(range(lo, max(lo, hi)))
+        assert covered == list(range(d))
+        assert rp["offsets"][i] == used
+        used += c * (n // d if d else 0)
+    assert rp["S"] % align == 0 and used <= rp["S"] < used + align
+    S = rp["S"]
+    params = _rows_case_bits(rng, rp, numels, elem)
+    locals_ = []
+    for r in range(world):
+        loc = np.full(S * elem, 0xEE, np.uint8)
+        o.shard_rows(rp, r, elem, params, loc)
+        locals_.append(loc)
+    gathered = np.concatenate(locals_) if locals_ else np.zeros(0, np.uint8)
+    outs = [None if p is None else np.full(p.size, 0xCD, np.uint8) for p in params]
+    o.unshard(rp, gathered, elem, outs)
+    for p, q in zip(params, outs):
+        if p is not None:
+            assert np.array_equal(p, q)
+    # padding rows and the tail are zero
+    for r, loc in enumerate(locals_):
+        mask = np.zeros(S * elem, bool)
+        for i, (d, n) in enumerate(zip(dim0, numels)):
+            if params[i] is None or d == 0:
+                continue
+            w = n // d
+            c = rp["rows_per_rank"][i]
+            rows = max(0, min((r + 1) * c, d) - r * c)
+            a = rp["offsets"][i] * elem
+            mask[a:a + rows * w * elem] = True
+        assert not loc[~mask].any(), "padding is not zero"
+
+
+def pin_rows_pages_layernorm(o):
+    """[Dissection] §7: a 768-element layer norm sharded over 64 ranks gives
+    12-element shards."""
+    g = read_golden_ledger()
+    rp = o.rows_plan([768], [768], world=64, align=1)
+    assert rp["rows_per_rank"][0] * rp["row_elems"][0] == g["layernorm_768_dp64_shard"][0]
+
+
+def pin_rows_reshard(o):
+    """Resharding to a smaller world M (an integer reshard_after_forward): the
+    M-way chunks are the full rows [r*ceil(d/M), ...), and gathering them back
+    over M ranks restores the parameters."""
+    rng = np.random.default_rng(6)
+    dim0, numels = [2048, 256, 11008, 7, 1], [2048, 256 * 2048, 11008 * 4, 7 * 3, 5]
+    elem = 2
+    full = [rng.integers(0, 256, size=n * elem, dtype=np.uint8) for n in numels]
+    for N, M in ((8, 4), (8, 2), (64, 8), (5, 3)):
+        rpN = o.rows_plan(dim0, numels, world=N, align=16)
+        rpM = o.rows_plan(dim0, numels, world=M, align=16)
+        locN = [np.zeros(rpN["S"] * elem, np.uint8) for _ in range(N)]
+        for r in range(N):
+            o.shard_rows(rpN, r, elem, full, locN[r])
+        back = [np.zeros(n * elem, np.uint8) for n in numels]
+        o.unshard(rpN, np.concatenate(locN), elem, back)
+        for r in range(M):
+            loc = np.zeros(rpM["S"] * elem, np.uint8)
+            o.shard_rows(rpM, r, elem, back, loc)
+            for i, (d, n) in enumerate(zip(dim0, numels)):
+                w, c = n // d, -(-d // M)
+                rows = max(0, min((r + 1) * c, d) - r * c)
+                a = rpM["offsets"][i] * elem
+                expect = full[i][r * c * w * elem:(r * c + rows) * w * elem]
+                assert np.array_equal(loc[a:a + rows * w * elem], expect), (N, M, r, i)
+
+
+def pin_rows_ddp_equivalence(o, steps=2):
+    """The sharded step on the row layout (each rank's slices are its chunks of
+    the N source ranks' gradients), gathered and copied out, equals the
+    unsharded DDP step on every parameter, bit for bit; so do master, m, v."""
+    dim0 = [1000, 96, 96, 3, 50]
+    numels = [1000 * 64, 96 * 64, 96 * 64, 3 * 64, 50]
+    ties = [-1, -1, 1, -1, -1]
+    N = 4
+    rp = o.rows_plan(dim0, numels, ties, world=N, align=128)
+    S = rp["S"]
+    owners = [i for i in range(len(numels)) if ties[i] < 0]
+    fp = o.plan([numels[i] for i in owners], None, world=1, align=1)   # DDP: one flat buffer
+    P = fp["P"]
+    master_full = synth.fill(P, seed=3, stream=synth.STREAM_MASTER, sigma=0.02)
+    ddp = dict(master=master_full.copy(), m=np.zeros(P, np.float32), v=np.zeros(P, np.float32),
+               params=np.zeros(P, np.uint16))
+
+    def split(flat):
+        return [flat[fp["offsets"][k]:fp["offsets"][k] + numels[i]]
+                for k, i in enumerate(owners)]
+
+    def per_param(parts):
+        out, k = [], 0
+        for i in range(len(numels)):
+            if ties[i] >= 0:
+                out.append(None)
+            else:
+                out.append(np.ascontiguousarray(parts[k]))
+                k += 1
+        return out
+
+    state = []
+    for r in range(N):
+        st = []
+        for arr in (ddp["master"], ddp["m"], ddp["v"]):
+            loc = np.zeros(S * 4, np.uint8)
+            o.shard_rows(rp, r, 4, [None if x is None else x.view(np.uint8)
+                                    for x in per_param(split(arr))], loc)
+            st.append(loc.view(np.float32))
+        state.append(st)
+    for t in range(1, steps + 1):
+        local = [synth.fill(P, seed=3, rank=j, step=t, bf16=True) for j in range(N)]
+        o.ddp_step(world=N, P_pad=P, local_grads=local, **ddp, t=t, **HP)
+        fulls = []
+        for r in range(N):
+            slices = []
+            for j in range(N):
+                loc = np.zeros(S * 2, np.uint8)
+                o.shard_rows(rp, r, 2, [None if x is None else x.view(np.uint8)
+                                        for x in per_param(split(local[j]))], loc)
+                slices.append(loc.view(np.uint16))
+            f = np.zeros(S * N, np.uint16)
+            o.shard_step(world=N, rank=r, S=S, lo=0, hi=S, grads=slices, master=state[r][0],
+                         m=state[r][1], v=state[r][2], full_flat=f, t=t, **HP)
+            fulls.append(f[r * S:(r + 1) * S].copy())
+        gathered = np.concatenate(fulls)
+        outs = [None if ties[i] >= 0 else np.zeros(numels[i], np.uint16) for i in range(len(numels))]
+        o.unshard(rp, gathered.view(np.uint8), 2, [None if x is None else x.view(np.uint8) for x in outs])
+        for k, i in enumerate(owners):
+            assert np.array_equal(outs[i], split(ddp["params"])[k]), f"param {i} at t={t}"
+        for idx, name in enumerate(("master", "m", "v")):
+            g = np.concatenate([state[r][idx] for r in range(N)])
+            back = [None if ties[i] >= 0 else np.zeros(numels[i], np.float32) for i in range(len(numels))]
+            o.unshard(rp, g.view(np.uint8), 4, [None if x is None else x.view(np.uint8) for x in back])
+            for k, i in enumerate(owners):
+                assert np.array_equal(back[i].view(np.uint32),
+                                      split(ddp[name])[k].view(np.uint32)), f"{name} {i} t={t}"
+
+
 ALL_PINS = [
     pin_sign_law, pin_zero_grad, pin_constant_grad, pin_eps_placement, pin_lr0_wd0,
     pin_fp64_bound, pin_bias_correction_t2, pin_reduce_dyadic, pin_reduce_order,
@@ -889,5 +1068,6 @@ ALL_PINS = [
     pin_bucket_invariance, pin_sqnorm_dyadic, pin_clip_coef_closed_forms,
     pin_clip_unit_identity, pin_clip_post_norm, pin_clip_skip, pin_clip_ddp_equivalence,
     pin_accum_single_microstep_identity, pin_accum_dyadic, pin_accum_equals_merged,
-    pin_accum_first_overwrites, pin_accum_ddp_equivalence,
+    pin_accum_first_overwrites, pin_accum_ddp_equivalence, pin_rows_bruteforce,
+    pin_rows_pages_layernorm, pin_rows_reshard, pin_rows_ddp_equivalence,
 ]

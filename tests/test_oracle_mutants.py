@@ -68,6 +68,15 @@ MUTANTS = [
      "float g = accum[i] + mean;"),
     ("accumulator ignored by the step", "float g = (accum[i] + mean) * invG;",
      "float g = mean * invG;"),
+    ("row chunks rounded down", "rows_per_rank[i] = (dim0[i] + world - 1) / world;",
+     "rows_per_rank[i] = dim0[i] / world + (dim0[i] % world > 1 ? 1 : 0);"),
+    ("segment offsets count rows, not elements",
+     "local += rows_per_rank[i] * row_elems[i];", "local += rows_per_rank[i];"),
+    ("local padding left uninitialised",
+     "std::memset(local, 0, (size_t)S * elem_size);", "(void)0;"),
+    ("copy-out ignores the rank's row offset",
+     "uint8_t* dst = static_cast<uint8_t*>(params[i]) + (size_t)r * rows_per_rank[i] * row_bytes;",
+     "uint8_t* dst = static_cast<uint8_t*>(params[i]) + (size_t)r * row_bytes;"),
 ]
 
 
