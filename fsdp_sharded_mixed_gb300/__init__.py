@@ -171,9 +171,10 @@ def _stream(stream):
 class Plan:
     """Owns a ``zs_plan*``; freed when garbage-collected or by ``free()``."""
 
-    def __init__(self, handle, n_params):
+    def __init__(self, handle, n_params, rows=False):
         self.handle = handle
         self.n_params = n_params
+        self.rows = rows  # made by zs_rows_plan (per-parameter row sharding)
         info = zs_plan_info(self)
         self.P, self.P_pad, self.S = info["P"], info["P_pad"], info["S"]
         self.n_buckets, self.world = info["n_buckets"], info["world"]
@@ -208,7 +209,7 @@ def zs_rows_plan(dim0, numels, tied_to=None, world=1, align_elems=128):
     ties = None if tied_to is None else (ctypes.c_int32 * max(n, 1))(*tied_to)
     out = ctypes.c_void_p()
     _check(lib().zs_rows_plan(d, arr, ties, n, world, align_elems, ctypes.byref(out)))
-    return Plan(out.value, n)
+    return Plan(out.value, n, rows=True)
 
 
 def zs_plan_rows(plan):
@@ -337,9 +338,11 @@ def zs_gather_assemble(plan, rank, shard_srcs, full_flat, param_dtype, stream=No
     """Enqueue the assembly of the other ranks' shards into ``full_flat``;
     return the per-parameter device addresses (the unflattened views)."""
     srcs = (ctypes.c_void_p * max(len(shard_srcs), 1))(*[_ptr(s) for s in shard_srcs])
-    views = (ctypes.c_void_p * max(plan.n_params, 1))()
+    views = None if plan.rows else (ctypes.c_void_p * max(plan.n_params, 1))()
     _check(lib().zs_gather_assemble(plan.handle, rank, srcs, _ptr(full_flat), param_dtype,
                                     views, _stream(stream)))
+    if views is None:  # row-sharded: the buffer is rank-major; see zs_unshard
+        return None
     return [v or 0 for v in list(views)[:plan.n_params]]
 
 

@@ -539,8 +539,9 @@ zs_status check_rows_params(const zs_plan* plan, const void* const* params, int 
     if (plan->owner[i] != i || plan->numels[i] == 0) continue;
     const void* q = params[i];
     if (!q) return zs::fail(ZS_ERR_INVAL, "%s: params[%d] is NULL", fn, i);
-    if ((uintptr_t)q % (uintptr_t)pb)
-      return zs::fail(ZS_ERR_ALIGN, "%s: params[%d] is not %d-byte aligned", fn, i, pb);
+    const uintptr_t need = pb == 3 ? 1u : (uintptr_t)pb;  // 3-byte elements: any byte
+    if ((uintptr_t)q % need)
+      return zs::fail(ZS_ERR_ALIGN, "%s: params[%d] is not %d-byte aligned", fn, i, (int)need);
     const int64_t bytes = plan->numels[i] * pb;
     ranges->push_back({(uintptr_t)q, (uintptr_t)q + (uint64_t)bytes, "params", i, output});
     if (zs_status st = check_device_buffer(q, bytes, fn, "params", i)) return st;
