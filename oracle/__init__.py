@@ -264,6 +264,51 @@ class Oracle:
                                  rp["n"], rank, rp["S"], elem_size, self._ptrs(params),
                                  local.ctypes.data)
 
+    # -- sharded checkpoint: what a restore must produce ------------------
+    # "从 Data Parallel 到 ZeRO/FSDP", "Checkpoint 不能假设每个 Rank 都有完整模型":
+    # each rank's shard is a piece of global tensors that the metadata
+    # describes; a restore into another world size (or layout) is the same
+    # global tensors cut the new way. Written here as exactly that: gather the
+    # global tensors from all old shards, then cut the new rank's shard.
+    # A layout is ("flat", numels, tied, world, align) or ("rows", rows_plan dict).
+    def global_params(self, layout, shards):
+        """The fp32 tensors of every owner parameter from all ranks' shards
+        (None for tied entries)."""
+        if layout[0] == "flat":
+            _, numels, tied, world, align = layout
+            pl = self.plan(numels, tied, world=world, align=align)
+            flat = np.concatenate([np.ascontiguousarray(s[:pl["S"]]) for s in shards])
+            return [None if (tied is not None and tied[i] >= 0) else
+                    flat[pl["offsets"][i]:pl["offsets"][i] + numels[i]].copy()
+                    for i in range(len(numels))]
+        rp = layout[1]
+        gathered = np.concatenate([np.ascontiguousarray(s[:rp["S"]]) for s in shards])
+        params = [None if (rp["tied"] is not None and rp["tied"][i] >= 0) else
+                  np.zeros(int(rp["dim0"][i] * rp["row_elems"][i]), np.float32)
+                  for i in range(rp["n"])]
+        self.unshard(rp, gathered.view(np.uint8), 4,
+                     [None if p is None else p.view(np.uint8) for p in params])
+        return params
+
+    def shard_of(self, layout, params, rank):
+        """Rank ``rank``'s fp32 shard of the given global tensors (padding 0)."""
+        if layout[0] == "flat":
+            _, numels, tied, world, align = layout
+            pl = self.plan(numels, tied, world=world, align=align)
+            flat = np.zeros(pl["P_pad"], np.float32)
+            for i, p in enumerate(params):
+                if p is not None:
+                    flat[pl["offsets"][i]:pl["offsets"][i] + numels[i]] = p
+            return flat[rank * pl["S"]:(rank + 1) * pl["S"]].copy()
+        rp = layout[1]
+        local = np.zeros(rp["S"], np.float32)
+        self.shard_rows(rp, rank, 4, [None if p is None else p.view(np.uint8) for p in params],
+                        local.view(np.uint8))
+        return local
+
+    def reshard(self, old_layout, old_shards, new_layout, rank):
+        return self.shard_of(new_layout, self.global_params(old_layout, old_shards), rank)
+
     # -- O6 gather -------------------------------------------------------
     def gather(self, *, world, S, elem_size, shards, full_flat):
         self.L.oracle_gather(world, S, elem_size, self._ptrs(shards), full_flat.ctypes.data)

@@ -1060,6 +1060,152 @@ def pin_rows_ddp_equivalence(o, steps=2):
                                       split(ddp[name])[k].view(np.uint32)), f"{name} {i} t={t}"
 
 
+# ------------------------------------------------ sharded checkpoint ----
+def _codes(numels, ties, start=1):
+    """Distinct float32 codes per element of every owner parameter."""
+    out, c = [], start
+    for n, t in zip(numels, ties):
+        if t >= 0:
+            out.append(None)
+            continue
+        out.append(np.arange(c, c + n, dtype=np.float32))
+        c += n
+    return out
+
+
+def pin_reshard_hand_examples(o):
+    """Restores worked by hand from the definition (each shard a piece of the
+    global tensors, cut again for the new world or layout):
+    flat [5, 3] over 2 ranks -> 3 ranks; FSDP2 rows (A: 3 rows x 2, B: 1 row
+    x 4) over 2 ranks -> flat over 1 and over 4 ranks; a tied list."""
+    flat2 = ("flat", [5, 3], None, 2, 1)
+    old = [np.array([1, 2, 3, 4], np.float32), np.array([5, 6, 7, 8], np.float32)]
+    assert o.global_params(flat2, old)[1].tolist() == [6, 7, 8]
+    want3 = [[1, 2, 3], [4, 5, 6], [7, 8, 0]]
+    for r in range(3):
+        assert o.reshard(flat2, old, ("flat", [5, 3], None, 3, 1), r).tolist() == want3[r]
+    rp = o.rows_plan([3, 1], [6, 4], None, world=2, align=1)
+    assert rp["S"] == 8
+    A, B = np.arange(1, 7, dtype=np.float32), np.arange(7, 11, dtype=np.float32)
+    rows = ("rows", rp)
+    old = [o.shard_of(rows, [A, B], r) for r in range(2)]
+    assert old[0].tolist() == [1, 2, 3, 4, 7, 8, 9, 10]
+    assert old[1].tolist() == [5, 6, 0, 0, 0, 0, 0, 0]
+    assert o.reshard(rows, old, ("flat", [6, 4], None, 1, 1), 0).tolist() == list(range(1, 11))
+    want4 = [[1, 2, 3], [4, 5, 6], [7, 8, 9], [10, 0, 0]]
+    for r in range(4):
+        assert o.reshard(rows, old, ("flat", [6, 4], None, 4, 1), r).tolist() == want4[r]
+    tied = ("flat", [4, 2, 4], [-1, -1, 0], 2, 1)
+    old = [np.array([1, 2, 3], np.float32), np.array([4, 5, 6], np.float32)]
+    got = o.global_params(tied, old)
+    assert got[0].tolist() == [1, 2, 3, 4] and got[1].tolist() == [5, 6] and got[2] is None
+    assert o.reshard(tied, old, ("flat", [4, 2, 4], [-1, -1, 0], 1, 1), 0).tolist() == \
+        [1, 2, 3, 4, 5, 6]
+
+
+def _random_layouts(o, rng, dims, numels, ties):
+    out = []
+    for _ in range(3):
+        world = int(rng.choice([1, 2, 3, 4, 8, 16]))
+        align = int(rng.choice([1, 4, 128]))
+        if rng.random() < 0.5:
+            out.append(("flat", numels, ties, world, align))
+        else:
+            out.append(("rows", o.rows_plan(dims, numels, ties, world=world, align=align)))
+    return out
+
+
+def _world(layout):
+    return layout[3] if layout[0] == "flat" else layout[1]["world"]
+
+
+def pin_reshard_invariants(o):
+    """For random parameter lists and layouts: a restore into the same layout
+    returns every shard unchanged; old -> new -> old is the identity; across
+    the new ranks every element code appears exactly once and everything
+    else is padding (0)."""
+    rng = np.random.default_rng(41)
+    for case in range(25):
+        k = int(rng.integers(1, 7))
+        dims, numels, ties = [], [], []
+        for i in range(k):
+            if i > 0 and rng.random() < 0.2:
+                j = int(rng.integers(0, i))
+                while ties[j] >= 0:
+                    j = ties[j]
+                dims.append(dims[j]); numels.append(numels[j]); ties.append(j)
+                continue
+            d = int(rng.integers(0, 40))
+            dims.append(d); numels.append(d * int(rng.integers(1, 9))); ties.append(-1)
+        codes = _codes(numels, ties)
+        total = sum(len(c) for c in codes if c is not None)
+        a, b, _ = _random_layouts(o, rng, dims, numels, ties)
+        A = [o.shard_of(a, codes, r) for r in range(_world(a))]
+        for r in range(_world(a)):
+            assert np.array_equal(o.reshard(a, A, a, r), A[r]), (case, "identity")
+        Bs = [o.reshard(a, A, b, r) for r in range(_world(b))]
+        back = [o.reshard(b, Bs, a, r) for r in range(_world(a))]
+        for r in range(_world(a)):
+            assert np.array_equal(back[r], A[r]), (case, "round trip")
+        allv = np.concatenate(Bs)
+        nz = np.sort(allv[allv != 0])
+        assert np.array_equal(nz, np.arange(1, total + 1, dtype=np.float32)), case
+
+
+def pin_reshard_next_update(o, steps=3):
+    """The pages' test of a restore: the next update after it equals that of
+    the uninterrupted run. N = 4 ranks take three steps; the state is
+    restored into M = 2 ranks (and into the row layout over 8); step 4 with
+    every rank's gradient equal to the same bf16 x (so the mean is exactly x
+    at any power-of-two world) gives the uninterrupted run's global master,
+    m, v and parameters, bit for bit."""
+    w = TINY
+    numels, ties = w.numels, w.tied_to
+    N = 4
+    fl = ("flat", numels, ties, N, w.align)
+    pl = o.plan(numels, ties, world=N, align=w.align)
+    S, P = pl["S"], pl["P"]
+    st = [[synth.fill(S, index0=r * S, seed=2, stream=synth.STREAM_MASTER, sigma=0.02,
+                      p_limit=P), np.zeros(S, np.float32), np.zeros(S, np.float32)]
+          for r in range(N)]
+
+    def step(state, t, grads_of_rank, world):
+        Sx = state[0][0].size
+        fulls = []
+        for r in range(world):
+            f = np.zeros(Sx * world, np.uint16)
+            o.shard_step(world=world, rank=r, S=Sx, lo=0, hi=Sx, grads=grads_of_rank(r),
+                         master=state[r][0], m=state[r][1], v=state[r][2], full_flat=f, t=t,
+                         **HP)
+            fulls.append(f[r * Sx:(r + 1) * Sx])
+        return fulls
+
+    for t in range(1, steps + 1):
+        step(st, t, lambda r: [synth.fill(S, index0=r * S, seed=2, rank=j, step=t,
+                                              p_limit=P, bf16=True) for j in range(N)], N)
+    x_full = synth.fill(pl["P_pad"], seed=9, step=99, p_limit=P, bf16=True)
+    cont = [[a.copy() for a in s] for s in st]
+    step(cont, steps + 1, lambda r: [x_full[r * S:(r + 1) * S]] * N, N)
+    want = [o.global_params(fl, [cont[r][k] for r in range(N)]) for k in range(3)]
+    # x per parameter as fp32 (bf16 bits widened), to cut for the new layouts
+    x32 = (x_full.astype(np.uint32) << 16).view(np.float32)
+    x_params = o.global_params(fl, [x32[r * S:(r + 1) * S] for r in range(N)])
+    dims = [p.shape[0] for p in w.params]
+    for new in (("flat", numels, ties, 2, w.align),
+                ("rows", o.rows_plan(dims, numels, ties, world=8, align=w.align))):
+        M = _world(new)
+        rs = [[o.reshard(fl, [st[r][k] for r in range(N)], new, q) for k in range(3)]
+              for q in range(M)]
+        xq = [o.shard_of(new, x_params, q) for q in range(M)]
+        bits = [o.bf16(x) for x in xq]   # x is bf16-exact: the cast gives it back
+        step(rs, steps + 1, lambda q: [bits[q]] * M, M)
+        for k, name in enumerate(("master", "m", "v")):
+            got = o.global_params(new, [rs[q][k] for q in range(M)])
+            for i, (g, e) in enumerate(zip(got, want[k])):
+                if e is not None:
+                    assert np.array_equal(g.view(np.uint32), e.view(np.uint32)), (new[0], name, i)
+
+
 ALL_PINS = [
     pin_sign_law, pin_zero_grad, pin_constant_grad, pin_eps_placement, pin_lr0_wd0,
     pin_fp64_bound, pin_bias_correction_t2, pin_reduce_dyadic, pin_reduce_order,
@@ -1070,4 +1216,5 @@ ALL_PINS = [
     pin_accum_single_microstep_identity, pin_accum_dyadic, pin_accum_equals_merged,
     pin_accum_first_overwrites, pin_accum_ddp_equivalence, pin_rows_bruteforce,
     pin_rows_pages_layernorm, pin_rows_reshard, pin_rows_ddp_equivalence,
+    pin_reshard_hand_examples, pin_reshard_invariants, pin_reshard_next_update,
 ]
