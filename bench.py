@@ -603,6 +603,165 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def run_checkpoint(args, w):
+    """--pipeline checkpoint: one rank's fp32 master/m/v shard (device-resident)
+    saved to a file, restored at the same world size, and restored into a
+    world of N/2 (its rank 0 reads old ranks 0 and 1). Wall-clock GB/s of
+    state bytes per leg, beside plain multi-threaded file writes/reads of the
+    same bytes on the same file system (the I/O bound of a leg). The legs are
+    host I/O; rank 0 alone runs them."""
+    import shutil
+    import tempfile
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+    import torch
+
+    import fsdp_sharded_mixed_gb300 as zs
+    import synth
+
+    grank, gworld, local = dist_env()
+    if grank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sptr = torch.cuda.current_stream().cuda_stream
+    plan = zs.zs_flatten_plan(w.numels, w.tied_to, world=w.world, align_elems=w.align)
+    N, S, P = plan.world, plan.S, plan.P
+    M = max(1, N // 2)
+    planM = zs.zs_flatten_plan(w.numels, w.tied_to, world=M, align_elems=w.align)
+    state_bytes = 3 * 4 * S
+    d = args.ckpt_dir or os.path.join(tempfile.gettempdir(), "zs_ckpt_bench")
+    os.makedirs(d, exist_ok=True)
+    need = 3 * state_bytes + (1 << 30)
+    free = shutil.disk_usage(d).free
+    if free < need:
+        print(json.dumps({"metric": "sharded checkpoint GB/s", "unavailable":
+                          f"needs {need / 1e9:.1f} GB free in {d}, has {free / 1e9:.1f} GB"}))
+        return
+    st = [torch.empty(S, device=dev) for _ in range(3)]
+    for k, a in enumerate(st):
+        synth.fill_device(a.data_ptr(), S, seed=w.seed + k, stream=synth.STREAM_MASTER,
+                          sigma=0.02, p_limit=P, bf16=False, cuda_stream=sptr)
+    stM = [torch.empty(planM.S, device=dev) for _ in range(3)]
+    paths = [os.path.join(d, f"{w.key}.rank{k}") for k in range(N)]
+    same = [paths[0]] + [None] * (N - 1)
+    resize = [paths[0], paths[1] if N > 1 else None] + [None] * (N - 2)
+    # (leg, call, bytes of state it moves). A save goes to a new file, as a
+    # training job's does: the previous one is removed before the clock starts.
+    legs = [
+        ("save", lambda: zs.zs_checkpoint_save(plan, 0, *st, 10, paths[0]), state_bytes),
+        ("load_same_world", lambda: zs.zs_checkpoint_load(plan, 0, same, *st), state_bytes),
+        (f"load_into_world_{M}", lambda: zs.zs_checkpoint_load(planM, 0, resize, *stM),
+         3 * 4 * planM.S),
+    ]
+    if N > 1:
+        zs.zs_checkpoint_save(plan, 1, *st, 10, paths[1])
+    warm = min(args.warmup, 3)
+    reps = args.ckpt_reps
+    results = {}
+    for name, fn, nbytes in legs:
+        ts = []
+        for i in range(warm + reps):
+            if name == "save" and os.path.exists(paths[0]):
+                os.remove(paths[0])
+            if args.ckpt_cold and name != "save":
+                for p in paths[:2]:
+                    if os.path.exists(p):
+                        fd = os.open(p, os.O_RDONLY)
+                        os.fsync(fd)
+                        os.posix_fadvise(fd, 0, 0, os.POSIX_FADV_DONTNEED)
+                        os.close(fd)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            t = time.perf_counter() - t0
+            if i >= warm:
+                ts.append(t)
+        results[name] = {"s_median": statistics.median(ts), "s_min": min(ts), "bytes": nbytes,
+                         "gbs": nbytes / statistics.median(ts) / 1e9}
+        log(f"checkpoint {name}: {results[name]}")
+    # restored state equals the saved state (same world) — a cheap end check
+    got = [torch.empty(S, device=dev) for _ in range(3)]
+    zs.zs_checkpoint_load(plan, 0, same, *got)
+    ok = all(torch.equal(a.view(torch.int32), b.view(torch.int32)) for a, b in zip(got, st))
+    del got
+    # The I/O bound of a leg on this file system: the same bytes written from
+    # host memory into a new, preallocated file by one thread in 64 MiB pwrites
+    # (the fastest way found to fill a new file), and read back by 16 threads
+    # in 8 MiB preadv calls.
+    buf = np.empty(state_bytes, np.uint8)
+    buf[::4096] = 1
+    plain = os.path.join(d, "plain.bin")
+    mv = memoryview(buf)
+
+    def plain_write():
+        fd = os.open(plain, os.O_RDWR | os.O_CREAT | os.O_TRUNC, 0o644)
+        try:
+            os.posix_fallocate(fd, 0, state_bytes)
+            for o in range(0, state_bytes, 64 << 20):
+                os.pwrite(fd, mv[o:o + (64 << 20)], o)
+        finally:
+            os.close(fd)
+
+    def plain_read():
+        fd = os.open(plain, os.O_RDONLY)
+        try:
+            with ThreadPoolExecutor(16) as ex:
+                list(ex.map(lambda o: os.preadv(fd, [mv[o:o + (8 << 20)]], o),
+                            range(0, state_bytes, 8 << 20)))
+        finally:
+            os.close(fd)
+
+    plain_t = {}
+    for kind, fn in (("write", plain_write), ("read", plain_read)):
+        ts = []
+        for i in range(warm + reps):
+            if kind == "write" and os.path.exists(plain):
+                os.remove(plain)
+            t0 = time.perf_counter()
+            fn()
+            if i >= warm:
+                ts.append(time.perf_counter() - t0)
+        plain_t[kind] = statistics.median(ts)
+    del buf
+    for p in paths[:2] + [plain]:
+        if os.path.exists(p):
+            os.remove(p)
+    w_gbs = state_bytes / plain_t["write"] / 1e9
+    r_gbs = state_bytes / plain_t["read"] / 1e9
+    for name, r in results.items():
+        r["frac_of_plain_io"] = r["gbs"] / (w_gbs if name == "save" else r_gbs)
+    value = min(r["gbs"] for r in results.values())
+    worst = min(results, key=lambda k: results[k]["gbs"])
+    line = {
+        "metric": "sharded checkpoint GB/s of fp32 optimizer state (save; restore at the same "
+                  f"world; restore into world {M}), 1 GPU",
+        "value": value, "unit": "GB/s", "n_gpus": 1, "steps": reps, "warmup": warm,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{w.key}: {w.title}", "pipeline": "checkpoint",
+                   "shard_elems": S, "state_bytes": state_bytes, "old_world": N,
+                   "new_world": M, "files": "cold (fsync + fadvise DONTNEED before each load)"
+                   if args.ckpt_cold else "warm page cache", "dir": d},
+        "legs": results, "restored_equal": ok,
+        "plain_io_gbs": {"write": w_gbs, "read": r_gbs,
+                         "note": "the same bytes from host memory: new preallocated file, one "
+                                 "writer, 64 MiB pwrite; read back by 16 threads, 8 MiB preadv"},
+        "roofline": {"bound": "io", "achieved": results[worst]["gbs"],
+                     "peak": w_gbs if worst == "save" else r_gbs, "unit": "GB/s",
+                     "frac": results[worst]["frac_of_plain_io"], "kernel": worst,
+                     "peak_source": "plain file I/O measured in this run", "traffic": None},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": state_bytes,
+                "d2h_bytes_per_step": state_bytes,
+                "note": "every leg moves the state between HBM and a file"},
+        "gpu_launches": 3 * (warm + reps), "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+    plan.free()
+    planM.free()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -612,13 +771,20 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--graph", action="store_true",
                     help="time one replay of a CUDA graph holding the K launches")
-    ap.add_argument("--pipeline", choices=["step", "clip", "accum", "unshard"], default="step",
+    ap.add_argument("--pipeline", choices=["step", "clip", "accum", "unshard", "checkpoint"],
+                    default="step",
                     help="step: the fused shard step; clip: global-norm pass + clip "
                          "coefficient + clipped step; accum: G-1 accumulations + the "
                          "accumulated step; unshard: FSDP2 copy-out of every wrap unit's "
-                         "gathered parameters")
+                         "gathered parameters; checkpoint: save / restore / resharding "
+                         "restore of one rank's optimizer state")
     ap.add_argument("--micro-steps", type=int, default=4,
                     help="G, micro-batches per optimizer step for --pipeline accum")
+    ap.add_argument("--ckpt-dir", default=None,
+                    help="directory for --pipeline checkpoint files (default: a temp dir)")
+    ap.add_argument("--ckpt-reps", type=int, default=3)
+    ap.add_argument("--ckpt-cold", action="store_true",
+                    help="drop the files from the page cache before each timed load")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--e2e-chunks", type=int, default=32)
     ap.add_argument("--no-e2e", action="store_true")
@@ -632,6 +798,8 @@ def main(argv=None):
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.pipeline == "checkpoint":
+        run_checkpoint(args, w)
     else:
         run_ours(args, w)
 

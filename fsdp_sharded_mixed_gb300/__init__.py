@@ -8,7 +8,10 @@ is no fallback: without the compiled library every call raises.
 
 Entry points: ``zs_flatten_plan`` (flat layout, rank shards, buckets),
 ``zs_shard_step`` (N-slice fp32 mean + AdamW + cast into the AllGather slot),
-``zs_gather_assemble`` (the AllGather's result and per-tensor views).
+``zs_gather_assemble`` (the AllGather's result and per-tensor views); the
+FSDP2 row layout (``zs_rows_plan``, ``zs_unshard``, ``zs_shard_rows``);
+clipping, accumulation, and the sharded checkpoint (``zs_checkpoint_save``,
+``zs_checkpoint_load``: host file I/O of host- or device-resident state).
 """
 from __future__ import annotations
 
@@ -26,6 +29,7 @@ INCLUDE = os.path.join(_ROOT, "include")
 
 ZS_OK, ZS_ERR_INVAL, ZS_ERR_ALIGN, ZS_ERR_RANGE = 0, -1, -2, -3
 ZS_ERR_CUDA, ZS_ERR_NOMEM, ZS_ERR_TIMEOUT, ZS_ERR_UNSUPPORTED = -4, -5, -6, -7
+ZS_ERR_IO, ZS_ERR_CORRUPT = -8, -9
 ZS_BF16, ZS_FP32, ZS_FP24 = 0, 1, 2
 ELEM_BYTES = {ZS_BF16: 2, ZS_FP32: 4, ZS_FP24: 3}
 ZS_MAX_WORLD = 1024
@@ -33,9 +37,9 @@ ZS_MAX_WORLD = 1024
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-fmad=false", "-prec-div=true",
               "-prec-sqrt=true", "-ftz=false", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
-CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-I/usr/local/cuda/include"]
-CUDA_SOURCES = ["shard_step.cu", "gather.cu", "clip.cu", "accum.cu", "rows.cu"]
-HOST_SOURCES = ["api.cpp", "plan.cpp"]
+CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-pthread", "-I/usr/local/cuda/include"]
+CUDA_SOURCES = ["shard_step.cu", "gather.cu", "clip.cu", "accum.cu", "rows.cu", "ckpt.cu"]
+HOST_SOURCES = ["api.cpp", "plan.cpp", "checkpoint.cpp"]
 
 
 # ----------------------------------------------------------------- build ----
@@ -119,6 +123,9 @@ EXPORTS = {
     "zs_plan_rows": ([_P, _P, _P, _I32], ctypes.c_int),
     "zs_unshard": ([_P, _P, ctypes.c_int, _P, _P], ctypes.c_int),
     "zs_shard_rows": ([_P, _I32, _P, ctypes.c_int, _P, _P], ctypes.c_int),
+    "zs_checkpoint_save": ([_P, _I32, _P, _P, _P, _I64, ctypes.c_char_p, _P], ctypes.c_int),
+    "zs_checkpoint_load": ([_P, _I32, _P, _I32, _P, _P, _P, _P, _P], ctypes.c_int),
+    "zs_checkpoint_info": ([ctypes.c_char_p, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "zs_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "zs_last_error": ([], ctypes.c_char_p),
     "zs_check_device_error": ([_P], ctypes.c_int),
@@ -151,12 +158,14 @@ def _check(status):
 
 
 def _ptr(x):
-    """Device address of a tensor (or an int address / None)."""
+    """Address of a tensor or a numpy array (or an int address / None)."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
-    return x.data_ptr()
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return x.ctypes.data
 
 
 def _stream(stream):
@@ -344,6 +353,47 @@ def zs_gather_assemble(plan, rank, shard_srcs, full_flat, param_dtype, stream=No
     if views is None:  # row-sharded: the buffer is rank-major; see zs_unshard
         return None
     return [v or 0 for v in list(views)[:plan.n_params]]
+
+
+def _io_stream(stream):
+    """The stream for a checkpoint call: as given, else the current CUDA
+    stream where there is a device, else NULL (host-resident state)."""
+    if stream is not None:
+        return _stream(stream)
+    import torch
+    return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+
+
+def zs_checkpoint_save(plan, rank, master, exp_avg, exp_avg_sq, step, path, stream=None):
+    """Write rank ``rank``'s fp32 master/exp_avg/exp_avg_sq shard (S elements
+    each; device tensors, or host tensors / numpy arrays) and the global step
+    to ``path``. Blocks until the file is complete."""
+    _check(lib().zs_checkpoint_save(plan.handle, rank, _ptr(master), _ptr(exp_avg),
+                                    _ptr(exp_avg_sq), step, os.fsencode(path),
+                                    _io_stream(stream)))
+
+
+def zs_checkpoint_load(plan, rank, paths, master, exp_avg, exp_avg_sq, stream=None):
+    """Fill rank ``rank``'s shard of ``plan`` from the files of the old ranks
+    (``paths[k]`` = old rank k's file; None for a file this rank does not
+    need, never for rank 0); returns the saved step."""
+    arr = (ctypes.c_char_p * max(len(paths), 1))(
+        *[None if p is None else os.fsencode(p) for p in paths])
+    step = ctypes.c_int64()
+    _check(lib().zs_checkpoint_load(plan.handle, rank, arr, len(paths), _ptr(master),
+                                    _ptr(exp_avg), _ptr(exp_avg_sq), ctypes.byref(step),
+                                    _io_stream(stream)))
+    return step.value
+
+
+def zs_checkpoint_info(path):
+    w, r, lay, n = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    P, S, step = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().zs_checkpoint_info(os.fsencode(path), ctypes.byref(w), ctypes.byref(r),
+                                    ctypes.byref(lay), ctypes.byref(n), ctypes.byref(P),
+                                    ctypes.byref(S), ctypes.byref(step)))
+    return dict(world=w.value, rank=r.value, layout=lay.value, n_params=n.value, P=P.value,
+                S=S.value, step=step.value)
 
 
 def zs_check_device_error(stream=None):

@@ -105,6 +105,10 @@ double pow_binary(double base, int64_t e) {
 
 namespace zs {
 
+zs_status check_device_array(const void* p, int64_t bytes, const char* fn, const char* name) {
+  return check_device_buffer(p, bytes, fn, name, 0);
+}
+
 zs_status fail(zs_status st, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -657,6 +661,8 @@ extern "C" const char* zs_status_string(zs_status st) {
     case ZS_ERR_NOMEM: return "out of host memory";
     case ZS_ERR_TIMEOUT: return "device wait timed out";
     case ZS_ERR_UNSUPPORTED: return "unsupported";
+    case ZS_ERR_IO: return "file I/O failed";
+    case ZS_ERR_CORRUPT: return "checkpoint corrupt or inconsistent";
   }
   return "unknown status";
 }

@@ -112,6 +112,18 @@ struct RowSegment {
 constexpr int kMaxSegs = 256;
 cudaError_t launch_segment_copy(const RowSegment* segs, int n, cudaStream_t stream);
 
+// Block checksums of checkpoint data (ckpt.cu, definition in block_hash.h):
+// out[j] = hash of bytes [j*block_bytes, min((j+1)*block_bytes, bytes)) of
+// `data` (16-byte aligned) as block first_block + j of array `array_id`.
+cudaError_t launch_block_hash(const void* data, int64_t bytes, int64_t first_block,
+                              int64_t block_bytes, uint32_t array_id, uint64_t* out,
+                              cudaStream_t stream);
+
+// Argument checks of the C-ABI layer, for the other host translation units:
+// device-resident on the current device and (where the driver can tell)
+// [p, p + bytes) inside one allocation.
+zs_status check_device_array(const void* p, int64_t bytes, const char* fn, const char* name);
+
 // Device error word (set by bounds-checked builds and bounded waits).
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* word);
 

@@ -17,9 +17,11 @@
  *   - Returns zs_status: 0 on success, a negative code on error. No call
  *     aborts or exits; zs_last_error() gives a one-line detail (per thread).
  *   - Device buffers and CUDA streams are owned by the caller. The library
- *     allocates host memory for plans only and never allocates device memory.
+ *     allocates host memory for plans (and staging inside the checkpoint
+ *     calls); it never allocates device memory.
  *   - Calls that take a stream enqueue work on it and return without
- *     synchronising; `cuda_stream` is a cudaStream_t (NULL = legacy default).
+ *     synchronising (but for the checkpoint calls, which block); `cuda_stream`
+ *     is a cudaStream_t (NULL = legacy default).
  *     Launch failures return ZS_ERR_CUDA.
  *   - Device pointers must be 16-byte aligned, resident on the current device,
  *     and (checked, where the driver can tell) cover the bytes the call uses;
@@ -44,7 +46,10 @@ typedef enum {
   ZS_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed */
   ZS_ERR_NOMEM = -5,       /* host allocation for a plan failed */
   ZS_ERR_TIMEOUT = -6,     /* a bounded device-side wait gave up */
-  ZS_ERR_UNSUPPORTED = -7  /* combination not built into this library */
+  ZS_ERR_UNSUPPORTED = -7, /* combination not built into this library */
+  ZS_ERR_IO = -8,          /* a checkpoint file could not be opened, read or written */
+  ZS_ERR_CORRUPT = -9      /* a checkpoint file fails a check (format, size, checksum,
+                              disagreement between the ranks' files) */
 } zs_status;
 
 /* Element types. ZS_FP24 is a 3-byte float: the top 24 bits of an fp32
@@ -307,7 +312,58 @@ zs_status zs_unshard(const zs_plan* plan, const void* gathered, zs_dtype dtype,
 zs_status zs_shard_rows(const zs_plan* plan, int32_t rank, const void* const* params_in,
                         zs_dtype dtype, void* local_out, void* cuda_stream);
 
-/* Diagnostics. *//* Diagnostics. *//* Diagnostics. */
+/* -------------------------------------------------------------------------
+ * Sharded checkpoint and resharding restore. [DP-to-ZeRO] "Checkpoint 不能假设
+ * 每个 Rank 都有完整模型": with sharded state each rank saves its own shards
+ * plus the metadata that places them in the global tensors; a restore into
+ * another world size reshards; a consistent checkpoint holds the master
+ * weights, the optimizer moments, the global step and the sharding metadata;
+ * and a restore is right only when the next update equals that of the
+ * uninterrupted run (its "常见误区" section). Its landing path, step 10: save,
+ * fault injection, restore at the same and at another world size.
+ *
+ * One file per rank holds: a header (format version, layout, world, rank,
+ * P, S, step), the parameter list with the plan's layout, the fp32 master /
+ * exp_avg / exp_avg_sq shard (S elements each), and a 64-bit checksum per
+ * 1 MiB block of each array. Element e of parameter i has one place in the
+ * global tensor in every layout, so a file saved under one plan loads into
+ * any plan over the same parameter list (numels and ties equal): another
+ * world size, and flat <-> row layouts. The new shard's padding is zeroed.
+ *
+ * State arrays are all device memory (current device, 16-byte aligned) or
+ * all host memory. Device-resident state moves through pinned host staging
+ * (these calls allocate pinned host memory for their duration and no device
+ * memory); saving hashes the blocks on the device, and so does loading for
+ * every block that lands whole in the device arrays. Both calls block until
+ * done, enqueueing their device work on `cuda_stream` and synchronising it.
+ * Not thread-safe for one path. Errors: ZS_ERR_IO (open/read/write),
+ * ZS_ERR_CORRUPT (bad magic or version, header or metadata checksum, file
+ * size, block checksum, files of different steps or layouts, a file in the
+ * wrong rank's place), ZS_ERR_INVAL (the parameter list differs from the
+ * plan's, NULL arguments, mixed host/device arrays).
+ * ------------------------------------------------------------------------- */
+/* Writes rank `rank`'s shard of `plan` (S fp32 elements per array) and `step`
+ * to `path`, through `path` + ".part" renamed on success (no torn file under
+ * the final name; the file is not fsync'ed). */
+zs_status zs_checkpoint_save(const zs_plan* plan, int32_t rank, const float* master,
+                             const float* exp_avg, const float* exp_avg_sq, int64_t step,
+                             const char* path, void* cuda_stream);
+/* Fills rank `rank`'s shard of `plan` from the files saved by the old ranks:
+ * paths[k] = old rank k's file, n_paths = the old world. Entries of old ranks
+ * whose elements this rank does not hold may be NULL (paths[0] never: it fixes
+ * the old layout). Every block read is checked against its checksum (on the
+ * device after it lands, or on the host before it is copied); on
+ * ZS_ERR_CORRUPT / ZS_ERR_IO the arrays may hold partial data. *step = the
+ * saved step (may be NULL). */
+zs_status zs_checkpoint_load(const zs_plan* plan, int32_t rank, const char* const* paths,
+                             int32_t n_paths, float* master, float* exp_avg, float* exp_avg_sq,
+                             int64_t* step, void* cuda_stream);
+/* The header of a checkpoint file, checked (any output may be NULL). layout:
+ * 0 flat, 1 rows. */
+zs_status zs_checkpoint_info(const char* path, int32_t* world, int32_t* rank, int32_t* layout,
+                             int32_t* n_params, int64_t* P, int64_t* S, int64_t* step);
+
+/* Diagnostics. */
 const char* zs_status_string(zs_status status);
 const char* zs_last_error(void);
 /* Synchronises `cuda_stream`, then reads and clears this device's error word
