@@ -271,19 +271,22 @@ def run_ours(args, w):
     G = max(1, args.micro_steps)
 
     # Inputs resident in HBM: one set of incoming slices, master from the
-    # generator, zero moments, the full AllGather buffer.
-    grads = [torch.empty(S, dtype=torch.int16, device=dev) for _ in range(N)]
-    for j, g in enumerate(grads):
-        synth.fill_device(g.data_ptr(), S, index0=r * S, seed=w.seed, rank=j, step=1,
-                          sigma=w.grad_sigma, p_limit=P, outlier_frac=w.outlier_frac,
-                          outlier_scale=w.outlier_scale, bf16=True, cuda_stream=sptr)
-    master = torch.empty(S, dtype=torch.float32, device=dev)
-    synth.fill_device(master.data_ptr(), S, index0=r * S, seed=w.seed,
-                      stream=synth.STREAM_MASTER, sigma=w.master_sigma, p_limit=P,
-                      bf16=False, cuda_stream=sptr)
-    m = torch.zeros(S, dtype=torch.float32, device=dev)
-    v = torch.zeros(S, dtype=torch.float32, device=dev)
-    full = torch.zeros(plan.P_pad, dtype=torch.int16, device=dev)
+    # generator, zero moments, the full AllGather buffer (not needed by the
+    # copy-out pipeline, which holds its own per-unit buffers).
+    grads = master = m = v = full = None
+    if args.pipeline != "unshard":
+        grads = [torch.empty(S, dtype=torch.int16, device=dev) for _ in range(N)]
+        for j, g in enumerate(grads):
+            synth.fill_device(g.data_ptr(), S, index0=r * S, seed=w.seed, rank=j, step=1,
+                              sigma=w.grad_sigma, p_limit=P, outlier_frac=w.outlier_frac,
+                              outlier_scale=w.outlier_scale, bf16=True, cuda_stream=sptr)
+        master = torch.empty(S, dtype=torch.float32, device=dev)
+        synth.fill_device(master.data_ptr(), S, index0=r * S, seed=w.seed,
+                          stream=synth.STREAM_MASTER, sigma=w.master_sigma, p_limit=P,
+                          bf16=False, cuda_stream=sptr)
+        m = torch.zeros(S, dtype=torch.float32, device=dev)
+        v = torch.zeros(S, dtype=torch.float32, device=dev)
+        full = torch.zeros(plan.P_pad, dtype=torch.int16, device=dev)
 
     # Clipping: this rank's partial sum of squares, the N partials (the other
     # ranks' as if every shard had this one's norm: the scalar AllReduce of a
@@ -330,12 +333,14 @@ def run_ours(args, w):
 
     units = []
     up_dims = {}
+    unit_params = []
     if args.pipeline == "unshard":
         # FSDP2's gather side over the whole model: per wrap unit a row-sharded
         # plan, the rank-major AllGather buffer (filled once from the
         # generator), and the unit's full parameters, written by the copy-out.
         from synth.workloads import wrap_units
-        for idx in wrap_units(w):
+        all_units = wrap_units(w)
+        for idx in all_units[:args.units] if args.units else all_units:
             local_of = {g_: k for k, g_ in enumerate(idx)}
             ps = [w.params[i] for i in idx]
             ties_u = [local_of[p.tied_to] if p.tied_to >= 0 else -1 for p in ps]
@@ -348,6 +353,7 @@ def run_ours(args, w):
                     for p, t in zip(ps, ties_u)]
             units.append((up, gbuf, outs))
             up_dims[id(up)] = [p.shape[0] for p in ps]
+            unit_params.extend(i for i, t in zip(idx, ties_u) if t < 0)
         torch.cuda.synchronize()
 
     def _segments(up, outs):
@@ -362,7 +368,7 @@ def run_ours(args, w):
     if args.pipeline == "unshard":
         # bytes per shard element of the workload's plan: every parameter
         # element read once from the gathered buffer and written once.
-        unit_bytes = 4 * sum(p.numel for p in w.params if p.tied_to < 0)
+        unit_bytes = 4 * sum(w.params[i].numel for i in unit_params)
         pipeline = [("segment_copy_kernel", part_unshard, unit_bytes / S)]
         launches_per_step = 0
         for up, _, outs in units:   # one launch per 256 (parameter, rank) row segments
@@ -595,6 +601,9 @@ def run_ours(args, w):
             line["config"]["clip_max_norm"] = max_norm
         if accum_mode:
             line["config"]["micro_steps"] = G
+        if args.pipeline == "unshard":
+            line["config"]["wrap_units"] = len(units)
+            line["config"]["unit_param_bytes"] = unit_bytes // 2
         print(json.dumps(line), flush=True)
     del grads, master, m, v, full
     plan.free()
@@ -778,6 +787,8 @@ def main(argv=None):
                          "accumulated step; unshard: FSDP2 copy-out of every wrap unit's "
                          "gathered parameters; checkpoint: save / restore / resharding "
                          "restore of one rank's optimizer state")
+    ap.add_argument("--units", type=int, default=0,
+                    help="--pipeline unshard: only the first K wrap units (0 = all)")
     ap.add_argument("--micro-steps", type=int, default=4,
                     help="G, micro-batches per optimizer step for --pipeline accum")
     ap.add_argument("--ckpt-dir", default=None,

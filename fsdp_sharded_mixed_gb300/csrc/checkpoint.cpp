@@ -571,35 +571,38 @@ extern "C" zs_status zs_checkpoint_save(const zs_plan* plan, int32_t rank, const
   h.meta_hash = host_hash(meta.data(), (int64_t)meta.size(), 0, kBlock, kMetaId);
   h.header_hash = header_hash_of(h);
 
-  // Block checksums: on the device into mapped pinned memory, or on the host.
-  uint64_t* table = nullptr;
+  // Block checksums: on the device (per-block partial sums into mapped pinned
+  // memory, added up once the stream is done), or on the host.
   std::vector<uint64_t> host_table;
+  try {
+    host_table.resize((size_t)(kArrays * nb));
+  } catch (...) {
+    return zs::fail(ZS_ERR_NOMEM, "%s: out of host memory", fn);
+  }
+  uint64_t* table = host_table.data();
+  uint64_t* partials = nullptr;
   struct PinnedFree {
     void* p = nullptr;
     ~PinnedFree() {
       if (p) cudaFreeHost(p);
     }
-  } table_guard;
+  } partials_guard;
+  const int parts = device && nb > 0 ? zs::block_hash_parts(nb, kBlock) : 1;
   if (device && nb > 0) {
-    cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&table), (size_t)(kArrays * nb * 8),
-                                  cudaHostAllocMapped);
+    cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&partials),
+                                  (size_t)(kArrays * nb * parts * 8), cudaHostAllocMapped);
     if (e != cudaSuccess) return cuda_fail(fn, "checksum table", e);
-    table_guard.p = table;
-    uint64_t* dtable = nullptr;
-    e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&dtable), table, 0);
+    partials_guard.p = partials;
+    uint64_t* dpartials = nullptr;
+    e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&dpartials), partials, 0);
     for (int a = 0; a < kArrays && e == cudaSuccess; ++a)
-      e = zs::launch_block_hash(arrays[a], bytes, 0, kBlock, (uint32_t)a, dtable + a * nb, stream);
+      e = zs::launch_block_hash(arrays[a], bytes, 0, kBlock, (uint32_t)a, parts,
+                                dpartials + a * nb * parts, stream);
     if (e != cudaSuccess) {
       cudaStreamSynchronize(stream);
       return cuda_fail(fn, "checksum kernel", e);
     }
   } else if (nb > 0) {
-    try {
-      host_table.resize((size_t)(kArrays * nb));
-    } catch (...) {
-      return zs::fail(ZS_ERR_NOMEM, "%s: out of host memory", fn);
-    }
-    table = host_table.data();
     Pool pool(pool_threads());
     pool.run(kArrays * nb, [&](int64_t j) {
       const int64_t a = j / nb, b = j % nb, off = b * kBlock;
@@ -679,10 +682,15 @@ extern "C" zs_status zs_checkpoint_save(const zs_plan* plan, int32_t rank, const
     }
   }
   if (device) {
-    const cudaError_t e = cudaStreamSynchronize(stream);  // the checksum table is complete
+    const cudaError_t e = cudaStreamSynchronize(stream);  // the partial sums are complete
     if (e != cudaSuccess) {
       abandon();
       return cuda_fail(fn, "stream", e);
+    }
+    for (int64_t j = 0; partials && j < kArrays * nb; ++j) {
+      uint64_t sum = 0;
+      for (int p = 0; p < parts; ++p) sum += partials[j * parts + p];
+      table[j] = sum;
     }
   }
   if (nb > 0 && !pwrite_full(f.fd, table, kArrays * nb * 8, h.table_offset))
@@ -865,11 +873,13 @@ extern "C" zs_status zs_checkpoint_load(const zs_plan* plan, int32_t rank,
   // hash kernel reads them where they landed in HBM, so for them the host
   // only reads the file; every other block read is hashed on the host.
   struct Span {
-    int64_t dst, fb0, fb1, slot;  // destination byte of block fb0; blocks [fb0, fb1)
+    int64_t dst, fb0, fb1;  // destination byte of block fb0; blocks [fb0, fb1)
+    int64_t slot;           // first of its (fb1 - fb0) * parts partial sums
+    int parts;
   };
   std::vector<std::vector<Span>> spans(units.size());
   std::vector<std::vector<char>> host_check(units.size());
-  int64_t n_dev = 0;  // device-checked blocks per array
+  int64_t n_dev = 0;  // partial sums of the device-checked blocks, per array
   try {
     for (size_t ui = 0; ui < units.size(); ++ui) {
       const Unit& u = units[ui];
@@ -882,8 +892,9 @@ extern "C" zs_status zs_checkpoint_load(const zs_plan* plan, int32_t rank,
         if (fb1 <= fb0) continue;
         const int64_t dst = c.dst + (fb0 * B - src0);
         if (dst % 16 != 0) continue;
-        spans[ui].push_back({dst, fb0, fb1, n_dev});
-        n_dev += fb1 - fb0;
+        const int parts = zs::block_hash_parts(fb1 - fb0, B);
+        spans[ui].push_back({dst, fb0, fb1, n_dev, parts});
+        n_dev += (fb1 - fb0) * parts;
         for (int64_t b = fb0; b < fb1; ++b) host_check[ui][(size_t)(b - u.blk_lo)] = 0;
       }
     }
@@ -972,7 +983,8 @@ extern "C" zs_status zs_checkpoint_load(const zs_plan* plan, int32_t rank,
       for (const Span& sp : spans[ui]) {
         if (e != cudaSuccess) break;
         e = zs::launch_block_hash(out + sp.dst, std::min(sp.fb1 * B, ob) - sp.fb0 * B, sp.fb0, B,
-                                  (uint32_t)a, dev_sums_d + a * n_dev + sp.slot, stream);
+                                  (uint32_t)a, sp.parts, dev_sums_d + a * n_dev + sp.slot,
+                                  stream);
       }
       if (e == cudaSuccess) e = cudaEventRecord(stg.ev[s], stream);
       if (e != cudaSuccess) {
@@ -991,12 +1003,15 @@ extern "C" zs_status zs_checkpoint_load(const zs_plan* plan, int32_t rank,
     for (size_t ui = 0; ui < units.size(); ++ui)
       for (const Span& sp : spans[ui])
         for (int a = 0; a < kArrays; ++a)
-          for (int64_t b = sp.fb0; b < sp.fb1; ++b)
-            if (dev_sums[a * n_dev + sp.slot + (b - sp.fb0)] !=
-                tables[(size_t)units[ui].k][(size_t)(a * onb + b)])
+          for (int64_t b = sp.fb0; b < sp.fb1; ++b) {
+            uint64_t sum = 0;
+            const uint64_t* part = dev_sums + a * n_dev + sp.slot + (b - sp.fb0) * sp.parts;
+            for (int p = 0; p < sp.parts; ++p) sum += part[p];
+            if (sum != tables[(size_t)units[ui].k][(size_t)(a * onb + b)])
               return zs::fail(ZS_ERR_CORRUPT, "%s: %s: %s block %lld checksum mismatch (the "
                               "state arrays now hold partial data)", fn, paths[units[ui].k],
                               kArrayName[a], (long long)b);
+          }
   }
   if (step) *step = h0.step;
   return ZS_OK;

@@ -113,11 +113,14 @@ constexpr int kMaxSegs = 256;
 cudaError_t launch_segment_copy(const RowSegment* segs, int n, cudaStream_t stream);
 
 // Block checksums of checkpoint data (ckpt.cu, definition in block_hash.h):
-// out[j] = hash of bytes [j*block_bytes, min((j+1)*block_bytes, bytes)) of
-// `data` (16-byte aligned) as block first_block + j of array `array_id`.
+// the checksum of bytes [j*block_bytes, min((j+1)*block_bytes, bytes)) of
+// `data` (16-byte aligned) as block first_block + j of array `array_id` is
+// the sum (mod 2^64) of out[j*parts + p], p < parts. block_hash_parts gives
+// the parts (a power of two) that spread `blocks` blocks over every SM.
 cudaError_t launch_block_hash(const void* data, int64_t bytes, int64_t first_block,
-                              int64_t block_bytes, uint32_t array_id, uint64_t* out,
+                              int64_t block_bytes, uint32_t array_id, int parts, uint64_t* out,
                               cudaStream_t stream);
+int block_hash_parts(int64_t blocks, int64_t block_bytes);
 
 // Argument checks of the C-ABI layer, for the other host translation units:
 // device-resident on the current device and (where the driver can tell)

@@ -43,14 +43,16 @@ def _random_list(rng):
     return dims, numels, ties
 
 
-@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("seed", range(12))
 def test_device_restore_other_world_and_layout(orc, tmp_path, seed):
     rng = np.random.default_rng(4100 + seed)
     dims, numels, ties = _random_list(rng)
     ka, kb = ("flat", "rows")[seed % 2], ("flat", "rows")[(seed // 2) % 2]
     N, M = int(rng.choice([1, 2, 4, 8])), int(rng.choice([1, 2, 3, 5, 8]))
-    pa, la = _pair(orc, dims, numels, ties, ka, N, int(rng.choice([16, 128])))
-    pb, lb = _pair(orc, dims, numels, ties, kb, M, int(rng.choice([16, 128])))
+    # align 1 gives shards whose byte length is not a multiple of 16 (the
+    # checksum's zero-padded last word) and unaligned copies (checked on the host)
+    pa, la = _pair(orc, dims, numels, ties, ka, N, int(rng.choice([1, 16, 128])))
+    pb, lb = _pair(orc, dims, numels, ties, kb, M, int(rng.choice([1, 16, 128])))
     host = []
     for r in range(N):
         raw = [rng.integers(0, 2 ** 32, size=pa.S, dtype=np.uint32).view(np.float32)
