@@ -104,6 +104,25 @@ def committed_traffic(workload_key):
     return None
 
 
+def host_cpu():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -557,6 +576,24 @@ def run_ours(args, w):
                                         "timed just before; the host link is shared"}}
         del h_grads, h_out
 
+    # A practical ceiling beside the measured peak: a device-to-device copy of
+    # 4 GiB (8.6 GB of traffic), timed with events, median of 5.
+    copy_gbs = None
+    if not args.no_copy_ceiling:
+        src = torch.empty(1 << 32, dtype=torch.uint8, device=dev)
+        dst = torch.empty_like(src)
+        src.fill_(1)
+        cts = []
+        for i in range(7):
+            a, b = Ev(), Ev()
+            a.record(stream)
+            dst.copy_(src)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                cts.append(a.elapsed_time(b) / 1e3)
+        copy_gbs = 2 * (1 << 32) / statistics.median(cts) / 1e9
+        del src, dst
     if grank == 0:
         peak, peak_kind = measured_peak()
         step_bpe = pipeline[-1][2]
@@ -579,7 +616,12 @@ def run_ours(args, w):
                                                       args.cpu_steps)
             cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                    "sample": f"first {n:,} elements of rank {r}'s shard x {args.cpu_steps} "
-                             f"steps ({secs:.1f} s, 1 pinned thread)"}
+                             f"steps ({secs:.1f} s, 1 pinned thread)",
+                   "ns_per_elem": 1e9 / rate, "algorithmic_gbs": rate * bpe / 1e9,
+                   "host": host_cpu(), "nproc": os.cpu_count()}
+        if copy_gbs is not None:
+            roofline["copy_ceiling_gbs"] = copy_gbs
+            roofline["frac_of_copy_ceiling"] = achieved / copy_gbs
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": gworld,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps,
@@ -610,6 +652,105 @@ def run_ours(args, w):
     if gworld > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_sweep(args):
+    """--pipeline sweep: the shard step over a grid of shard sizes S x emulated
+    ranks N x incoming-gradient dtype x parameter dtype (one tensor of N*S
+    elements, rank 0's step), 20 timed steps per point with state carried
+    forward, per-step CUDA events; points whose buffers do not fit in free
+    device memory are reported as skipped, points whose working set fits in
+    L2 are marked cache-resident (not roofline points)."""
+    import torch
+
+    import fsdp_sharded_mixed_gb300 as zs
+    import synth
+    from synth.workloads import (SWEEP_GRAD_BYTES, SWEEP_PARAM_BYTES, SWEEP_SHARD_SIZES,
+                                 SWEEP_WORLDS)
+
+    grank, gworld, local = dist_env()
+    if grank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sptr = torch.cuda.current_stream().cuda_stream
+    peak, peak_kind = measured_peak()
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    pdt_of = {2: zs.ZS_BF16, 3: zs.ZS_FP24, 4: zs.ZS_FP32}
+    warm, reps = max(3, min(args.warmup, 5)), 20
+    sizes = [S for S in SWEEP_SHARD_SIZES if S <= (1 << args.sweep_max_log2)]
+    points, launches = [], 0
+    clocks_s = ClockSampler()
+    clocks_s.start()
+    for S in sizes:
+        torch.cuda.empty_cache()
+        free = torch.cuda.mem_get_info()[0]
+        for N in SWEEP_WORLDS:
+            for gb in SWEEP_GRAD_BYTES:
+                for pb in SWEEP_PARAM_BYTES:
+                    need = N * S * gb + 12 * S + N * S * pb
+                    pt = {"S": S, "N": N, "grad": "bf16" if gb == 2 else "fp32",
+                          "param_bytes": pb, "bytes_per_elem": gb * N + 24 + pb,
+                          "footprint_gb": need / 1e9}
+                    if need > 0.85 * free:
+                        pt["skipped"] = f"needs {need / 1e9:.1f} GB, {free / 1e9:.1f} GB free"
+                        points.append(pt)
+                        continue
+                    plan = zs.zs_flatten_plan([N * S], world=N, align_elems=128)
+                    grads = [torch.empty(S * gb, dtype=torch.uint8, device=dev) for _ in range(N)]
+                    for j, g in enumerate(grads):
+                        synth.fill_device(g.data_ptr(), S, seed=1, rank=j, step=1, sigma=1e-3,
+                                          bf16=gb == 2, cuda_stream=sptr)
+                    master = torch.empty(S, dtype=torch.float32, device=dev)
+                    synth.fill_device(master.data_ptr(), S, seed=1, stream=synth.STREAM_MASTER,
+                                      sigma=0.02, bf16=False, cuda_stream=sptr)
+                    m = torch.zeros(S, dtype=torch.float32, device=dev)
+                    v = torch.zeros(S, dtype=torch.float32, device=dev)
+                    full = torch.zeros(N * S * pb, dtype=torch.uint8, device=dev)
+                    gdt = zs.ZS_BF16 if gb == 2 else zs.ZS_FP32
+                    ev = [(torch.cuda.Event(enable_timing=True),
+                           torch.cuda.Event(enable_timing=True)) for _ in range(warm + reps)]
+                    torch.cuda.synchronize()
+                    for t, (a, b) in enumerate(ev, start=1):
+                        a.record()
+                        zs.zs_shard_step(plan, 0, 0, S, grads, gdt, master, m, v, full,
+                                         pdt_of[pb], hp, t, stream=sptr)
+                        b.record()
+                    torch.cuda.synchronize()
+                    launches += reps
+                    ts = sorted(a.elapsed_time(b) for a, b in ev[warm:])
+                    med = statistics.median(ts)
+                    gbs = pt["bytes_per_elem"] * S / med / 1e6
+                    pt.update({"ms_median": med, "ms_p10": ts[len(ts) // 10],
+                               "ms_p90": ts[(9 * len(ts)) // 10], "gbs": gbs,
+                               "frac": gbs / peak})
+                    if need < 129e6:
+                        pt["cache_resident"] = True
+                    points.append(pt)
+                    del grads, master, m, v, full
+                    plan.free()
+    clocks = clocks_s.stop()
+    roof = [p for p in points if "gbs" in p and not p.get("cache_resident")]
+    value = statistics.median(p["gbs"] for p in roof) if roof else None
+    line = {
+        "metric": "C5 sweep: shard-step achieved HBM GB/s per (S, N, grad dtype, param dtype), "
+                  "median over the roofline points, 1 GPU",
+        "value": value, "unit": "GB/s", "n_gpus": 1, "steps": reps, "warmup": warm,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "sweep: one tensor of N*S elements, rank 0's step",
+                   "pipeline": "sweep", "shard_sizes": sizes, "worlds": SWEEP_WORLDS,
+                   "grad_bytes": SWEEP_GRAD_BYTES, "param_bytes": SWEEP_PARAM_BYTES,
+                   "l2": "points under 129 MB of buffers are cache-resident, not roofline points"},
+        "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s",
+                     "frac": None if value is None else value / peak, "peak_source": peak_kind,
+                     "traffic": None,
+                     "min_frac": min((p["frac"] for p in roof), default=None),
+                     "max_frac": max((p["frac"] for p in roof), default=None)},
+        "points": points, "gpu_launches": launches, "clocks": clocks, "e2e": None,
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
 
 
 def run_checkpoint(args, w):
@@ -780,17 +921,21 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--graph", action="store_true",
                     help="time one replay of a CUDA graph holding the K launches")
-    ap.add_argument("--pipeline", choices=["step", "clip", "accum", "unshard", "checkpoint"],
+    ap.add_argument("--pipeline",
+                    choices=["step", "clip", "accum", "unshard", "checkpoint", "sweep"],
                     default="step",
                     help="step: the fused shard step; clip: global-norm pass + clip "
                          "coefficient + clipped step; accum: G-1 accumulations + the "
                          "accumulated step; unshard: FSDP2 copy-out of every wrap unit's "
                          "gathered parameters; checkpoint: save / restore / resharding "
-                         "restore of one rank's optimizer state")
+                         "restore of one rank's optimizer state; sweep: the step over "
+                         "shard sizes x N x gradient and parameter dtypes")
     ap.add_argument("--units", type=int, default=0,
                     help="--pipeline unshard: only the first K wrap units (0 = all)")
     ap.add_argument("--micro-steps", type=int, default=4,
                     help="G, micro-batches per optimizer step for --pipeline accum")
+    ap.add_argument("--sweep-max-log2", type=int, default=30,
+                    help="--pipeline sweep: largest shard size 2^k")
     ap.add_argument("--ckpt-dir", default=None,
                     help="directory for --pipeline checkpoint files (default: a temp dir)")
     ap.add_argument("--ckpt-reps", type=int, default=3)
@@ -800,6 +945,8 @@ def main(argv=None):
     ap.add_argument("--e2e-chunks", type=int, default=32)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-copy-ceiling", action="store_true",
+                    help="skip the device-to-device copy measured beside the roofline")
     ap.add_argument("--cpu-sample-elems", type=int, default=32 * 1024 * 1024)
     ap.add_argument("--cpu-steps", type=int, default=8)
     args = ap.parse_args(argv)
@@ -811,6 +958,8 @@ def main(argv=None):
         run_reference(args, w)
     elif args.pipeline == "checkpoint":
         run_checkpoint(args, w)
+    elif args.pipeline == "sweep":
+        run_sweep(args)
     else:
         run_ours(args, w)
 
