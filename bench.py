@@ -628,7 +628,8 @@ def run_ours(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": dict(workload_config(w, plan),
                                                 parallelism=f"replicas{gworld}",
-                                                emulated_rank_gpu0=r, pipeline=args.pipeline),
+                                                emulated_rank_gpu0=r, pipeline=args.pipeline,
+                                                step_path=args.step_path),
             "hbm_gbs": pipe_bpe * value / gworld / 1e9,
             "step_ms": {"median": statistics.median(per_step),
                         "p10": per_step[len(per_step) // 10],
@@ -679,6 +680,10 @@ def run_sweep(args):
     pdt_of = {2: zs.ZS_BF16, 3: zs.ZS_FP24, 4: zs.ZS_FP32}
     warm, reps = max(3, min(args.warmup, 5)), 20
     sizes = [S for S in SWEEP_SHARD_SIZES if S <= (1 << args.sweep_max_log2)]
+    only = None
+    if args.sweep_only:
+        # "log2S:N:grad_bytes:param_bytes,..." selects points of the grid
+        only = {tuple(int(x) for x in q.split(":")) for q in args.sweep_only.split(",")}
     points, launches = [], 0
     clocks_s = ClockSampler()
     clocks_s.start()
@@ -688,6 +693,8 @@ def run_sweep(args):
         for N in SWEEP_WORLDS:
             for gb in SWEEP_GRAD_BYTES:
                 for pb in SWEEP_PARAM_BYTES:
+                    if only is not None and (S.bit_length() - 1, N, gb, pb) not in only:
+                        continue
                     need = N * S * gb + 12 * S + N * S * pb
                     pt = {"S": S, "N": N, "grad": "bf16" if gb == 2 else "fp32",
                           "param_bytes": pb, "bytes_per_elem": gb * N + 24 + pb,
@@ -739,7 +746,7 @@ def run_sweep(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": "sweep: one tensor of N*S elements, rank 0's step",
-                   "pipeline": "sweep", "shard_sizes": sizes, "worlds": SWEEP_WORLDS,
+                   "pipeline": "sweep", "step_path": args.step_path, "shard_sizes": sizes, "worlds": SWEEP_WORLDS,
                    "grad_bytes": SWEEP_GRAD_BYTES, "param_bytes": SWEEP_PARAM_BYTES,
                    "l2": "points under 129 MB of buffers are cache-resident, not roofline points"},
         "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s",
@@ -934,8 +941,13 @@ def main(argv=None):
                     help="--pipeline unshard: only the first K wrap units (0 = all)")
     ap.add_argument("--micro-steps", type=int, default=4,
                     help="G, micro-batches per optimizer step for --pipeline accum")
+    ap.add_argument("--step-path", choices=["auto", "direct", "staged"], default="auto",
+                    help="the step's kernel: chosen per call (auto), the register-streaming "
+                         "kernel (direct) or the bulk-async staged kernel where it applies")
     ap.add_argument("--sweep-max-log2", type=int, default=30,
                     help="--pipeline sweep: largest shard size 2^k")
+    ap.add_argument("--sweep-only", default=None,
+                    help="--pipeline sweep: only these points, 'log2S:N:gbytes:pbytes,...'")
     ap.add_argument("--ckpt-dir", default=None,
                     help="directory for --pipeline checkpoint files (default: a temp dir)")
     ap.add_argument("--ckpt-reps", type=int, default=3)
@@ -954,6 +966,9 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     from synth.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.impl != "reference" and args.step_path != "auto":
+        import fsdp_sharded_mixed_gb300 as zs
+        zs.zs_set_step_path({"direct": 1, "staged": 2}[args.step_path])
     if args.impl == "reference":
         run_reference(args, w)
     elif args.pipeline == "checkpoint":

@@ -130,6 +130,7 @@ EXPORTS = {
     "zs_last_error": ([], ctypes.c_char_p),
     "zs_check_device_error": ([_P], ctypes.c_int),
     "zs_set_validation": ([_I32], _I32),
+    "zs_set_step_path": ([_I32], _I32),
     "zs_version": ([], ctypes.c_char_p),
 }
 
@@ -402,6 +403,18 @@ def zs_check_device_error(stream=None):
 
 def zs_set_validation(level):
     return lib().zs_set_validation(level)
+
+
+STEP_PATH_AUTO, STEP_PATH_DIRECT, STEP_PATH_STAGED = 0, 1, 2
+
+
+def zs_set_step_path(path):
+    """0 = kernel chosen per call, 1 = register-streaming, 2 = staged (bulk
+    async copies into shared memory) where it applies; returns the old path."""
+    old = lib().zs_set_step_path(path)
+    if old < 0:
+        raise ValueError(f"unknown step path {path}")
+    return old
 
 
 def zs_version():

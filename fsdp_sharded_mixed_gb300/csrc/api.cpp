@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -678,6 +679,19 @@ extern "C" zs_status zs_check_device_error(void* cuda_stream) {
   if (word & 2u) return zs::fail(ZS_ERR_TIMEOUT, "zs_check_device_error: a device wait timed out");
   if (word & 1u) return zs::fail(ZS_ERR_RANGE, "zs_check_device_error: a bounds check failed");
   return ZS_OK;
+}
+
+namespace {
+std::atomic<int32_t> g_step_path{0};
+}  // namespace
+
+namespace zs {
+int step_path() { return g_step_path.load(std::memory_order_relaxed); }
+}  // namespace zs
+
+extern "C" int32_t zs_set_step_path(int32_t path) {
+  if (path < 0 || path > 2) return -1;
+  return g_step_path.exchange(path);
 }
 
 extern "C" int32_t zs_set_validation(int32_t level) {

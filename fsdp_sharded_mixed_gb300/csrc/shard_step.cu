@@ -35,11 +35,25 @@
 
 namespace zs {
 
-// Set by bounds-checked builds; read and cleared by zs_check_device_error.
+// Set by bounds-checked builds (bit 0) and by bounded waits that gave up
+// (bit 1); read and cleared by zs_check_device_error.
 __device__ unsigned int g_error_word;
 
 cudaError_t launch_shard_step(const ShardStepLaunch& a, cudaStream_t stream) {
   return launch_step_kernel<false>(a, stream);
+}
+
+unsigned int* device_error_word() {
+  static unsigned int* by_dev[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  unsigned int*& w = by_dev[dev & 63];
+  if (!w) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_error_word) != cudaSuccess) return nullptr;
+    w = static_cast<unsigned int*>(addr);
+  }
+  return w;
 }
 
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* word) {

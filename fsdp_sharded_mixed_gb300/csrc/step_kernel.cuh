@@ -331,6 +331,265 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+// ---- the staged path ------------------------------------------------------------
+// The same step with the N slices and the state tile staged in shared memory
+// by bulk asynchronous copies (cp.async.bulk, completion counted on an
+// mbarrier): one producer thread keeps the next tiles' copies in flight while
+// 16 consumer warps compute the current one from shared memory, so loads and
+// arithmetic overlap instead of alternating per thread. A tile is 2048
+// elements, each consumer thread 4 of them; stages are reused once every
+// consumer warp has released them. On GB300 this wins where the register-
+// streaming kernel above cannot keep enough bytes in flight: short ranges,
+// large stages (many slices) and N <= 2 with 3-byte parameters; elsewhere the
+// kernel above is faster (the choice is in try_staged). Every wait is bounded: a wait that
+// gives up sets bit 2 of the device error word and the thread stops; the
+// producer waits, bounded, for its own copies before the block exits.
+constexpr int kStagedWarps = 16;                     // consumer warps
+constexpr int kStagedThreads = (kStagedWarps + 1) * 32;
+constexpr int kStagedE = 4;                          // elements per consumer thread per tile
+constexpr int kTile = kStagedWarps * 32 * kStagedE;  // 2048
+constexpr int kStagedMaxN = 16;
+constexpr int kStagedMaxStages = 4;
+constexpr uint32_t kWaitPolls = 1u << 21;
+
+struct StagedArgs {
+  StepArgs<kStagedMaxN> a;
+  int64_t t0, t1;      // whole tiles [t0, t1): elements [t0*kTile, t1*kTile)
+  int64_t rag_lo[2], rag_hi[2];  // the ragged head and tail, element by element
+  int stages;
+  uint32_t stage_bytes;
+  unsigned int* err;   // the device error word
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+// Bounded wait for the phase of parity `parity` to complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, unsigned int* err) {
+  for (uint32_t it = 0; it < kWaitPolls; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  atomicOr(err, 2u);
+  return false;
+}
+__device__ __forceinline__ void bulk_to_smem(void* dst, const void* src, uint32_t bytes,
+                                             uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void st_u32(void* p, uint32_t w) {
+  asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(w) : "memory");
+}
+
+// Bytes of one tile of one slice.
+template <bool BF16G>
+__host__ __device__ constexpr uint32_t tile_grad_bytes() {
+  return kTile * (BF16G ? 2 : 4);
+}
+
+template <bool BF16G, int PD, bool ACC>
+__global__ void __launch_bounds__(kStagedThreads, 2)
+    staged_step_kernel(const __grid_constant__ StagedArgs sa) {
+  const StepArgs<kStagedMaxN>& a = sa.a;
+  if (a.skip && *a.skip) return;  // the ranks' shared non-finite decision
+  const bool clip = a.coef != nullptr;
+  const float coef = clip ? *a.coef : 1.0f;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int NS = sa.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * sa.stage_bytes);
+  uint64_t* empty = full + NS;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = a.world;
+  constexpr uint32_t gtile = tile_grad_bytes<BF16G>();
+  constexpr uint32_t stile = kTile * 4;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kStagedWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == kStagedWarps) {
+    // The producer: one thread arms each stage with the tile's byte count and
+    // issues the N + 3 (+1) bulk copies into it.
+    if (lane != 0) return;
+    int64_t i = 0;
+    for (int64_t t = sa.t0 + blockIdx.x; t < sa.t1; t += gridDim.x, ++i) {
+      const int s = (int)(i % NS);
+      const uint32_t use = (uint32_t)(i / NS);
+      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, sa.err)) break;
+      unsigned char* st = smem + (size_t)s * sa.stage_bytes;
+      mbar_expect_tx(&full[s], sa.stage_bytes);
+      for (int j = 0; j < n; ++j)
+        bulk_to_smem(st + j * gtile, static_cast<const unsigned char*>(a.grads[j]) + t * gtile,
+                     gtile, &full[s]);
+      unsigned char* sp = st + n * gtile;
+      bulk_to_smem(sp, a.master + t * kTile, stile, &full[s]);
+      bulk_to_smem(sp + stile, a.m + t * kTile, stile, &full[s]);
+      bulk_to_smem(sp + 2 * stile, a.v + t * kTile, stile, &full[s]);
+      if constexpr (ACC) bulk_to_smem(sp + 3 * stile, a.accum + t * kTile, stile, &full[s]);
+    }
+    // Every copy issued has landed before the block may exit.
+    for (int64_t k = i > NS ? i - NS : 0; k < i; ++k)
+      mbar_wait(&full[k % NS], (uint32_t)(k / NS) & 1u, sa.err);
+    return;
+  }
+
+  // The ragged head and tail, one element per consumer thread of the grid.
+  const int c = threadIdx.x;
+  {
+    const int64_t nh = sa.rag_hi[0] - sa.rag_lo[0], nt = sa.rag_hi[1] - sa.rag_lo[1];
+    const int64_t consumers = (int64_t)gridDim.x * (kStagedWarps * 32);
+    for (int64_t q = (int64_t)blockIdx.x * (kStagedWarps * 32) + c; q < nh + nt; q += consumers)
+      process_element<BF16G, PD, kStagedMaxN, ACC>(
+          a, q < nh ? sa.rag_lo[0] + q : sa.rag_lo[1] + (q - nh), clip, coef);
+  }
+  int64_t i = 0;
+  for (int64_t t = sa.t0 + blockIdx.x; t < sa.t1; t += gridDim.x, ++i) {
+    const int s = (int)(i % NS);
+    const uint32_t use = (uint32_t)(i / NS);
+    if (!mbar_wait(&full[s], use & 1u, sa.err)) return;
+    const unsigned char* st = smem + (size_t)s * sa.stage_bytes;
+    float acc[kStagedE];
+#pragma unroll
+    for (int k = 0; k < kStagedE; ++k) acc[k] = 0.0f;
+#pragma unroll 1
+    for (int j = 0; j < n; ++j) {
+      const unsigned char* gp = st + j * gtile;
+      if constexpr (BF16G) {
+        const uint2 w = *reinterpret_cast<const uint2*>(gp + c * 8);
+        acc[0] = __fadd_rn(acc[0], bf16_lo(w.x));
+        acc[1] = __fadd_rn(acc[1], bf16_hi(w.x));
+        acc[2] = __fadd_rn(acc[2], bf16_lo(w.y));
+        acc[3] = __fadd_rn(acc[3], bf16_hi(w.y));
+      } else {
+        const float4 x = *reinterpret_cast<const float4*>(gp + c * 16);
+        acc[0] = __fadd_rn(acc[0], x.x);
+        acc[1] = __fadd_rn(acc[1], x.y);
+        acc[2] = __fadd_rn(acc[2], x.z);
+        acc[3] = __fadd_rn(acc[3], x.w);
+      }
+    }
+    const float* sp = reinterpret_cast<const float*>(st + n * gtile) + c * kStagedE;
+    const float4 p4 = *reinterpret_cast<const float4*>(sp);
+    const float4 m4 = *reinterpret_cast<const float4*>(sp + kTile);
+    const float4 v4 = *reinterpret_cast<const float4*>(sp + 2 * kTile);
+    float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (ACC) a4 = *reinterpret_cast<const float4*>(sp + 3 * kTile);
+    // The stage's next fill is written by the async proxy: order this
+    // thread's reads of it before the warp releases the stage.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    float p[4] = {p4.x, p4.y, p4.z, p4.w}, m[4] = {m4.x, m4.y, m4.z, m4.w},
+          v[4] = {v4.x, v4.y, v4.z, v4.w};
+    const float prev[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      adamw(a.s, step_grad<ACC>(acc[k], prev[k], a.s.invN, a.invG, clip, coef), p[k], m[k],
+            v[k]);
+    const int64_t e0 = t * kTile + (int64_t)c * kStagedE;
+    st16_f(a.master + e0, p);
+    st16_f(a.m + e0, m);
+    st16_f(a.v + e0, v);
+    if constexpr (PD == kParamBf16) {
+      const uint32_t w[2] = {pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3])};
+      st8_u(a.slot + 2 * e0, w);
+    } else if constexpr (PD == kParamFp32) {
+      st16_f(reinterpret_cast<float*>(a.slot) + e0, p);
+    } else {
+      const uint32_t q0 = to_fp24(p[0]), q1 = to_fp24(p[1]), q2 = to_fp24(p[2]),
+                     q3 = to_fp24(p[3]);
+      unsigned char* d = a.slot + 3 * e0;  // 12 bytes = three little-endian words
+      st_u32(d, q0 | (q1 << 24));
+      st_u32(d + 4, (q1 >> 8) | (q2 << 16));
+      st_u32(d + 8, (q2 >> 16) | (q3 << 8));
+    }
+  }
+}
+
+// Shared memory of the staged path: the stages a block holds and the blocks
+// an SM holds, from the tile's byte count; 0 stages = the path does not fit.
+inline void staged_shape(uint32_t stage_bytes, int smem_per_sm, int smem_per_block, int* stages,
+                         int* blocks_per_sm) {
+  const int reserve = 1024 + 16 * kStagedMaxStages;  // per-block system use and barriers
+  *blocks_per_sm = 2 * (2 * (int64_t)stage_bytes + reserve) <= smem_per_sm ? 2 : 1;
+  int64_t budget = smem_per_sm / *blocks_per_sm - reserve;
+  if (budget > smem_per_block - 16 * kStagedMaxStages) budget = smem_per_block - 16 * kStagedMaxStages;
+  int64_t ns = budget / stage_bytes;
+  if (ns > kStagedMaxStages) ns = kStagedMaxStages;
+  *stages = ns >= 2 ? (int)ns : 0;
+}
+
+template <bool BF16G, int PD, bool ACC>
+cudaError_t launch_staged(const ShardStepLaunch& in, uint32_t stage_bytes, int stages,
+                          int blocks_per_sm, int sms, cudaStream_t stream) {
+  auto kernel = staged_step_kernel<BF16G, PD, ACC>;
+  const size_t smem = (size_t)stages * stage_bytes + 16 * (size_t)stages;
+  static size_t smem_set_by_dev[64];  // this instantiation's opt-in so far, per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (smem > smem_set_by_dev[dev & 63]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    smem_set_by_dev[dev & 63] = smem;
+  }
+  StagedArgs sa;
+  for (int j = 0; j < in.world; ++j) sa.a.grads[j] = in.grads[j];
+  for (int j = in.world; j < kStagedMaxN; ++j) sa.a.grads[j] = nullptr;
+  sa.a.master = in.master;
+  sa.a.m = in.m;
+  sa.a.v = in.v;
+  sa.a.slot = in.slot;
+  sa.a.lo = in.lo;
+  sa.a.hi = in.hi;
+  sa.a.world = in.world;
+  sa.a.coef = in.coef;
+  sa.a.skip = in.skip;
+  sa.a.accum = in.accum;
+  sa.a.invG = in.invG;
+  sa.a.s = in.s;
+  sa.t0 = (in.lo + kTile - 1) / kTile;
+  sa.t1 = in.hi / kTile;
+  sa.rag_lo[0] = in.lo;
+  sa.rag_hi[0] = sa.t0 * kTile;
+  sa.rag_lo[1] = sa.t1 * kTile;
+  sa.rag_hi[1] = in.hi;
+  sa.stages = stages;
+  sa.stage_bytes = stage_bytes;
+  sa.err = device_error_word();
+  if (!sa.err) return cudaErrorInvalidSymbol;
+  int64_t blocks = sa.t1 - sa.t0;
+  if (blocks > (int64_t)sms * blocks_per_sm) blocks = (int64_t)sms * blocks_per_sm;
+  kernel<<<(unsigned)blocks, kStagedThreads, smem, stream>>>(sa);
+  return cudaGetLastError();
+}
+
 template <int GW, bool BF16G, int PD, int MAXN, bool ACC>
 cudaError_t launch_one(const ShardStepLaunch& in, cudaStream_t stream) {
   // Resident blocks on the whole GPU for this instantiation, per device; the
@@ -372,8 +631,59 @@ cudaError_t launch_one(const ShardStepLaunch& in, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// The staged path where it is eligible and (path 0) measured faster: N <= 16,
+// 16-byte aligned state and slices, a slot aligned for its stores, at least 8
+// whole tiles, two stages that fit in shared memory.
+template <bool BF16G, int PD, bool ACC>
+bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* result) {
+  const int path = step_path();
+  if (path == 1 || a.world > kStagedMaxN) return false;
+  const int64_t tiles = a.hi / kTile - (a.lo + kTile - 1) / kTile;
+  if (tiles < 8) return false;
+  uintptr_t ptrs = (uintptr_t)a.master | (uintptr_t)a.m | (uintptr_t)a.v | (uintptr_t)a.accum;
+  for (int j = 0; j < a.world; ++j) ptrs |= (uintptr_t)a.grads[j];
+  const uintptr_t slot_align = PD == kParamBf16 ? 8 : PD == kParamFp32 ? 16 : 4;
+  if (ptrs % 16 != 0 || (uintptr_t)a.slot % slot_align != 0) return false;
+  static int shape_by_dev[64][2];  // smem per SM, per block (opt-in), per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  int* sh = shape_by_dev[dev & 63];
+  static int sms_by_dev[64];
+  if (sh[0] == 0) {
+    int per_sm = 0, per_block = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&per_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    sh[1] = per_block;
+    sms_by_dev[dev & 63] = sms;
+    sh[0] = per_sm;
+  }
+  const uint32_t stage_bytes =
+      (uint32_t)a.world * tile_grad_bytes<BF16G>() + (ACC ? 4u : 3u) * kTile * 4u;
+  // The per-call choice, from the GB300 sweep (S x N x dtypes, both kernels):
+  // the staged kernel is faster for ranges under 2^24 elements, for stages of
+  // 64 KiB or more (one block per SM: N >= 12 bf16 slices, N >= 6 fp32), and
+  // at N <= 2 with 3-byte parameters; the register-streaming kernel elsewhere.
+  if (path == 0 && !(a.hi - a.lo < (int64_t(1) << 24) || stage_bytes >= 64u * 1024u ||
+                     (a.world <= 2 && PD == kParamFp24)))
+    return false;
+  int stages = 0, per_sm_blocks = 0;
+  staged_shape(stage_bytes, sh[0], sh[1], &stages, &per_sm_blocks);
+  if (stages == 0) return false;
+  *result = launch_staged<BF16G, PD, ACC>(a, stage_bytes, stages, per_sm_blocks,
+                                          sms_by_dev[dev & 63], stream);
+  return true;
+}
+
 template <bool BF16G, int PD, bool ACC>
 cudaError_t dispatch(const ShardStepLaunch& a, cudaStream_t stream) {
+  cudaError_t staged_result = cudaSuccess;
+  if (try_staged<BF16G, PD, ACC>(a, stream, &staged_result)) return staged_result;
   if (a.vec_width == 16) {
     if (a.world <= 16) return launch_one<16, BF16G, PD, 16, ACC>(a, stream);
     return launch_one<16, BF16G, PD, ZS_MAX_WORLD, ACC>(a, stream);

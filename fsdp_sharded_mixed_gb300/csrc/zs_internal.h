@@ -127,6 +127,12 @@ int block_hash_parts(int64_t blocks, int64_t block_bytes);
 // [p, p + bytes) inside one allocation.
 zs_status check_device_array(const void* p, int64_t bytes, const char* fn, const char* name);
 
+// Which kernel runs the step: 0 = chosen per call, 1 = the register-streaming
+// kernel, 2 = the staged kernel wherever it is eligible (zs_set_step_path).
+int step_path();
+// This device's error word (device address), for kernels that report into it.
+unsigned int* device_error_word();
+
 // Device error word (set by bounds-checked builds and bounded waits).
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* word);
 

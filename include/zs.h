@@ -370,6 +370,17 @@ const char* zs_last_error(void);
  * (set by bounds-checked builds and bounded waits); ZS_ERR_TIMEOUT or
  * ZS_ERR_RANGE if it was set, ZS_ERR_CUDA if the stream reports an error. */
 zs_status zs_check_device_error(void* cuda_stream);
+/* The step's kernel. Two kernels compute the same step with the same fp32
+ * operations in the same order (results are identical): the register-
+ * streaming kernel (each thread loads its 16-element group of every slice and
+ * state array straight into registers) and the staged kernel (one thread per
+ * block streams 2048-element tiles of the slices and state into shared memory
+ * with bulk asynchronous copies while 16 warps compute; N <= 16 only). path 0
+ * (default): chosen per call by N and the range's length; 1: always the
+ * register-streaming kernel; 2: the staged kernel wherever it applies.
+ * Returns the previous path, or -1 for an unknown path (nothing changed).
+ * The pages have no counterpart: this is a choice between two GB300 kernels. */
+int32_t zs_set_step_path(int32_t path);
 /* 1 = check device pointers against the driver's allocation records on each
  * call (default), 0 = only NULL/alignment/range checks. Returns the old level. */
 int32_t zs_set_validation(int32_t level);
