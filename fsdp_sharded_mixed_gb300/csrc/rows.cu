@@ -17,7 +17,7 @@
 // chunks (a binary search over the segments' chunk prefix sums finds a chunk's
 // segment), so the load is even however unequal the segments are (a unit mixes
 // 1 KB norm rows with 11 MB MLP chunks); each chunk moves with the widest
-// access its segment's alignment allows (16 bytes for real layouts). Bound:
+// access its segment's alignment allows (32 bytes for real layouts). Bound:
 // HBM, 2 bytes of traffic per byte copied (read + write) and 1 per zero byte.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -46,6 +46,39 @@ __device__ __forceinline__ uint4 ld_once(const void* p) {
       : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
       : "l"(p));
   return r;
+}
+
+__device__ __forceinline__ void ld32_once(const void* p, uint32_t* r) {
+  asm("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "l"(p));
+}
+__device__ __forceinline__ void st32(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// 32-byte aligned run: 32-byte loads and stores, 4 loads in flight per thread
+// (32 KB per block).
+__device__ __forceinline__ void copy_range32(const unsigned char* src, unsigned char* dst,
+                                             int64_t b0, int64_t b1) {
+  constexpr int U = 4;
+  const int n = (int)((b1 - b0) / 32);
+  for (int base = 0; base < n; base += kThreads * U) {
+    uint32_t r[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * kThreads + threadIdx.x;
+      if (i < n) ld32_once(src + b0 + 32 * (int64_t)i, r[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * kThreads + threadIdx.x;
+      if (i < n) st32(dst + b0 + 32 * (int64_t)i, r[u]);
+    }
+  }
 }
 
 // 16-byte aligned run: each thread issues 4 loads before its stores, so a
@@ -90,7 +123,12 @@ __device__ __forceinline__ void zero_range(unsigned char* dst, int64_t b0, int64
 }
 
 __device__ __forceinline__ int unit_of(uintptr_t a) {
-  return (a & 15u) == 0 ? 16 : (a & 7u) == 0 ? 8 : (a & 3u) == 0 ? 4 : (a & 1u) == 0 ? 2 : 1;
+  return (a & 31u) == 0   ? 32
+         : (a & 15u) == 0 ? 16
+         : (a & 7u) == 0  ? 8
+         : (a & 3u) == 0  ? 4
+         : (a & 1u) == 0  ? 2
+                          : 1;
 }
 
 __global__ void __launch_bounds__(kThreads) segment_copy_kernel(const __grid_constant__ SegArgs a) {
@@ -113,6 +151,7 @@ __global__ void __launch_bounds__(kThreads) segment_copy_kernel(const __grid_con
     if (b0 < c1) {
       const int64_t e = c1 == s.copy_bytes ? s.copy_bytes : kChunk;
       switch (unit_of((uintptr_t)s.src | (uintptr_t)s.dst | (uintptr_t)e)) {
+        case 32: copy_range32(s.src, s.dst, b0, c1); break;
         case 16: copy_range16(s.src, s.dst, b0, c1); break;
         case 8: copy_range<uint2>(s.src, s.dst, b0, c1); break;
         case 4: copy_range<uint32_t>(s.src, s.dst, b0, c1); break;
