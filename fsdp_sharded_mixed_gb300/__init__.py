@@ -131,6 +131,7 @@ EXPORTS = {
     "zs_check_device_error": ([_P], ctypes.c_int),
     "zs_set_validation": ([_I32], _I32),
     "zs_set_step_path": ([_I32], _I32),
+    "zs_selftest_wait_timeout": ([ctypes.c_uint32, _P], ctypes.c_int),
     "zs_version": ([], ctypes.c_char_p),
 }
 
@@ -395,6 +396,11 @@ def zs_checkpoint_info(path):
                                     ctypes.byref(S), ctypes.byref(step)))
     return dict(world=w.value, rank=r.value, layout=lay.value, n_params=n.value, P=P.value,
                 S=S.value, step=step.value)
+
+
+def zs_selftest_wait_timeout(polls, stream=None):
+    """Enqueue a bounded wait that runs out (see include/zs.h)."""
+    _check(lib().zs_selftest_wait_timeout(polls, _stream(stream)))
 
 
 def zs_check_device_error(stream=None):

@@ -689,6 +689,16 @@ namespace zs {
 int step_path() { return g_step_path.load(std::memory_order_relaxed); }
 }  // namespace zs
 
+extern "C" zs_status zs_selftest_wait_timeout(uint32_t polls, void* cuda_stream) {
+  zs::clear_error();
+  if (polls == 0 || polls > (1u << 20))
+    return zs::fail(ZS_ERR_RANGE, "zs_selftest_wait_timeout: polls %u outside 1..2^20", polls);
+  const cudaError_t e = zs::launch_wait_timeout(polls, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess)
+    return zs::fail(ZS_ERR_CUDA, "zs_selftest_wait_timeout: %s", cudaGetErrorString(e));
+  return ZS_OK;
+}
+
 extern "C" int32_t zs_set_step_path(int32_t path) {
   if (path < 0 || path > 2) return -1;
   return g_step_path.exchange(path);

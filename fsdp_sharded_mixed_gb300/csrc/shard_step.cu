@@ -43,6 +43,27 @@ cudaError_t launch_shard_step(const ShardStepLaunch& a, cudaStream_t stream) {
   return launch_step_kernel<false>(a, stream);
 }
 
+namespace {
+// A wait that is never satisfied: one mbarrier, initialised and never arrived
+// on, waited for through the step kernels' bounded wait with `polls` polls.
+__global__ void wait_timeout_kernel(unsigned int* err, uint32_t polls) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, err, polls);
+}
+}  // namespace
+
+cudaError_t launch_wait_timeout(uint32_t polls, cudaStream_t stream) {
+  unsigned int* err = device_error_word();
+  if (!err) return cudaErrorInvalidSymbol;
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(err, polls);
+  return cudaGetLastError();
+}
+
 unsigned int* device_error_word() {
   static unsigned int* by_dev[64];
   int dev = 0;

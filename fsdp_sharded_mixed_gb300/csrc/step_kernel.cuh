@@ -376,9 +376,11 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
 }
-// Bounded wait for the phase of parity `parity` to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, unsigned int* err) {
-  for (uint32_t it = 0; it < kWaitPolls; ++it) {
+// Bounded wait for the phase of parity `parity` to complete: at most `polls`
+// polls, then bit 2 of the error word is set and the caller stops.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, unsigned int* err,
+                                          uint32_t polls = kWaitPolls) {
+  for (uint32_t it = 0; it < polls; ++it) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"

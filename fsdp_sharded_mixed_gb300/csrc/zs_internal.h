@@ -132,6 +132,8 @@ zs_status check_device_array(const void* p, int64_t bytes, const char* fn, const
 int step_path();
 // This device's error word (device address), for kernels that report into it.
 unsigned int* device_error_word();
+// One block waiting, bounded by `polls`, on an mbarrier nothing arrives on.
+cudaError_t launch_wait_timeout(uint32_t polls, cudaStream_t stream);
 
 // Device error word (set by bounds-checked builds and bounded waits).
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* word);

@@ -381,6 +381,14 @@ zs_status zs_check_device_error(void* cuda_stream);
  * Returns the previous path, or -1 for an unknown path (nothing changed).
  * The pages have no counterpart: this is a choice between two GB300 kernels. */
 int32_t zs_set_step_path(int32_t path);
+/* Failure detection without a fault: enqueues one block that waits, through
+ * the same bounded mbarrier wait the staged step kernel uses, on a barrier
+ * nothing arrives on, giving up after `polls` polls (1..2^20). The wait then
+ * sets the device error word's timeout bit, so a following
+ * zs_check_device_error returns ZS_ERR_TIMEOUT; the context stays usable.
+ * The pages have no counterpart (their failure detection is watchdog
+ * timeouts on hung collectives). */
+zs_status zs_selftest_wait_timeout(uint32_t polls, void* cuda_stream);
 /* 1 = check device pointers against the driver's allocation records on each
  * call (default), 0 = only NULL/alignment/range checks. Returns the old level. */
 int32_t zs_set_validation(int32_t level);

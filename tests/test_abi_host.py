@@ -151,3 +151,17 @@ def test_null_plan_rejected():
     assert L.zs_shard_step(None, 0, 0, 1, None, 0, None, None, None, None, 0, None, 1,
                            None) == zs.ZS_ERR_INVAL
     assert L.zs_gather_assemble(None, 0, None, None, 0, None, None) == zs.ZS_ERR_INVAL
+
+
+def test_selftest_and_step_path_arguments():
+    """Argument checks of the wait self-test and the step-path switch, on the
+    host (no kernel is launched for a rejected call)."""
+    L = zs.lib()
+    assert L.zs_selftest_wait_timeout(0, None) == zs.ZS_ERR_RANGE
+    assert L.zs_selftest_wait_timeout((1 << 20) + 1, None) == zs.ZS_ERR_RANGE
+    old = zs.zs_set_step_path(zs.STEP_PATH_DIRECT)
+    assert zs.zs_set_step_path(zs.STEP_PATH_STAGED) == zs.STEP_PATH_DIRECT
+    assert zs.zs_set_step_path(old) == zs.STEP_PATH_STAGED
+    with pytest.raises(ValueError):
+        zs.zs_set_step_path(5)
+    assert L.zs_set_step_path(-1) == -1

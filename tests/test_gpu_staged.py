@@ -172,3 +172,37 @@ def test_step_path_switch():
     with pytest.raises(ValueError):
         zs.zs_set_step_path(3)
     assert zs.zs_set_step_path(old) == old
+
+
+def test_bounded_wait_runs_out_and_the_context_survives(orc):
+    """A wait that nothing satisfies gives up after its poll limit, sets the
+    timeout bit of the device error word (ZS_ERR_TIMEOUT on the host), and the
+    context stays usable: a staged step afterwards matches the oracle."""
+    zs.zs_check_device_error()   # start from a clear error word
+    zs.zs_selftest_wait_timeout(1000)
+    with pytest.raises(zs.ZsError) as e:
+        zs.zs_check_device_error()
+    assert e.value.status == zs.ZS_ERR_TIMEOUT
+    zs.zs_check_device_error()   # read and cleared
+    old = zs.zs_set_step_path(2)
+    try:
+        N, S0 = 4, 40_000
+        plan = zs.zs_flatten_plan([N * S0], world=N, align_elems=128)
+        S = plan.S
+        g = [synth.fill(S, seed=3, rank=j, step=1, bf16=True, p_limit=N * S) for j in range(N)]
+        master = synth.fill(S, seed=3, stream=synth.STREAM_MASTER, sigma=0.02, p_limit=N * S)
+        o = [master.copy(), np.zeros(S, np.float32), np.zeros(S, np.float32)]
+        d = [to_dev(x.copy()) for x in o]
+        full = torch.zeros(plan.P_pad, dtype=torch.int16, device=DEV)
+        o_full = np.zeros(plan.P_pad, np.uint16)
+        zs.zs_shard_step(plan, 0, 0, S, [to_dev(x) for x in g], zs.ZS_BF16, *d, full, zs.ZS_BF16,
+                         HP, 1)
+        orc.shard_step(world=N, rank=0, S=S, lo=0, hi=S, grads=g, master=o[0], m=o[1], v=o[2],
+                       full_flat=o_full, t=1, **oracle_hp(HP))
+        zs.zs_check_device_error()
+        for x, ref, name in zip(d, o, ("master", "m", "v")):
+            assert assert_state_close(to_host(x, np.float32), ref, name) == 0
+        assert np.array_equal(to_host(full, np.uint16), o_full)
+        plan.free()
+    finally:
+        zs.zs_set_step_path(old)
