@@ -340,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 // elements, each consumer thread 4 of them; stages are reused once every
 // consumer warp has released them. On GB300 this wins where the register-
 // streaming kernel above cannot keep enough bytes in flight: short ranges,
-// large stages (many slices) and N <= 2 with 3-byte parameters; elsewhere the
+// many slices (32 bytes or more per element) and N <= 2 with 3-byte
+// parameters; elsewhere the
 // kernel above is faster (the choice is in try_staged). Every wait is bounded: a wait that
 // gives up sets bit 2 of the device error word and the thread stops; the
 // producer waits, bounded, for its own copies before the block exits.
@@ -667,11 +668,14 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
   }
   const uint32_t stage_bytes =
       (uint32_t)a.world * tile_grad_bytes<BF16G>() + (ACC ? 4u : 3u) * kTile * 4u;
-  // The per-call choice, from the GB300 sweep (S x N x dtypes, both kernels):
-  // the staged kernel is faster for ranges under 2^24 elements, for stages of
-  // 64 KiB or more (one block per SM: N >= 12 bf16 slices, N >= 6 fp32), and
-  // at N <= 2 with 3-byte parameters; the register-streaming kernel elsewhere.
-  if (path == 0 && !(a.hi - a.lo < (int64_t(1) << 24) || stage_bytes >= 64u * 1024u ||
+  // The per-call choice, from the GB300 sweep (S x N x dtypes, both kernels)
+  // and the accumulated step: the staged kernel is faster for ranges under
+  // 2^24 elements, where the slices bring 32 bytes or more per element (N >= 16
+  // bf16, N >= 8 fp32), and at N <= 2 with 3-byte parameters; the register-
+  // streaming kernel elsewhere (including N = 8 bf16 with the accumulator:
+  // 1.026 vs 0.956 on Llama-7B).
+  const int slice_bytes = a.world * (BF16G ? 2 : 4);
+  if (path == 0 && !(a.hi - a.lo < (int64_t(1) << 24) || slice_bytes >= 32 ||
                      (a.world <= 2 && PD == kParamFp24)))
     return false;
   int stages = 0, per_sm_blocks = 0;
