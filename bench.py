@@ -80,12 +80,21 @@ def sum_over_ranks(value, device=None):
     return float(t.item())
 
 
+def code_of(text):
+    """C++ source without comments and with whitespace runs collapsed: what
+    the compiler sees (the sources' string literals hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_sha():
-    """sha256[:16] over the sources of the step kernel."""
+    """sha256[:16] over the code (comments and layout ignored) of the step
+    kernel's sources."""
     h = hashlib.sha256()
     for path in KERNEL_SOURCES:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            h.update(code_of(f.read()).encode())
     return h.hexdigest()[:16]
 
 

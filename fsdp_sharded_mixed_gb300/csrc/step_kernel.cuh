@@ -341,10 +341,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 // consumer warp has released them. On GB300 this wins where the register-
 // streaming kernel above cannot keep enough bytes in flight: short ranges,
 // many slices (32 bytes or more per element) and N <= 2 with 3-byte
-// parameters; elsewhere the
-// kernel above is faster (the choice is in try_staged). Every wait is bounded: a wait that
-// gives up sets bit 2 of the device error word and the thread stops; the
-// producer waits, bounded, for its own copies before the block exits.
+// parameters; elsewhere the kernel above is faster (the choice is in
+// try_staged). Every wait is bounded: a wait that gives up sets the device
+// error word's timeout bit (value 2) and the thread stops; the producer
+// waits, bounded, for its own copies before the block exits.
 constexpr int kStagedWarps = 16;                     // consumer warps
 constexpr int kStagedThreads = (kStagedWarps + 1) * 32;
 constexpr int kStagedE = 4;                          // elements per consumer thread per tile
@@ -378,7 +378,8 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
 }
 // Bounded wait for the phase of parity `parity` to complete: at most `polls`
-// polls, then bit 2 of the error word is set and the caller stops.
+// polls, then the error word's timeout bit (value 2) is set and the caller
+// stops.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, unsigned int* err,
                                           uint32_t polls = kWaitPolls) {
   for (uint32_t it = 0; it < polls; ++it) {
