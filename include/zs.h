@@ -44,7 +44,7 @@ typedef enum {
   ZS_ERR_ALIGN = -2,       /* a device pointer is not 16-byte aligned */
   ZS_ERR_RANGE = -3,       /* index range, rank or size out of bounds */
   ZS_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed */
-  ZS_ERR_NOMEM = -5,       /* host allocation for a plan failed */
+  ZS_ERR_NOMEM = -5,       /* a host allocation failed (a plan, checkpoint staging) */
   ZS_ERR_TIMEOUT = -6,     /* a bounded device-side wait gave up */
   ZS_ERR_UNSUPPORTED = -7, /* combination not built into this library */
   ZS_ERR_IO = -8,          /* a checkpoint file could not be opened, read or written */
@@ -130,6 +130,9 @@ zs_status zs_plan_free(zs_plan* plan);
  *   p   = p*(1 - lr*wd) - lr*u;  full_flat[rank*S + i] = round(p)
  * with b1, b2, 1-b1, 1-b2, 1-b1^t, 1-b2^t, lr, eps, 1-lr*wd and 1/N each
  * computed once in double (beta^t by binary powering) and rounded to fp32.
+ * One kernel launch: the register-streaming kernel or, for short ranges and
+ * many slices, the staged kernel (zs_set_step_path); both compute exactly
+ * these operations, so the result does not depend on which runs.
  *
  *   grad_slices[N]  device pointers; slice j is source rank j's gradient for
  *                   this rank's shard, element 0 of the shard at index 0,
