@@ -586,6 +586,47 @@ def pin_ddp_equivalence(o, w=TINY, steps=None):
         assert not gathered[P:].any() and not ddp["master"][P:].any()
 
 
+def pin_ddp_equivalence_gpt2_buckets(o, steps=1):
+    """The C2 configuration at full size: the GPT-2-small list over N = 8
+    ranks with 25M-element buckets, each rank's step run bucket by bucket (its
+    shard-local part of every bucket), gathered, equals the unsharded DDP
+    AllReduce + AdamW step bit for bit (parameters, master, m, v), and the
+    768-element tail pad stays zero."""
+    w = GPT2_SMALL
+    plan = o.plan(w.numels, w.tied_to, world=w.world, align=w.align,
+                  bucket_elems=w.bucket_elems)
+    P, P_pad, S, N = plan["P"], plan["P_pad"], plan["S"], w.world
+    assert len(plan["buckets"]) == 5 and P_pad - P == 768
+    master0 = synth.fill(P_pad, seed=w.seed, stream=synth.STREAM_MASTER, sigma=w.master_sigma,
+                         p_limit=P)
+    ddp = dict(master=master0.copy(), m=np.zeros(P_pad, np.float32),
+               v=np.zeros(P_pad, np.float32), params=np.zeros(P_pad, np.uint16))
+    sh = [[master0[r * S:(r + 1) * S].copy(), np.zeros(S, np.float32), np.zeros(S, np.float32)]
+          for r in range(N)]
+    hp = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, wd=w.weight_decay)
+    for t in range(1, steps + 1):
+        local = _local_grads(w, P_pad, P, t, N)
+        o.ddp_step(world=N, P_pad=P_pad, local_grads=local, **ddp, t=t, **hp)
+        own = []
+        for r in range(N):
+            full = np.zeros(P_pad, np.uint16)
+            slices = [local[j][r * S:(r + 1) * S].copy() for j in range(N)]
+            for flo, fhi in plan["buckets"]:
+                lo, hi = o.shard_range(flo, fhi, r, S)
+                if lo < hi:
+                    o.shard_step(world=N, rank=r, S=S, lo=lo, hi=hi, grads=slices,
+                                 master=sh[r][0], m=sh[r][1], v=sh[r][2], full_flat=full, t=t,
+                                 **hp)
+            own.append(full[r * S:(r + 1) * S].copy())
+        gathered = np.zeros(P_pad, np.uint16)
+        o.gather(world=N, S=S, elem_size=2, shards=own, full_flat=gathered)
+        assert np.array_equal(gathered, ddp["params"]), f"params differ at t={t}"
+        for k, name in enumerate(("master", "m", "v")):
+            assert np.array_equal(np.concatenate([x[k] for x in sh]).view(np.uint32),
+                                  ddp[name].view(np.uint32)), f"{name} differs at t={t}"
+        assert not gathered[P:].any() and not ddp["master"][P:].any()
+
+
 def pin_bucket_invariance(o):
     """A step run as per-bucket sub-range calls equals the whole-shard call bit
     for bit (the step is element-local)."""
@@ -1217,4 +1258,5 @@ ALL_PINS = [
     pin_accum_first_overwrites, pin_accum_ddp_equivalence, pin_rows_bruteforce,
     pin_rows_pages_layernorm, pin_rows_reshard, pin_rows_ddp_equivalence,
     pin_reshard_hand_examples, pin_reshard_invariants, pin_reshard_next_update,
+    pin_ddp_equivalence_gpt2_buckets,
 ]
