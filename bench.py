@@ -606,11 +606,17 @@ def run_ours(args, w):
                                         "timed just before; the host link is shared"}}
         del h_grads, h_out
 
-    # A practical ceiling beside the measured peak: a device-to-device copy of
-    # 4 GiB (8.6 GB of traffic), timed with events, median of 5.
+    # A practical ceiling beside the measured peak: a device-to-device copy
+    # moving the step's own algorithmic byte count (half read, half written;
+    # at least 1 GiB, at most what free memory allows), timed with events,
+    # median of 5.
     copy_gbs = None
+    copy_bytes = 0
     if not args.no_copy_ceiling:
-        src = torch.empty(1 << 32, dtype=torch.uint8, device=dev)
+        half = int(pipe_bpe * S) // 2 // 256 * 256
+        free = torch.cuda.mem_get_info(dev)[0]
+        copy_bytes = max(1 << 30, min(half, int(0.4 * free) // 256 * 256))
+        src = torch.empty(copy_bytes, dtype=torch.uint8, device=dev)
         dst = torch.empty_like(src)
         src.fill_(1)
         cts = []
@@ -622,7 +628,7 @@ def run_ours(args, w):
             torch.cuda.synchronize()
             if i >= 2:
                 cts.append(a.elapsed_time(b) / 1e3)
-        copy_gbs = 2 * (1 << 32) / statistics.median(cts) / 1e9
+        copy_gbs = 2 * copy_bytes / statistics.median(cts) / 1e9
         del src, dst
     if grank == 0:
         peak, peak_kind = measured_peak()
@@ -651,6 +657,7 @@ def run_ours(args, w):
                    "host": host_cpu(), "nproc": os.cpu_count()}
         if copy_gbs is not None:
             roofline["copy_ceiling_gbs"] = copy_gbs
+            roofline["copy_ceiling_bytes"] = 2 * copy_bytes
             roofline["frac_of_copy_ceiling"] = achieved / copy_gbs
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": gworld,
