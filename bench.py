@@ -18,6 +18,15 @@ barrier and a synchronize, and the slowest rank's time is reported.
 
 --impl reference times the CPU oracle (single thread) on a bounded sample of
 the same workload, on the host's cores, as the reference arm.
+
+Other measurements (--pipeline; the default is the step above):
+    clip        global-norm pass + clip coefficient + clipped step
+    accum       G-1 gradient accumulations + the accumulated step
+    gather      the AllGather's assembly of the other ranks' shards
+    unshard     FSDP2 copy-out of every wrap unit's gathered parameters
+    checkpoint  save, restore, and restore into world N/2 of one rank's state
+    sweep       the step over shard sizes x N x gradient and parameter dtypes
+--step-path forces either step kernel (register-streaming or staged).
 """
 from __future__ import annotations
 
