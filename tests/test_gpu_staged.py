@@ -206,3 +206,41 @@ def test_bounded_wait_runs_out_and_the_context_survives(orc):
         plan.free()
     finally:
         zs.zs_set_step_path(old)
+
+
+@pytest.mark.parametrize("N,bf16", [(2, True), (3, True), (4, True), (8, True), (16, True),
+                                    (2, False), (8, False)])
+def test_large_ranges_identical_bits(N, bf16):
+    """S = 2^25 (16,384 tiles; every stage of every block reused hundreds of
+    times), two steps through each kernel from the same inputs: master, m, v
+    and the parameter slot identical bit for bit. A stage released too early
+    or a copy landing late would show here."""
+    S = 1 << 25
+    plan = zs.zs_flatten_plan([N * S], world=N, align_elems=128)
+    assert plan.S == S
+    stream = torch.cuda.current_stream().cuda_stream
+    grads = [torch.empty(S * (2 if bf16 else 4), dtype=torch.uint8, device=DEV) for _ in range(N)]
+    outs = []
+    for path in (1, 2):
+        old = zs.zs_set_step_path(path)
+        try:
+            st = [torch.empty(S, dtype=torch.float32, device=DEV) for _ in range(3)]
+            synth.fill_device(st[0].data_ptr(), S, seed=11, stream=synth.STREAM_MASTER, sigma=0.02,
+                              cuda_stream=stream)
+            st[1].zero_()
+            st[2].zero_()
+            full = torch.zeros(N * S, dtype=torch.int16, device=DEV)
+            for t in (1, 2):
+                for j, g in enumerate(grads):
+                    synth.fill_device(g.data_ptr(), S, seed=11, rank=j, step=t, bf16=bf16,
+                                      cuda_stream=stream)
+                zs.zs_shard_step(plan, 0, 0, S, grads, zs.ZS_BF16 if bf16 else zs.ZS_FP32, *st,
+                                 full, zs.ZS_BF16, HP, t)
+            torch.cuda.synchronize()
+            outs.append([x.view(torch.int32) for x in st] + [full.narrow(0, 0, S)])
+        finally:
+            zs.zs_set_step_path(old)
+    zs.zs_check_device_error()
+    for name, a, b in zip(("master", "m", "v", "params"), *outs):
+        assert torch.equal(a, b), name
+    plan.free()
