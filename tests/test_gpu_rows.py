@@ -183,3 +183,31 @@ def test_rows_argument_errors():
         zs.zs_shard_rows(rows, 2, [small], zs.ZS_BF16, buf)
     flat.free()
     rows.free()
+
+
+def test_fsdp1_flat_units_gather(orc):
+    """FSDP1's layout, a FlatParameter per wrap unit: each of two Llama-7B
+    transformer blocks gets its own flat plan over N = 8 ranks; the ranks'
+    shards of each unit are assembled into the unit's flat buffer by
+    zs_gather_assemble (the AllGather's result) and every view lands on the
+    oracle's offsets, bytes identical to the oracle's gather."""
+    from synth.workloads import wrap_units
+    N = 8
+    for idx in wrap_units(LLAMA_7B)[:2]:
+        numels = [LLAMA_7B.params[i].numel for i in idx]
+        plan = zs.zs_flatten_plan(numels, world=N, align_elems=128)
+        op = orc.plan(numels, None, world=N, align=128)
+        S = plan.S
+        assert (S, plan.P_pad) == (op["S"], op["P_pad"])
+        shards = [synth.fill(S, index0=j * S, seed=21, rank=j, step=idx[0], p_limit=plan.P,
+                             bf16=True) for j in range(N)]
+        full = torch.zeros(plan.P_pad, dtype=torch.int16, device=DEV)
+        full.narrow(0, 3 * S, S).copy_(to_dev(shards[3]))        # rank 3's own slot
+        views = zs.zs_gather_assemble(plan, 3, [to_dev(x) for x in shards], full, zs.ZS_BF16)
+        ref = np.zeros(plan.P_pad, np.uint16)
+        orc.gather(world=N, S=S, elem_size=2, shards=shards, full_flat=ref)
+        torch.cuda.synchronize()
+        assert np.array_equal(to_host(full, np.uint16), ref)
+        base = full.data_ptr()
+        assert [(v - base) // 2 for v in views] == list(op["offsets"])
+        plan.free()
