@@ -13,7 +13,7 @@ import fsdp_sharded_mixed_gb300 as zs
 import oracle
 import synth
 from gpu_util import DEV, assert_params_close, assert_state_close, oracle_hp, to_dev, to_host
-from synth.workloads import LLAMA_7B
+from synth.workloads import GPT2_SMALL, LLAMA_7B
 
 pytestmark = pytest.mark.gpu
 
@@ -206,4 +206,24 @@ def test_norm_argument_errors():
     with pytest.raises(zs.ZsError) as e:
         zs.zs_clip_coefficient(out, 1, -1.0, c, f)
     assert e.value.status == zs.ZS_ERR_INVAL
+    plan.free()
+
+
+def test_gpt2_small_norm(orc):
+    """The GPT-2-small shard (S = 15,555,072, N = 8) against the oracle's sum
+    over 16 chunks."""
+    w = GPT2_SMALL
+    plan = zs.zs_flatten_plan(w.numels, w.tied_to, world=w.world, align_elems=w.align)
+    N, S, P = plan.world, plan.S, plan.P
+    rank = 5
+    stream = torch.cuda.current_stream().cuda_stream
+    grads = [torch.empty(S, dtype=torch.int16, device=DEV) for _ in range(N)]
+    for j, g in enumerate(grads):
+        synth.fill_device(g.data_ptr(), S, index0=rank * S, seed=w.seed, rank=j, step=1,
+                          sigma=w.grad_sigma, p_limit=P, bf16=True, cuda_stream=stream)
+    got = float(gpu_sqnorm(plan, rank, 0, S, grads, zs.ZS_BF16).item())
+    host = [synth.fill(S, index0=rank * S, seed=w.seed, rank=j, step=1, sigma=w.grad_sigma,
+                       p_limit=P, bf16=True) for j in range(N)]
+    ref = float(_chunked_oracle_sqnorm(orc, N, S, host))
+    assert abs(got - ref) <= sum_bound(S) * ref, (got, ref)
     plan.free()
