@@ -107,6 +107,9 @@ EXPORTS = {
     "zs_plan_free": ([_P], ctypes.c_int),
     "zs_shard_step": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _P, _P, _P, ctypes.c_int,
                        ctypes.POINTER(AdamWHparams), _I64, _P], ctypes.c_int),
+    "zs_shard_step_to_shard": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _P, _P, _P,
+                                ctypes.c_int, ctypes.POINTER(AdamWHparams), _I64, _P],
+                               ctypes.c_int),
     "zs_gather_assemble": ([_P, _I32, _P, _P, ctypes.c_int, _P, _P], ctypes.c_int),
     "zs_grad_norm_workspace_bytes": ([], _I64),
     "zs_grad_sqnorm": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _I64, _P, _P], ctypes.c_int),
@@ -281,6 +284,17 @@ def zs_shard_step(plan, rank, lo, hi, grad_slices, grad_dtype, master, exp_avg, 
     _check(lib().zs_shard_step(plan.handle, rank, lo, hi, ptrs, grad_dtype, _ptr(master),
                                _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(full_flat), param_dtype,
                                ctypes.byref(h), step, _stream(stream)))
+
+
+def zs_shard_step_to_shard(plan, rank, lo, hi, grad_slices, grad_dtype, master, exp_avg,
+                           exp_avg_sq, param_shard, param_dtype, hp, step, stream=None):
+    """``zs_shard_step`` writing the cast parameters into ``param_shard`` (S
+    elements of ``param_dtype``) instead of the rank's slot of the flat buffer."""
+    ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
+    h = AdamWHparams(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"])
+    _check(lib().zs_shard_step_to_shard(plan.handle, rank, lo, hi, ptrs, grad_dtype, _ptr(master),
+                                        _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(param_shard),
+                                        param_dtype, ctypes.byref(h), step, _stream(stream)))
 
 
 def zs_shard_step_clipped(plan, rank, lo, hi, grad_slices, grad_dtype, master, exp_avg,

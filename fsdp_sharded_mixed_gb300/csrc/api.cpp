@@ -138,7 +138,7 @@ zs_status shard_step_impl(const char* fn, const zs_plan* plan, int32_t rank, int
                           float* master, float* exp_avg, float* exp_avg_sq, void* full_flat,
                           zs_dtype param_dtype, const zs_adamw_hparams* hp, int64_t step,
                           const float* coef, const int32_t* skip, const float* accum,
-                          int32_t micro_steps, void* cuda_stream) {
+                          int32_t micro_steps, void* cuda_stream, bool shard_only = false) {
   zs::clear_error();
   if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
   const int32_t N = plan->world;
@@ -172,8 +172,11 @@ zs_status shard_step_impl(const char* fn, const zs_plan* plan, int32_t rank, int
     ranges.push_back({(uintptr_t)g, (uintptr_t)g + (uint64_t)S * gb, "grad_slices", j, false});
   }
   const void* outs[4] = {master, exp_avg, exp_avg_sq, full_flat};
-  const char* names[4] = {"master", "exp_avg", "exp_avg_sq", "full_flat"};
-  const int64_t out_bytes[4] = {S * 4, S * 4, S * 4, plan->P_pad * pb};
+  // full_flat: the flat buffer of all N slots, or (shard_only) the rank's own
+  // parameter shard of S elements.
+  const char* names[4] = {"master", "exp_avg", "exp_avg_sq",
+                          shard_only ? "param_shard" : "full_flat"};
+  const int64_t out_bytes[4] = {S * 4, S * 4, S * 4, (shard_only ? S : plan->P_pad) * pb};
   for (int k = 0; k < 4; ++k) {
     if (!aligned16(outs[k])) return zs::fail(ZS_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, names[k]);
     ranges.push_back({(uintptr_t)outs[k], (uintptr_t)outs[k] + (uint64_t)out_bytes[k], names[k], 0, true});
@@ -198,7 +201,7 @@ zs_status shard_step_impl(const char* fn, const zs_plan* plan, int32_t rank, int
   a.master = master;
   a.m = exp_avg;
   a.v = exp_avg_sq;
-  a.slot = static_cast<unsigned char*>(full_flat) + (uint64_t)rank * S * pb;
+  a.slot = static_cast<unsigned char*>(full_flat) + (shard_only ? 0 : (uint64_t)rank * S * pb);
   a.lo = lo;
   a.hi = hi;
   // The widest vector path every pointer allows: 32-byte accesses need all
@@ -254,6 +257,17 @@ extern "C" zs_status zs_shard_step(const zs_plan* plan, int32_t rank, int64_t lo
   return shard_step_impl("zs_shard_step", plan, rank, lo, hi, grad_slices, grad_dtype, master,
                          exp_avg, exp_avg_sq, full_flat, param_dtype, hp, step, nullptr, nullptr,
                          nullptr, 1, cuda_stream);
+}
+
+extern "C" zs_status zs_shard_step_to_shard(const zs_plan* plan, int32_t rank, int64_t lo,
+                                            int64_t hi, const void* const* grad_slices,
+                                            zs_dtype grad_dtype, float* master, float* exp_avg,
+                                            float* exp_avg_sq, void* param_shard,
+                                            zs_dtype param_dtype, const zs_adamw_hparams* hp,
+                                            int64_t step, void* cuda_stream) {
+  return shard_step_impl("zs_shard_step_to_shard", plan, rank, lo, hi, grad_slices, grad_dtype,
+                         master, exp_avg, exp_avg_sq, param_shard, param_dtype, hp, step, nullptr,
+                         nullptr, nullptr, 1, cuda_stream, true);
 }
 
 extern "C" zs_status zs_shard_step_clipped(const zs_plan* plan, int32_t rank, int64_t lo,

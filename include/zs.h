@@ -154,6 +154,21 @@ zs_status zs_shard_step(const zs_plan* plan, int32_t rank, int64_t lo, int64_t h
                         zs_dtype param_dtype, const zs_adamw_hparams* hp, int64_t step,
                         void* cuda_stream);
 
+/* zs_shard_step with the cast parameters written into the rank's own
+ * parameter shard instead of its slot of the flat buffer: param_shard is a
+ * device buffer of S elements of param_dtype, element 0 of the shard at index
+ * 0; elements [lo, hi) are written. For layouts that keep each rank's
+ * parameters as a persistent shard of their own and all-gather them into a
+ * transient buffer before use ([DP-to-ZeRO] "ZeRO 与 FSDP 的关系": FSDP2's
+ * per-parameter sharded state; [Dissection] §2.3 ZeRO-3: each rank keeps 1/N
+ * of the parameters). Same arithmetic, same kernels, same errors (param_shard
+ * in the place of full_flat). */
+zs_status zs_shard_step_to_shard(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                                 const void* const* grad_slices, zs_dtype grad_dtype,
+                                 float* master, float* exp_avg, float* exp_avg_sq,
+                                 void* param_shard, zs_dtype param_dtype,
+                                 const zs_adamw_hparams* hp, int64_t step, void* cuda_stream);
+
 /* ---------------------------------------------------------------------------
  * zs_gather_assemble — the AllGather's result on one GPU, and the unflatten.
  * [DP-to-ZeRO] "ZeRO Stage 1" (all-gather updated parameter shards; all

@@ -244,3 +244,38 @@ def test_large_ranges_identical_bits(N, bf16):
     for name, a, b in zip(("master", "m", "v", "params"), *outs):
         assert torch.equal(a, b), name
     plan.free()
+
+
+@pytest.mark.parametrize("path", [1, 2], indirect=True, ids=["direct", "staged"])
+@pytest.mark.parametrize("pdt", [oracle.BF16, oracle.FP24, oracle.FP32], ids=["bf16", "fp24", "fp32"])
+def test_step_to_shard_matches_oracle(orc, path, pdt):
+    """zs_shard_step_to_shard writes the parameters into a shard buffer of its
+    own (S elements, guard bands around it): its bytes equal the oracle's slot,
+    the state matches, and nothing outside [lo, hi) of the shard is written."""
+    N, rank = 4, 2
+    plan = zs.zs_flatten_plan([N * 60_000 - 37], world=N, align_elems=128)
+    S, P = plan.S, plan.P
+    lo, hi = 1111, S - 777
+    eb = oracle.ELEM_BYTES[pdt]
+    master0 = synth.fill(S, index0=rank * S, seed=8, stream=synth.STREAM_MASTER, sigma=0.02,
+                         p_limit=P)
+    o = [master0.copy(), np.zeros(S, np.float32), np.zeros(S, np.float32)]
+    d = [guarded(S * 4, x) for x in o]
+    o_full = np.zeros(plan.P_pad * eb, np.uint8)
+    shard_whole, shard = guarded(S * eb, np.zeros(S * eb, np.uint8))
+    for t in (1, 2):
+        g = [synth.fill(S, index0=rank * S, seed=8, rank=j, step=t, p_limit=P, bf16=True)
+             for j in range(N)]
+        zs.zs_shard_step_to_shard(plan, rank, lo, hi, [to_dev(x) for x in g], zs.ZS_BF16,
+                                  d[0][1], d[1][1], d[2][1], shard, ZS_OF[pdt], HP, t)
+        orc.shard_step(world=N, rank=rank, S=S, lo=lo, hi=hi, grads=g, master=o[0], m=o[1],
+                       v=o[2], full_flat=o_full, param_dtype=pdt, t=t, **oracle_hp(HP))
+    torch.cuda.synchronize()
+    zs.zs_check_device_error()
+    for name, (whole, inner), ref in zip(("master", "m", "v"), d, o):
+        assert assert_state_close(to_host(inner, np.float32), ref, name) == 0
+        assert guards_intact(whole)
+    got = to_host(shard, np.uint8)
+    assert np.array_equal(got, o_full[rank * S * eb:(rank + 1) * S * eb])
+    assert guards_intact(shard_whole)
+    plan.free()
