@@ -256,3 +256,30 @@ def test_not_a_checkpoint(tmp_path, saved):
     with pytest.raises(zs.ZsError) as e:
         zs.zs_checkpoint_info(junk)
     assert e.value.status == zs.ZS_ERR_CORRUPT
+
+
+def test_empty_plan_and_padding_ranks(tmp_path):
+    """An empty parameter list round-trips (S = 0, no arrays); restoring 10
+    elements saved by one rank into 8 ranks of 4 gives rank 2 elements 8, 9
+    and two zeros of padding, and rank 7 padding only."""
+    p0 = zs.zs_flatten_plan([], world=2)
+    assert p0.S == 0
+    paths = [str(tmp_path / f"e{r}") for r in range(2)]
+    for r in range(2):
+        zs.zs_checkpoint_save(p0, r, None, None, None, 5, paths[r])
+    assert zs.zs_checkpoint_load(p0, 1, paths, None, None, None) == 5
+    assert zs.zs_checkpoint_info(paths[0])["P"] == 0
+    p1 = zs.zs_flatten_plan([10], world=1, align_elems=1)
+    src = [np.arange(10, dtype=np.float32) + 100 * k for k in range(3)]
+    one = str(tmp_path / "s0")
+    zs.zs_checkpoint_save(p1, 0, *src, 3, one)
+    p8 = zs.zs_flatten_plan([10], world=8, align_elems=4)
+    assert p8.S == 4
+    for rank, want in ((2, [8, 9, 0, 0]), (7, [0, 0, 0, 0])):
+        out = [np.full(p8.S, np.nan, np.float32) for _ in range(3)]
+        assert zs.zs_checkpoint_load(p8, rank, [one], *out) == 3
+        for k in range(3):
+            exp = [x + 100 * k if i < 2 and rank == 2 else 0.0 for i, x in enumerate(want)]
+            assert out[k].tolist() == exp, (rank, k)
+    for p in (p0, p1, p8):
+        p.free()
