@@ -39,7 +39,7 @@ NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-fmad=false", "-prec-div
               "-prec-sqrt=true", "-ftz=false", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-pthread", "-I/usr/local/cuda/include"]
 CUDA_SOURCES = ["shard_step.cu", "gather.cu", "clip.cu", "accum.cu", "rows.cu", "ckpt.cu"]
-HOST_SOURCES = ["api.cpp", "plan.cpp", "checkpoint.cpp"]
+HOST_SOURCES = ["api.cpp", "plan.cpp", "checkpoint.cpp", "trace.cpp"]
 
 
 # ----------------------------------------------------------------- build ----
@@ -129,6 +129,8 @@ EXPORTS = {
     "zs_checkpoint_save": ([_P, _I32, _P, _P, _P, _I64, ctypes.c_char_p, _P], ctypes.c_int),
     "zs_checkpoint_load": ([_P, _I32, _P, _I32, _P, _P, _P, _P, _P], ctypes.c_int),
     "zs_checkpoint_info": ([ctypes.c_char_p, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "zs_set_trace": ([ctypes.c_char_p], ctypes.c_int),
+    "zs_trace_first_divergence": ([_P, _I32, _P, ctypes.c_char_p, _I64], ctypes.c_int),
     "zs_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "zs_last_error": ([], ctypes.c_char_p),
     "zs_check_device_error": ([_P], ctypes.c_int),
@@ -415,6 +417,21 @@ def zs_checkpoint_info(path):
 def zs_selftest_wait_timeout(polls, stream=None):
     """Enqueue a bounded wait that runs out (see include/zs.h)."""
     _check(lib().zs_selftest_wait_timeout(polls, _stream(stream)))
+
+
+def zs_set_trace(path):
+    """Per-call trace to ``path`` (``%r`` = RANK, ``%p`` = pid); None = off."""
+    _check(lib().zs_set_trace(None if path is None else os.fsencode(path)))
+
+
+def zs_trace_first_divergence(paths):
+    """The first record at which the ranks' traces disagree: (index, detail),
+    or None when they agree throughout."""
+    arr = (ctypes.c_char_p * len(paths))(*[os.fsencode(p) for p in paths])
+    seq = ctypes.c_int64()
+    buf = ctypes.create_string_buffer(8192)
+    _check(lib().zs_trace_first_divergence(arr, len(paths), ctypes.byref(seq), buf, len(buf)))
+    return None if seq.value < 0 else (seq.value, buf.value.decode())
 
 
 def zs_check_device_error(stream=None):

@@ -248,7 +248,7 @@ zs_status check_device_scalar(const void* p, int64_t bytes, const char* fn, cons
 
 }  // namespace
 
-extern "C" zs_status zs_shard_step(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+static zs_status zs_shard_step_untraced(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
                                    const void* const* grad_slices, zs_dtype grad_dtype,
                                    float* master, float* exp_avg, float* exp_avg_sq,
                                    void* full_flat, zs_dtype param_dtype,
@@ -259,7 +259,7 @@ extern "C" zs_status zs_shard_step(const zs_plan* plan, int32_t rank, int64_t lo
                          nullptr, 1, cuda_stream);
 }
 
-extern "C" zs_status zs_shard_step_to_shard(const zs_plan* plan, int32_t rank, int64_t lo,
+static zs_status zs_shard_step_to_shard_untraced(const zs_plan* plan, int32_t rank, int64_t lo,
                                             int64_t hi, const void* const* grad_slices,
                                             zs_dtype grad_dtype, float* master, float* exp_avg,
                                             float* exp_avg_sq, void* param_shard,
@@ -270,7 +270,7 @@ extern "C" zs_status zs_shard_step_to_shard(const zs_plan* plan, int32_t rank, i
                          nullptr, nullptr, 1, cuda_stream, true);
 }
 
-extern "C" zs_status zs_shard_step_clipped(const zs_plan* plan, int32_t rank, int64_t lo,
+static zs_status zs_shard_step_clipped_untraced(const zs_plan* plan, int32_t rank, int64_t lo,
                                            int64_t hi, const void* const* grad_slices,
                                            zs_dtype grad_dtype, float* master, float* exp_avg,
                                            float* exp_avg_sq, void* full_flat,
@@ -288,7 +288,7 @@ extern "C" zs_status zs_shard_step_clipped(const zs_plan* plan, int32_t rank, in
                          cuda_stream);
 }
 
-extern "C" zs_status zs_shard_step_accumulated(const zs_plan* plan, int32_t rank, int64_t lo,
+static zs_status zs_shard_step_accumulated_untraced(const zs_plan* plan, int32_t rank, int64_t lo,
                                                int64_t hi, const void* const* grad_slices,
                                                zs_dtype grad_dtype, const float* accum,
                                                int32_t micro_steps, float* master,
@@ -306,7 +306,7 @@ extern "C" zs_status zs_shard_step_accumulated(const zs_plan* plan, int32_t rank
                          micro_steps, cuda_stream);
 }
 
-extern "C" zs_status zs_grad_accumulate(const zs_plan* plan, int32_t rank, int64_t lo,
+static zs_status zs_grad_accumulate_untraced(const zs_plan* plan, int32_t rank, int64_t lo,
                                         int64_t hi, const void* const* grad_slices,
                                         zs_dtype grad_dtype, float* accum, int32_t first,
                                         void* cuda_stream) {
@@ -359,7 +359,7 @@ extern "C" zs_status zs_grad_accumulate(const zs_plan* plan, int32_t rank, int64
 
 extern "C" int64_t zs_grad_norm_workspace_bytes(void) { return zs::kNormWorkspaceBytes; }
 
-extern "C" zs_status zs_grad_sqnorm(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+static zs_status zs_grad_sqnorm_untraced(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
                                     const void* const* grad_slices, zs_dtype grad_dtype,
                                     void* workspace, int64_t workspace_bytes, double* sqnorm_out,
                                     void* cuda_stream) {
@@ -415,7 +415,7 @@ extern "C" zs_status zs_grad_sqnorm(const zs_plan* plan, int32_t rank, int64_t l
   return ZS_OK;
 }
 
-extern "C" zs_status zs_grad_sqnorm_noalloc(const zs_plan* plan, int32_t rank, int64_t lo,
+static zs_status zs_grad_sqnorm_noalloc_untraced(const zs_plan* plan, int32_t rank, int64_t lo,
                                             int64_t hi, const void* const* grad_slices,
                                             zs_dtype grad_dtype, double* sqnorm_out,
                                             void* cuda_stream) {
@@ -467,7 +467,7 @@ extern "C" zs_status zs_grad_sqnorm_noalloc(const zs_plan* plan, int32_t rank, i
   return ZS_OK;
 }
 
-extern "C" zs_status zs_clip_coefficient(const double* rank_sqnorms, int32_t n, double max_norm,
+static zs_status zs_clip_coefficient_untraced(const double* rank_sqnorms, int32_t n, double max_norm,
                                          float* coef_out, int32_t* nonfinite_out,
                                          void* cuda_stream) {
   static const char* fn = "zs_clip_coefficient";
@@ -487,7 +487,7 @@ extern "C" zs_status zs_clip_coefficient(const double* rank_sqnorms, int32_t n, 
   return ZS_OK;
 }
 
-extern "C" zs_status zs_gather_assemble(const zs_plan* plan, int32_t rank,
+static zs_status zs_gather_assemble_untraced(const zs_plan* plan, int32_t rank,
                                         const void* const* shard_srcs, void* full_flat,
                                         zs_dtype param_dtype, void** views_out,
                                         void* cuda_stream) {
@@ -570,7 +570,7 @@ zs_status check_rows_params(const zs_plan* plan, const void* const* params, int 
 
 }  // namespace
 
-extern "C" zs_status zs_unshard(const zs_plan* plan, const void* gathered, zs_dtype dtype,
+static zs_status zs_unshard_untraced(const zs_plan* plan, const void* gathered, zs_dtype dtype,
                                 void* const* params_out, void* cuda_stream) {
   static const char* fn = "zs_unshard";
   zs::clear_error();
@@ -614,7 +614,7 @@ extern "C" zs_status zs_unshard(const zs_plan* plan, const void* gathered, zs_dt
   return ZS_OK;
 }
 
-extern "C" zs_status zs_shard_rows(const zs_plan* plan, int32_t rank, const void* const* params_in,
+static zs_status zs_shard_rows_untraced(const zs_plan* plan, int32_t rank, const void* const* params_in,
                                    zs_dtype dtype, void* local_out, void* cuda_stream) {
   static const char* fn = "zs_shard_rows";
   zs::clear_error();
@@ -725,3 +725,117 @@ extern "C" int32_t zs_set_validation(int32_t level) {
 }
 
 extern "C" const char* zs_version(void) { return "0.1.0"; }
+
+// ---- traced entry points ----------------------------------------------------------
+// Each call at a collective site of the real system leaves one record in the
+// per-call trace (trace.cpp) with its status, whatever path it returned by.
+extern "C" zs_status zs_shard_step(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                                   const void* const* grad_slices, zs_dtype grad_dtype,
+                                   float* master, float* exp_avg, float* exp_avg_sq,
+                                   void* full_flat, zs_dtype param_dtype,
+                                   const zs_adamw_hparams* hp, int64_t step,
+                                   void* cuda_stream) {
+  return zs::traced(zs_shard_step_untraced(plan, rank, lo, hi, grad_slices, grad_dtype, master,
+                                           exp_avg, exp_avg_sq, full_flat, param_dtype, hp,
+                                           step, cuda_stream),
+                    "zs_shard_step", plan, rank, lo, hi, grad_dtype, param_dtype, step);
+}
+
+extern "C" zs_status zs_shard_step_to_shard(const zs_plan* plan, int32_t rank, int64_t lo,
+                                            int64_t hi, const void* const* grad_slices,
+                                            zs_dtype grad_dtype, float* master, float* exp_avg,
+                                            float* exp_avg_sq, void* param_shard,
+                                            zs_dtype param_dtype, const zs_adamw_hparams* hp,
+                                            int64_t step, void* cuda_stream) {
+  return zs::traced(zs_shard_step_to_shard_untraced(plan, rank, lo, hi, grad_slices, grad_dtype,
+                                                    master, exp_avg, exp_avg_sq, param_shard,
+                                                    param_dtype, hp, step, cuda_stream),
+                    "zs_shard_step_to_shard", plan, rank, lo, hi, grad_dtype, param_dtype, step);
+}
+
+extern "C" zs_status zs_shard_step_clipped(const zs_plan* plan, int32_t rank, int64_t lo,
+                                           int64_t hi, const void* const* grad_slices,
+                                           zs_dtype grad_dtype, float* master, float* exp_avg,
+                                           float* exp_avg_sq, void* full_flat,
+                                           zs_dtype param_dtype, const zs_adamw_hparams* hp,
+                                           int64_t step, const float* coef,
+                                           const int32_t* skip, void* cuda_stream) {
+  return zs::traced(zs_shard_step_clipped_untraced(plan, rank, lo, hi, grad_slices, grad_dtype,
+                                                   master, exp_avg, exp_avg_sq, full_flat,
+                                                   param_dtype, hp, step, coef, skip,
+                                                   cuda_stream),
+                    "zs_shard_step_clipped", plan, rank, lo, hi, grad_dtype, param_dtype, step);
+}
+
+extern "C" zs_status zs_shard_step_accumulated(const zs_plan* plan, int32_t rank, int64_t lo,
+                                               int64_t hi, const void* const* grad_slices,
+                                               zs_dtype grad_dtype, const float* accum,
+                                               int32_t micro_steps, float* master,
+                                               float* exp_avg, float* exp_avg_sq,
+                                               void* full_flat, zs_dtype param_dtype,
+                                               const zs_adamw_hparams* hp, int64_t step,
+                                               void* cuda_stream) {
+  return zs::traced(zs_shard_step_accumulated_untraced(plan, rank, lo, hi, grad_slices,
+                                                       grad_dtype, accum, micro_steps, master,
+                                                       exp_avg, exp_avg_sq, full_flat,
+                                                       param_dtype, hp, step, cuda_stream),
+                    "zs_shard_step_accumulated", plan, rank, lo, hi, grad_dtype, param_dtype,
+                    step);
+}
+
+extern "C" zs_status zs_grad_accumulate(const zs_plan* plan, int32_t rank, int64_t lo,
+                                        int64_t hi, const void* const* grad_slices,
+                                        zs_dtype grad_dtype, float* accum, int32_t first,
+                                        void* cuda_stream) {
+  return zs::traced(zs_grad_accumulate_untraced(plan, rank, lo, hi, grad_slices, grad_dtype,
+                                                accum, first, cuda_stream),
+                    "zs_grad_accumulate", plan, rank, lo, hi, grad_dtype, -1, 0);
+}
+
+extern "C" zs_status zs_grad_sqnorm(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                                    const void* const* grad_slices, zs_dtype grad_dtype,
+                                    void* workspace, int64_t workspace_bytes,
+                                    double* sqnorm_out, void* cuda_stream) {
+  return zs::traced(zs_grad_sqnorm_untraced(plan, rank, lo, hi, grad_slices, grad_dtype,
+                                            workspace, workspace_bytes, sqnorm_out,
+                                            cuda_stream),
+                    "zs_grad_sqnorm", plan, rank, lo, hi, grad_dtype, -1, 0);
+}
+
+extern "C" zs_status zs_grad_sqnorm_noalloc(const zs_plan* plan, int32_t rank, int64_t lo,
+                                            int64_t hi, const void* const* grad_slices,
+                                            zs_dtype grad_dtype, double* sqnorm_out,
+                                            void* cuda_stream) {
+  return zs::traced(zs_grad_sqnorm_noalloc_untraced(plan, rank, lo, hi, grad_slices, grad_dtype,
+                                                    sqnorm_out, cuda_stream),
+                    "zs_grad_sqnorm_noalloc", plan, rank, lo, hi, grad_dtype, -1, 0);
+}
+
+extern "C" zs_status zs_clip_coefficient(const double* rank_sqnorms, int32_t n, double max_norm,
+                                         float* coef_out, int32_t* nonfinite_out,
+                                         void* cuda_stream) {
+  return zs::traced(zs_clip_coefficient_untraced(rank_sqnorms, n, max_norm, coef_out,
+                                                 nonfinite_out, cuda_stream),
+                    "zs_clip_coefficient", nullptr, -1, 0, 0, -1, -1, 0, n);
+}
+
+extern "C" zs_status zs_gather_assemble(const zs_plan* plan, int32_t rank,
+                                        const void* const* shard_srcs, void* full_flat,
+                                        zs_dtype param_dtype, void** views_out,
+                                        void* cuda_stream) {
+  return zs::traced(zs_gather_assemble_untraced(plan, rank, shard_srcs, full_flat, param_dtype,
+                                                views_out, cuda_stream),
+                    "zs_gather_assemble", plan, rank, 0, 0, -1, param_dtype, 0);
+}
+
+extern "C" zs_status zs_unshard(const zs_plan* plan, const void* gathered, zs_dtype dtype,
+                                void* const* params_out, void* cuda_stream) {
+  return zs::traced(zs_unshard_untraced(plan, gathered, dtype, params_out, cuda_stream),
+                    "zs_unshard", plan, -1, 0, 0, -1, dtype, 0);
+}
+
+extern "C" zs_status zs_shard_rows(const zs_plan* plan, int32_t rank, const void* const* params_in,
+                                   zs_dtype dtype, void* local_out, void* cuda_stream) {
+  return zs::traced(zs_shard_rows_untraced(plan, rank, params_in, dtype, local_out, cuda_stream),
+                    "zs_shard_rows", plan, rank, 0, 0, -1, dtype, 0);
+}

@@ -525,7 +525,7 @@ zs_status read_header(int fd, const char* path, Header* h, const char* fn) {
 
 }  // namespace
 
-extern "C" zs_status zs_checkpoint_save(const zs_plan* plan, int32_t rank, const float* master,
+static zs_status zs_checkpoint_save_untraced(const zs_plan* plan, int32_t rank, const float* master,
                                         const float* exp_avg, const float* exp_avg_sq,
                                         int64_t step, const char* path, void* cuda_stream) {
   static const char* fn = "zs_checkpoint_save";
@@ -732,7 +732,7 @@ extern "C" zs_status zs_checkpoint_info(const char* path, int32_t* world, int32_
   return ZS_OK;
 }
 
-extern "C" zs_status zs_checkpoint_load(const zs_plan* plan, int32_t rank,
+static zs_status zs_checkpoint_load_untraced(const zs_plan* plan, int32_t rank,
                                         const char* const* paths, int32_t n_paths, float* master,
                                         float* exp_avg, float* exp_avg_sq, int64_t* step,
                                         void* cuda_stream) {
@@ -1015,4 +1015,24 @@ extern "C" zs_status zs_checkpoint_load(const zs_plan* plan, int32_t rank,
   }
   if (step) *step = h0.step;
   return ZS_OK;
+}
+
+// ---- traced entry points ----------------------------------------------------------
+extern "C" zs_status zs_checkpoint_save(const zs_plan* plan, int32_t rank, const float* master,
+                                        const float* exp_avg, const float* exp_avg_sq,
+                                        int64_t step, const char* path, void* cuda_stream) {
+  return zs::traced(zs_checkpoint_save_untraced(plan, rank, master, exp_avg, exp_avg_sq, step,
+                                                path, cuda_stream),
+                    "zs_checkpoint_save", plan, rank, 0, 0, -1, -1, step);
+}
+
+extern "C" zs_status zs_checkpoint_load(const zs_plan* plan, int32_t rank,
+                                        const char* const* paths, int32_t n_paths, float* master,
+                                        float* exp_avg, float* exp_avg_sq, int64_t* step,
+                                        void* cuda_stream) {
+  int64_t saved = -1;
+  const zs_status st = zs_checkpoint_load_untraced(plan, rank, paths, n_paths, master, exp_avg,
+                                                   exp_avg_sq, &saved, cuda_stream);
+  if (st == ZS_OK && step) *step = saved;
+  return zs::traced(st, "zs_checkpoint_load", plan, rank, 0, 0, -1, -1, saved);
 }

@@ -127,6 +127,12 @@ int block_hash_parts(int64_t blocks, int64_t block_bytes);
 // [p, p + bytes) inside one allocation.
 zs_status check_device_array(const void* p, int64_t bytes, const char* fn, const char* name);
 
+// Appends one record of a call to the per-call trace when tracing is on
+// (trace.cpp) and returns st. grad_dtype / param_dtype -1 = not applicable;
+// world is used when plan is not a live plan.
+zs_status traced(zs_status st, const char* call, const zs_plan* plan, int32_t rank, int64_t lo,
+                 int64_t hi, int grad_dtype, int param_dtype, int64_t step, int32_t world = 0);
+
 // Which kernel runs the step: 0 = chosen per call, 1 = the register-streaming
 // kernel, 2 = the staged kernel wherever it is eligible (zs_set_step_path).
 int step_path();

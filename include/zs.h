@@ -381,6 +381,42 @@ zs_status zs_checkpoint_load(const zs_plan* plan, int32_t rank, const char* cons
 zs_status zs_checkpoint_info(const char* path, int32_t* world, int32_t* rank, int32_t* layout,
                              int32_t* n_params, int64_t* P, int64_t* S, int64_t* step);
 
+/* -------------------------------------------------------------------------
+ * Per-call trace. [DP-to-ZeRO] "训练 Hang 应按 Collective 顺序排查": ZeRO/FSDP
+ * issue their collectives from hooks, so ranks that run modules in another
+ * order or another number of times end up waiting in different collectives;
+ * the section's remedy is to log, for each collective, its sequence number,
+ * group, numel, dtype, module and phase, and look for the first place where
+ * the ranks' logs part.
+ *
+ * Each call that stands at a collective of the real system (the steps, the
+ * accumulation, the norm and the clip coefficient, the gather assembly, the
+ * row copy-out and copy-in, checkpoint save and load) appends one line to
+ * this process's trace when tracing is on, after it returns:
+ *   seq=<n> call=<name> plan=<id> world=<N> S=<shard elements> rank=<r>
+ *   lo=<lo> hi=<hi> grad=<dtype> param=<dtype> step=<t> status=<code>
+ * seq counts from 0 per trace file; plan is a 64-bit hash of the plan's
+ * parameter list and layout ("-" when the call has no live plan); dtypes are
+ * bf16 / fp32 / fp24 or "-". Tracing is off until ZS_TRACE names a file
+ * (read at the first traced call) or zs_set_trace is called; in the name, %r
+ * stands for the RANK environment variable (0 if unset) and %p for the
+ * process id. Lines are appended under a lock and flushed per record. The
+ * pages have no device-side counterpart; this is the host log they ask for.
+ * ------------------------------------------------------------------------- */
+/* Opens `path` (expanded as above, appended to) as this process's trace and
+ * restarts seq at 0; NULL or "" turns tracing off (and ZS_TRACE is not read
+ * afterwards). ZS_ERR_IO if the file cannot be opened (tracing is then off). */
+zs_status zs_set_trace(const char* path);
+/* Compares the traces of the ranks of one job record by record on the fields
+ * all ranks must share at one seq (call, plan, world, S, grad, param, step;
+ * not rank, lo, hi, status) and reports the first seq at which they differ,
+ * or at which a trace ends while another goes on: *seq_out = that seq, or -1
+ * when all agree to the end. `detail` (if not NULL, `detail_bytes` long)
+ * receives the differing records, one per trace, NUL-terminated and cut to
+ * fit. n_paths >= 2. ZS_ERR_IO if a file cannot be read. */
+zs_status zs_trace_first_divergence(const char* const* paths, int32_t n_paths, int64_t* seq_out,
+                                    char* detail, int64_t detail_bytes);
+
 /* Diagnostics. */
 const char* zs_status_string(zs_status status);
 const char* zs_last_error(void);
