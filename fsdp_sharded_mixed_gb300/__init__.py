@@ -25,6 +25,10 @@ _ROOT = os.path.dirname(_HERE)
 CSRC = os.path.join(_HERE, "csrc")
 BUILD_DIR = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_HERE, "libzs.so")
+# The same library with every kernel access checked against its launch's
+# window (CUDA sources compiled with ZS_BOUNDS_CHECK=1); loaded instead of
+# libzs.so when the environment variable ZS_BOUNDS_CHECK is 1.
+CHECKED_LIB_PATH = os.path.join(_HERE, "libzs_checked.so")
 INCLUDE = os.path.join(_ROOT, "include")
 
 ZS_OK, ZS_ERR_INVAL, ZS_ERR_ALIGN, ZS_ERR_RANGE = 0, -1, -2, -3
@@ -44,23 +48,29 @@ HOST_SOURCES = ["api.cpp", "plan.cpp", "checkpoint.cpp", "trace.cpp"]
 
 # ----------------------------------------------------------------- build ----
 def _compile_jobs():
+    """(command, object, variant) per translation unit: the CUDA sources once
+    per variant ("" ordinary, "checked" bounds-checked), the host sources once
+    (they are the same in both libraries)."""
     jobs = []
-    for src in CUDA_SOURCES:
-        obj = os.path.join(BUILD_DIR, src + ".o")
-        jobs.append((["nvcc", "-c", *NVCC_FLAGS, os.path.join(CSRC, src), "-o", obj], obj))
+    for variant, defs in (("", []), ("checked", ["-DZS_BOUNDS_CHECK=1"])):
+        for src in CUDA_SOURCES:
+            obj = os.path.join(BUILD_DIR, variant, src + ".o")
+            jobs.append((["nvcc", "-c", *NVCC_FLAGS, *defs, os.path.join(CSRC, src), "-o", obj],
+                         obj, variant))
     for src in HOST_SOURCES:
         obj = os.path.join(BUILD_DIR, src + ".o")
-        jobs.append((["g++", "-c", *CXX_FLAGS, os.path.join(CSRC, src), "-o", obj], obj))
+        jobs.append((["g++", "-c", *CXX_FLAGS, os.path.join(CSRC, src), "-o", obj], obj, None))
     return jobs
 
 
 def build(log=True):
-    """Compile the library for sm_103a in-tree (sources in parallel) and link."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    """Compile both libraries for sm_103a in-tree (sources in parallel) and
+    link them: libzs.so and the bounds-checked libzs_checked.so."""
+    os.makedirs(os.path.join(BUILD_DIR, "checked"), exist_ok=True)
     jobs = _compile_jobs()
 
     def run(job):
-        cmd, _ = job
+        cmd = job[0]
         p = subprocess.run(cmd, capture_output=True, text=True)
         return cmd, p.returncode, p.stdout + p.stderr
 
@@ -71,11 +81,13 @@ def build(log=True):
         report.append("$ " + " ".join(cmd) + "\n" + out)
         if rc != 0:
             raise RuntimeError("libzs build failed:\n" + out)
-    link = ["nvcc", "-shared", *ARCH, "-o", LIB_PATH + ".tmp", *[o for _, o in jobs]]
-    p = subprocess.run(link, capture_output=True, text=True)
-    if p.returncode != 0:
-        raise RuntimeError("libzs link failed:\n" + p.stdout + p.stderr)
-    os.replace(LIB_PATH + ".tmp", LIB_PATH)
+    for variant, path in (("", LIB_PATH), ("checked", CHECKED_LIB_PATH)):
+        objs = [o for _, o, v in jobs if v in (variant, None)]
+        link = ["nvcc", "-shared", *ARCH, "-o", path + ".tmp", *objs]
+        p = subprocess.run(link, capture_output=True, text=True)
+        if p.returncode != 0:
+            raise RuntimeError(f"{os.path.basename(path)} link failed:\n" + p.stdout + p.stderr)
+        os.replace(path + ".tmp", path)
     if log:
         with open(os.path.join(BUILD_DIR, "build.log"), "w") as f:
             f.write("\n".join(report))
@@ -137,18 +149,26 @@ EXPORTS = {
     "zs_set_validation": ([_I32], _I32),
     "zs_set_step_path": ([_I32], _I32),
     "zs_selftest_wait_timeout": ([ctypes.c_uint32, _P], ctypes.c_int),
+    "zs_bounds_checked": ([], _I32),
+    "zs_selftest_bounds_window": ([_I64], ctypes.c_int),
     "zs_version": ([], ctypes.c_char_p),
 }
+
+
+def lib_path():
+    """The library this process uses: libzs_checked.so when ZS_BOUNDS_CHECK=1."""
+    return CHECKED_LIB_PATH if os.environ.get("ZS_BOUNDS_CHECK") == "1" else LIB_PATH
 
 
 def lib():
     """The loaded C library; raises if it has not been built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: the CUDA library must be built "
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: the CUDA library must be built "
                                "(__graft_entry__.build()); there is no fallback")
-        L = ctypes.CDLL(LIB_PATH)
+        L = ctypes.CDLL(path)
         for name, (args, res) in EXPORTS.items():
             f = getattr(L, name)
             f.argtypes = args
@@ -417,6 +437,17 @@ def zs_checkpoint_info(path):
 def zs_selftest_wait_timeout(polls, stream=None):
     """Enqueue a bounded wait that runs out (see include/zs.h)."""
     _check(lib().zs_selftest_wait_timeout(polls, _stream(stream)))
+
+
+def zs_bounds_checked():
+    """True when the loaded library is the bounds-checked build."""
+    return bool(lib().zs_bounds_checked())
+
+
+def zs_selftest_bounds_window(shrink):
+    """Bounds-checked build only: narrow the window the step, accumulation and
+    norm kernels check against by ``shrink`` elements at each end (0 = off)."""
+    _check(lib().zs_selftest_bounds_window(shrink))
 
 
 def zs_set_trace(path):

@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   auto one = [&](int64_t i) {
+    if (!within(i, i + 1, a.win_lo, a.win_hi, a.err)) return;
     float acc = 0.0f;
     for (int j = 0; j < a.world; ++j) {
       const float x = BF16G ? __uint_as_float(
@@ -54,6 +55,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (tid < head) one(a.lo + tid);
     else if (tid < head + tail) one(g1 * GW + (tid - head));
     for (int64_t g = g0 + tid; g < g1; g += stride) {
+      if (!within(GW * g, GW * g + GW, a.win_lo, a.win_hi, a.err)) continue;
       float prev[GW], acc[GW];
       if (!first) load_state<GW>(accum + GW * g, prev);
       reduce_group<GW, BF16G>(a, g, acc);
@@ -95,6 +97,10 @@ cudaError_t launch_acc(const ShardStepLaunch& in, int first, cudaStream_t stream
   a.accum = in.accum;
   a.invG = 1.0f;
   a.s = in.s;
+  a.win_lo = in.win.lo;
+  a.win_hi = in.win.hi;
+  a.err = ZS_BOUNDS_CHECK ? device_error_word() : nullptr;
+  if (ZS_BOUNDS_CHECK && !a.err) return cudaErrorInvalidSymbol;
   const int64_t units = GW > 0 ? (in.hi - in.lo) / GW + 2 : (in.hi - in.lo);
   int64_t blocks = (units + kThreads - 1) / kThreads;
   if (blocks > max_blocks) blocks = max_blocks;

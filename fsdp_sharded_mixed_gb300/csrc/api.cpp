@@ -204,6 +204,7 @@ zs_status shard_step_impl(const char* fn, const zs_plan* plan, int32_t rank, int
   a.slot = static_cast<unsigned char*>(full_flat) + (shard_only ? 0 : (uint64_t)rank * S * pb);
   a.lo = lo;
   a.hi = hi;
+  a.win = zs::step_window(lo, hi);
   // The widest vector path every pointer allows: 32-byte accesses need all
   // bases (and the slot's 16-element groups) 32-byte aligned; 16-byte
   // accesses need the slot's 8-element groups aligned; else element by element.
@@ -346,6 +347,7 @@ static zs_status zs_grad_accumulate_untraced(const zs_plan* plan, int32_t rank, 
   a.param_dtype = ZS_BF16;
   a.lo = lo;
   a.hi = hi;
+  a.win = zs::step_window(lo, hi);
   a.vec_width = all32 ? 16 : 8;
   a.accum = accum;
   a.invG = 1.0f;
@@ -403,6 +405,7 @@ static zs_status zs_grad_sqnorm_untraced(const zs_plan* plan, int32_t rank, int6
   a.grad_dtype = grad_dtype;
   a.lo = lo;
   a.hi = hi;
+  a.win = zs::step_window(lo, hi);
   a.vec = all32;
   a.invN = (float)(1.0 / (double)N);
   a.partials = static_cast<double*>(workspace);
@@ -456,6 +459,7 @@ static zs_status zs_grad_sqnorm_noalloc_untraced(const zs_plan* plan, int32_t ra
   a.grad_dtype = grad_dtype;
   a.lo = lo;
   a.hi = hi;
+  a.win = zs::step_window(lo, hi);
   a.vec = all32;
   a.invN = (float)(1.0 / (double)N);
   a.partials = nullptr;  // set to the static array by the launcher
@@ -697,11 +701,31 @@ extern "C" zs_status zs_check_device_error(void* cuda_stream) {
 
 namespace {
 std::atomic<int32_t> g_step_path{0};
+std::atomic<int64_t> g_bounds_shrink{0};
 }  // namespace
 
 namespace zs {
 int step_path() { return g_step_path.load(std::memory_order_relaxed); }
+
+Window step_window(int64_t lo, int64_t hi) {
+  const int64_t k = g_bounds_shrink.load(std::memory_order_relaxed);
+  return Window{lo + k, hi - k};
+}
 }  // namespace zs
+
+extern "C" int32_t zs_bounds_checked(void) { return zs::bounds_checked(); }
+
+extern "C" zs_status zs_selftest_bounds_window(int64_t shrink) {
+  zs::clear_error();
+  if (!zs::bounds_checked())
+    return zs::fail(ZS_ERR_UNSUPPORTED,
+                    "zs_selftest_bounds_window: this library is not the bounds-checked build");
+  if (shrink < 0 || shrink > (int64_t(1) << 40))
+    return zs::fail(ZS_ERR_RANGE, "zs_selftest_bounds_window: shrink %lld outside 0..2^40",
+                    (long long)shrink);
+  g_bounds_shrink.store(shrink);
+  return ZS_OK;
+}
 
 extern "C" zs_status zs_selftest_wait_timeout(uint32_t polls, void* cuda_stream) {
   zs::clear_error();

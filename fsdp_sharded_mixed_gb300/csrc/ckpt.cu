@@ -12,6 +12,7 @@
 #include <stdint.h>
 
 #include "block_hash.h"
+#include "bounds.cuh"
 #include "zs_internal.h"
 
 namespace zs {
@@ -44,7 +45,7 @@ __global__ void __launch_bounds__(kThreads) block_hash_kernel(const unsigned cha
                                                               int64_t bytes, int64_t first_block,
                                                               int64_t block_bytes,
                                                               uint32_t array_id, int parts,
-                                                              uint64_t* out) {
+                                                              uint64_t* out, unsigned int* err) {
   const int64_t j = blockIdx.x / parts;
   const int p = (int)(blockIdx.x % parts);
   const int64_t len = bytes - j * block_bytes < block_bytes ? bytes - j * block_bytes
@@ -53,10 +54,13 @@ __global__ void __launch_bounds__(kThreads) block_hash_kernel(const unsigned cha
   const int64_t s0 = p * slice;
   const int64_t s1 = s0 + slice < len ? s0 + slice : len;
   const unsigned char* blk = data + j * block_bytes;
+  // Checked build: the slice lies in its block, and the block in the data.
+  const bool ok = within(j * block_bytes, j * block_bytes + len, 0, bytes, err) &&
+                  (s0 >= s1 || within(s0, s1, 0, len, err));
   const uint64_t base = hash_base(array_id, first_block + j, block_bytes);
   constexpr int U = 4;
   uint64_t acc = 0;
-  if (s0 < s1) {
+  if (ok && s0 < s1) {
     // 16-byte vectors i in [v0, v1) of the block (word 2i and 2i + 1).
     const int64_t v0 = s0 / 16, v1 = s1 / 16;
     for (int64_t i0 = v0; i0 < v1; i0 += (int64_t)kThreads * U) {
@@ -85,7 +89,7 @@ __global__ void __launch_bounds__(kThreads) block_hash_kernel(const unsigned cha
   __shared__ uint64_t warp_sum[kThreads / 32];
   if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = acc;
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && within(blockIdx.x, blockIdx.x + 1, 0, (int64_t)gridDim.x, err)) {
     uint64_t sum = p == 0 ? hash_seed(len, array_id) : 0;
     for (int w = 0; w < kThreads / 32; ++w) sum += warp_sum[w];
     out[blockIdx.x] = sum;
@@ -99,9 +103,11 @@ cudaError_t launch_block_hash(const void* data, int64_t bytes, int64_t first_blo
                               cudaStream_t stream) {
   if (bytes <= 0) return cudaSuccess;
   const int64_t blocks = (bytes + block_bytes - 1) / block_bytes;
+  unsigned int* err = ZS_BOUNDS_CHECK ? device_error_word() : nullptr;
+  if (ZS_BOUNDS_CHECK && !err) return cudaErrorInvalidSymbol;
   block_hash_kernel<<<(unsigned)(blocks * parts), kThreads, 0, stream>>>(
       static_cast<const unsigned char*>(data), bytes, first_block, block_bytes, array_id, parts,
-      out);
+      out, err);
   return cudaGetLastError();
 }
 

@@ -27,6 +27,7 @@
 
 #include <mutex>
 
+#include "bounds.cuh"
 #include "zs_internal.h"
 
 namespace zs {
@@ -44,6 +45,8 @@ struct NormArgs {
   double* partials;        // [kNormPartials]
   unsigned int* ticket;    // zero on entry; the last block resets it
   double* out;
+  int64_t win_lo, win_hi;  // checked build: the elements any read may touch
+  unsigned int* err;       // checked build: the device error word
 };
 
 __device__ __forceinline__ void ld32_nc(const void* p, uint32_t* r) {
@@ -68,6 +71,7 @@ __device__ __forceinline__ void acc_square(float g, float& s, float& c) {
 
 template <bool BF16G, int MAXN>
 __device__ __forceinline__ float mean_grad(const NormArgs<MAXN>& a, int64_t i) {
+  if (!within(i, i + 1, a.win_lo, a.win_hi, a.err)) return 0.0f;
   float acc = 0.0f;
   for (int j = 0; j < a.world; ++j) {
     const float x = BF16G ? __uint_as_float(
@@ -110,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, 2) grad_sqnorm_kernel(const __grid_c
     constexpr int KB = 64 / W;                        // slices loaded back to back
     constexpr int kStride = BF16G ? 2 * kGW : 4 * kGW;
     for (int64_t g = g0 + tid; g < g1; g += stride) {
+      if (!within(kGW * g, kGW * g + kGW, a.win_lo, a.win_hi, a.err)) continue;
       float acc[kGW];
 #pragma unroll
       for (int k = 0; k < kGW; ++k) acc[k] = 0.0f;
@@ -154,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 2) grad_sqnorm_kernel(const __grid_c
   if (threadIdx.x == 0) {
     double b = 0.0;
     for (int w = 0; w < kThreads / 32; ++w) b += warp_sums[w];
-    a.partials[blockIdx.x] = b;
+    if (within(blockIdx.x, blockIdx.x + 1, 0, kNormPartials, a.err)) a.partials[blockIdx.x] = b;
     __threadfence();
     last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
   }
@@ -195,6 +200,10 @@ cudaError_t launch_norm(const NormLaunch& in, cudaStream_t stream) {
   a.partials = in.partials;
   a.ticket = in.ticket;
   a.out = in.out;
+  a.win_lo = in.win.lo;
+  a.win_hi = in.win.hi;
+  a.err = ZS_BOUNDS_CHECK ? device_error_word() : nullptr;
+  if (ZS_BOUNDS_CHECK && !a.err) return cudaErrorInvalidSymbol;
   cudaError_t e = cudaMemsetAsync(in.ticket, 0, sizeof(unsigned int), stream);
   if (e != cudaSuccess) return e;
   grad_sqnorm_kernel<BF16G, VEC, MAXN><<<kNormPartials, kThreads, 0, stream>>>(a);

@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "bounds.cuh"
 #include "zs_internal.h"
 
 namespace zs {
@@ -23,7 +24,16 @@ struct GatherArgs {
   int32_t slot[ZS_MAX_WORLD];
   unsigned char* dst;
   int64_t slot_bytes;
+  int32_t world;       // checked build: dst holds world slots
+  unsigned int* err;   // checked build: the device error word
 };
+
+// Checked build: a unit of `u` bytes at byte `off` of a slot lies inside the
+// slot, and the slot inside the world's buffer.
+__device__ __forceinline__ bool unit_ok(const GatherArgs& a, int64_t off, int64_t u) {
+  return within(off, off + u, 0, a.slot_bytes, a.err) &&
+         within(a.slot[blockIdx.y], a.slot[blockIdx.y] + 1, 0, a.world, a.err);
+}
 
 __device__ __forceinline__ uint4 ld_once(const void* p) {
   uint4 r;
@@ -45,12 +55,12 @@ __global__ void __launch_bounds__(kThreads) gather16_kernel(const __grid_constan
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t i = base + (int64_t)u * kThreads;
-      if (i < n) r[u] = ld_once(src + i);
+      if (i < n && unit_ok(a, 16 * i, 16)) r[u] = ld_once(src + i);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t i = base + (int64_t)u * kThreads;
-      if (i < n) dst[i] = r[u];
+      if (i < n && unit_ok(a, 16 * i, 16)) dst[i] = r[u];
     }
   }
 }
@@ -78,12 +88,12 @@ __global__ void __launch_bounds__(kThreads) gather32_kernel(const __grid_constan
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t i = base + (int64_t)u * kThreads;
-      if (i < n) ld32_once(src + 32 * i, r[u]);
+      if (i < n && unit_ok(a, 32 * i, 32)) ld32_once(src + 32 * i, r[u]);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t i = base + (int64_t)u * kThreads;
-      if (i < n) st32(dst + 32 * i, r[u]);
+      if (i < n && unit_ok(a, 32 * i, 32)) st32(dst + 32 * i, r[u]);
     }
   }
 }
@@ -94,7 +104,7 @@ __global__ void __launch_bounds__(kThreads) gather1_kernel(const __grid_constant
   unsigned char* dst = a.dst + (int64_t)a.slot[blockIdx.y] * a.slot_bytes;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < a.slot_bytes; i += stride)
-    dst[i] = src[i];
+    if (unit_ok(a, i, 1)) dst[i] = src[i];
 }
 
 }  // namespace
@@ -111,6 +121,9 @@ cudaError_t launch_gather(const GatherLaunch& in, cudaStream_t stream) {
   if (active == 0) return cudaSuccess;
   a.dst = in.dst;
   a.slot_bytes = in.slot_bytes;
+  a.world = in.world;
+  a.err = ZS_BOUNDS_CHECK ? device_error_word() : nullptr;
+  if (ZS_BOUNDS_CHECK && !a.err) return cudaErrorInvalidSymbol;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

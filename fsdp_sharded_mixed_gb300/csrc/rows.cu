@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "bounds.cuh"
 #include "zs_internal.h"
 
 namespace zs {
@@ -38,6 +39,7 @@ struct SegArgs {
   RowSegment seg[kMaxSegs];
   int64_t first[kMaxSegs + 1];
   int count;
+  unsigned int* err;  // checked build: the device error word
 };
 
 __device__ __forceinline__ uint4 ld_once(const void* p) {
@@ -140,15 +142,18 @@ __global__ void __launch_bounds__(kThreads) segment_copy_kernel(const __grid_con
       if (a.first[mid] <= c) lo = mid;
       else hi = mid - 1;
     }
+    if (!within(lo, lo + 1, 0, a.count, a.err)) continue;
     const RowSegment& s = a.seg[lo];
     const int64_t b0 = (c - a.first[lo]) * kChunk;
     const int64_t len = s.copy_bytes + s.zero_bytes;
     const int64_t b1 = b0 + kChunk < len ? b0 + kChunk : len;
+    // Checked build: the chunk lies inside its segment's byte run.
+    if (!within(b0, b1, 0, len, a.err)) continue;
     // Copy part [b0, min(b1, copy_bytes)); chunk edges are multiples of kChunk,
     // so the widest unit dividing the segment's base addresses and copy length
     // also divides every chunk edge inside it.
     const int64_t c1 = b1 < s.copy_bytes ? b1 : s.copy_bytes;
-    if (b0 < c1) {
+    if (b0 < c1 && within(b0, c1, 0, s.copy_bytes, a.err)) {
       const int64_t e = c1 == s.copy_bytes ? s.copy_bytes : kChunk;
       switch (unit_of((uintptr_t)s.src | (uintptr_t)s.dst | (uintptr_t)e)) {
         case 32: copy_range32(s.src, s.dst, b0, c1); break;
@@ -165,7 +170,7 @@ __global__ void __launch_bounds__(kThreads) segment_copy_kernel(const __grid_con
     }
     // Zero part [max(b0, copy_bytes), b1).
     const int64_t z0 = b0 > s.copy_bytes ? b0 : s.copy_bytes;
-    if (z0 < b1) {
+    if (z0 < b1 && within(z0, b1, s.copy_bytes, len, a.err)) {
       // From the first 16-byte boundary at or after z0 to the last one at or
       // before b1: whole 16-byte stores; the bytes around them one by one.
       const int64_t a0 = (int64_t)((((uintptr_t)(s.dst + z0) + 15u) & ~(uintptr_t)15u) -
@@ -192,6 +197,8 @@ cudaError_t launch_segment_copy(const RowSegment* segs, int n, cudaStream_t stre
   if (e != cudaSuccess) return e;
   for (int first = 0; first < n; first += kMaxSegs) {
     SegArgs a;
+    a.err = ZS_BOUNDS_CHECK ? device_error_word() : nullptr;
+    if (ZS_BOUNDS_CHECK && !a.err) return cudaErrorInvalidSymbol;
     a.count = n - first < kMaxSegs ? n - first : kMaxSegs;
     a.first[0] = 0;
     for (int k = 0; k < a.count; ++k) {

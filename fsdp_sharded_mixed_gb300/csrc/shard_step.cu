@@ -35,9 +35,11 @@
 
 namespace zs {
 
-// Set by bounds-checked builds (bit 0) and by bounded waits that gave up
-// (bit 1); read and cleared by zs_check_device_error.
+// Bit value 1: a check of the bounds-checked build failed; 2: a bounded wait
+// gave up. Read and cleared by zs_check_device_error.
 __device__ unsigned int g_error_word;
+
+int bounds_checked() { return ZS_BOUNDS_CHECK; }
 
 cudaError_t launch_shard_step(const ShardStepLaunch& a, cudaStream_t stream) {
   return launch_step_kernel<false>(a, stream);

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "bounds.cuh"
 #include "zs_internal.h"
 
 namespace zs {
@@ -31,6 +32,8 @@ struct StepArgs {
   const float* accum;   // ACC: fp32 sum of the earlier micro-steps' mean gradients
   float invG;           // ACC: fp32(1/G), G micro-steps per optimizer step
   StepScalars s;
+  int64_t win_lo, win_hi;  // checked build: the elements any access may touch
+  unsigned int* err;       // checked build: the device error word
 };
 
 // ---- global loads and stores -----------------------------------------------
@@ -256,6 +259,7 @@ __device__ __forceinline__ float step_grad(float acc, float prev, float invN, fl
 template <int GW, bool BF16G, int PD, int MAXN, bool ACC>
 __device__ __forceinline__ void process_group(const StepArgs<MAXN>& a, int64_t g, bool clip,
                                               float coef) {
+  if (!within(GW * g, GW * g + GW, a.win_lo, a.win_hi, a.err)) return;
   float p[GW], m[GW], v[GW], acc[GW], prev[ACC ? GW : 1];
   load_state<GW>(a.master + GW * g, p);
   load_state<GW>(a.m + GW * g, m);
@@ -276,6 +280,7 @@ __device__ __forceinline__ void process_group(const StepArgs<MAXN>& a, int64_t g
 template <bool BF16G, int PD, int MAXN, bool ACC>
 __device__ __forceinline__ void process_element(const StepArgs<MAXN>& a, int64_t i, bool clip,
                                                 float coef) {
+  if (!within(i, i + 1, a.win_lo, a.win_hi, a.err)) return;
   float acc = 0.0f;
   for (int j = 0; j < a.world; ++j) {
     const float x = BF16G ? __uint_as_float(
@@ -447,6 +452,10 @@ __global__ void __launch_bounds__(kStagedThreads, 2)
       const uint32_t use = (uint32_t)(i / NS);
       if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, sa.err)) break;
       unsigned char* st = smem + (size_t)s * sa.stage_bytes;
+      if (!within(t * kTile, (t + 1) * kTile, a.win_lo, a.win_hi, sa.err)) {
+        mbar_expect_tx(&full[s], 0);  // checked build: the stage completes empty
+        continue;
+      }
       mbar_expect_tx(&full[s], sa.stage_bytes);
       for (int j = 0; j < n; ++j)
         bulk_to_smem(st + j * gtile, static_cast<const unsigned char*>(a.grads[j]) + t * gtile,
@@ -477,6 +486,11 @@ __global__ void __launch_bounds__(kStagedThreads, 2)
     const int s = (int)(i % NS);
     const uint32_t use = (uint32_t)(i / NS);
     if (!mbar_wait(&full[s], use & 1u, sa.err)) return;
+    if (!within(t * kTile, (t + 1) * kTile, a.win_lo, a.win_hi, sa.err)) {
+      __syncwarp();  // checked build: an empty stage, released untouched
+      if (lane == 0) mbar_arrive(&empty[s]);
+      continue;
+    }
     const unsigned char* st = smem + (size_t)s * sa.stage_bytes;
     float acc[kStagedE];
 #pragma unroll
@@ -578,6 +592,8 @@ cudaError_t launch_staged(const ShardStepLaunch& in, uint32_t stage_bytes, int s
   sa.a.accum = in.accum;
   sa.a.invG = in.invG;
   sa.a.s = in.s;
+  sa.a.win_lo = in.win.lo;
+  sa.a.win_hi = in.win.hi;
   sa.t0 = (in.lo + kTile - 1) / kTile;
   sa.t1 = in.hi / kTile;
   sa.rag_lo[0] = in.lo;
@@ -588,6 +604,7 @@ cudaError_t launch_staged(const ShardStepLaunch& in, uint32_t stage_bytes, int s
   sa.stage_bytes = stage_bytes;
   sa.err = device_error_word();
   if (!sa.err) return cudaErrorInvalidSymbol;
+  sa.a.err = sa.err;
   int64_t blocks = sa.t1 - sa.t0;
   if (blocks > (int64_t)sms * blocks_per_sm) blocks = (int64_t)sms * blocks_per_sm;
   kernel<<<(unsigned)blocks, kStagedThreads, smem, stream>>>(sa);
@@ -627,6 +644,10 @@ cudaError_t launch_one(const ShardStepLaunch& in, cudaStream_t stream) {
   a.accum = in.accum;
   a.invG = in.invG;
   a.s = in.s;
+  a.win_lo = in.win.lo;
+  a.win_hi = in.win.hi;
+  a.err = ZS_BOUNDS_CHECK ? device_error_word() : nullptr;
+  if (ZS_BOUNDS_CHECK && !a.err) return cudaErrorInvalidSymbol;
   const int64_t units = GW > 0 ? (in.hi - in.lo) / GW + 2 : (in.hi - in.lo);
   int64_t blocks = (units + kThreads - 1) / kThreads;
   if (blocks > max_blocks) blocks = max_blocks;

@@ -45,6 +45,19 @@ struct StepScalars {
   float b1, b2, omb1, omb2, bc1, bc2, lr, eps, decay, invN;
 };
 
+// The index window a kernel's accesses are checked against in the bounds-
+// checked build (the CUDA sources compiled with ZS_BOUNDS_CHECK=1, see
+// bounds.cuh): [lo, hi) in elements of the shard. Every build carries it in
+// the launch structures; only the checked build's kernels read it.
+struct Window {
+  int64_t lo, hi;
+};
+// The step-family window for the range [lo, hi): the range itself, narrowed
+// at both ends by the self-test shrink (zs_selftest_bounds_window).
+Window step_window(int64_t lo, int64_t hi);
+// 1 in the bounds-checked build, 0 otherwise (defined by the CUDA sources).
+int bounds_checked();
+
 // Kernel launchers (shard_step.cu, gather.cu). They assume validated input.
 struct ShardStepLaunch {
   const void* const* grads;  // host array of N device pointers
@@ -62,6 +75,7 @@ struct ShardStepLaunch {
   const float* accum;   // fp32 [S] micro-step accumulator (accumulation kernels), or NULL
   float invG;           // fp32(1/G) for the accumulated step
   StepScalars s;
+  Window win;           // checked build: every element the kernels touch lies in it
 };
 cudaError_t launch_shard_step(const ShardStepLaunch& a, cudaStream_t stream);
 // Gradient accumulation (accum.cu): accum = (first ? 0 : accum) + mean, and the
@@ -92,6 +106,7 @@ struct NormLaunch {
   double* partials;     // [kNormPartials]
   unsigned int* ticket;
   double* out;
+  Window win;           // checked build: every element the pass reads lies in it
 };
 cudaError_t launch_grad_sqnorm(const NormLaunch& a, cudaStream_t stream);
 // The same norm pass with its scratch in a file-scope device array of
@@ -141,7 +156,8 @@ unsigned int* device_error_word();
 // One block waiting, bounded by `polls`, on an mbarrier nothing arrives on.
 cudaError_t launch_wait_timeout(uint32_t polls, cudaStream_t stream);
 
-// Device error word (set by bounds-checked builds and bounded waits).
+// Device error word: bit value 1 set by the bounds-checked build's checks,
+// 2 by bounded waits that gave up.
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* word);
 
 int elem_bytes(zs_dtype dt);

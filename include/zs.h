@@ -421,9 +421,27 @@ zs_status zs_trace_first_divergence(const char* const* paths, int32_t n_paths, i
 const char* zs_status_string(zs_status status);
 const char* zs_last_error(void);
 /* Synchronises `cuda_stream`, then reads and clears this device's error word
- * (set by bounds-checked builds and bounded waits); ZS_ERR_TIMEOUT or
- * ZS_ERR_RANGE if it was set, ZS_ERR_CUDA if the stream reports an error. */
+ * (set by the bounds-checked build's checks and by bounded waits);
+ * ZS_ERR_TIMEOUT or ZS_ERR_RANGE if it was set, ZS_ERR_CUDA if the stream
+ * reports an error. */
 zs_status zs_check_device_error(void* cuda_stream);
+/* The bounds-checked build. The library also exists as libzs_checked.so: the
+ * same host code, and kernels that check, before each global access or bulk
+ * copy, that what it touches lies in the window its launch declares (the
+ * shard range [lo, hi) for the step, accumulation and norm kernels; the slot
+ * and the world's buffer for the gather; the segment for the row copies; the
+ * block for the checksums). A range outside its window is not accessed and
+ * sets the error word's bounds bit (ZS_ERR_RANGE from zs_check_device_error);
+ * no trap, the context stays usable. For tests of the kernels' index
+ * arithmetic, not for timing. Returns 1 in that build, else 0. The pages have
+ * no counterpart (their tooling stops at profilers). */
+int32_t zs_bounds_checked(void);
+/* Checked build only: narrows the window of the step, accumulation and norm
+ * kernels to [lo + shrink, hi - shrink) (0 = the range itself), so that a
+ * test sees the checks fire on accesses that are in fact in bounds. Process-
+ * wide. ZS_ERR_UNSUPPORTED in the ordinary build, ZS_ERR_RANGE for shrink
+ * outside 0..2^40. */
+zs_status zs_selftest_bounds_window(int64_t shrink);
 /* The step's kernel. Two kernels compute the same step with the same fp32
  * operations in the same order (results are identical): the register-
  * streaming kernel (each thread loads its 16-element group of every slice and

@@ -31,8 +31,19 @@ def pytest_sessionstart(session):
         import fsdp_sharded_mixed_gb300 as zs
     except ImportError:
         return
-    if not os.path.exists(zs.LIB_PATH):
+    if not (os.path.exists(zs.LIB_PATH) and os.path.exists(zs.CHECKED_LIB_PATH)):
         zs.build()
+
+
+@pytest.fixture(autouse=True)
+def _bounds_word_clear(request):
+    """Under the bounds-checked library (ZS_BOUNDS_CHECK=1), every GPU test
+    ends with the device error word clear: no kernel access fell outside its
+    launch's window (tests that set the word on purpose read and clear it)."""
+    yield
+    if os.environ.get("ZS_BOUNDS_CHECK") == "1" and request.node.get_closest_marker("gpu"):
+        import fsdp_sharded_mixed_gb300 as zs
+        zs.zs_check_device_error()
 
 
 @pytest.fixture(scope="session")

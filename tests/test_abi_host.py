@@ -165,3 +165,22 @@ def test_selftest_and_step_path_arguments():
     with pytest.raises(ValueError):
         zs.zs_set_step_path(5)
     assert L.zs_set_step_path(-1) == -1
+
+
+def test_checked_library_exports_and_flags():
+    """Both builds export the same symbols; only libzs_checked.so says it is
+    the bounds-checked build and accepts the window self-test (host-side
+    calls, no kernel)."""
+    import ctypes
+    names = declared_functions()
+    checked = ctypes.CDLL(zs.CHECKED_LIB_PATH)
+    for name in names:
+        assert hasattr(checked, name), f"{name} missing from libzs_checked.so"
+    checked.zs_bounds_checked.restype = ctypes.c_int32
+    checked.zs_selftest_bounds_window.argtypes = [ctypes.c_int64]
+    assert checked.zs_bounds_checked() == 1
+    assert checked.zs_selftest_bounds_window(-1) == zs.ZS_ERR_RANGE
+    assert checked.zs_selftest_bounds_window(0) == zs.ZS_OK
+    L = zs.lib()
+    assert zs.lib_path() == zs.LIB_PATH and not zs.zs_bounds_checked()
+    assert L.zs_selftest_bounds_window(3) == zs.ZS_ERR_UNSUPPORTED
