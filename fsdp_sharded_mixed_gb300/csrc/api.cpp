@@ -759,6 +759,7 @@ extern "C" zs_status zs_shard_step(const zs_plan* plan, int32_t rank, int64_t lo
                                    void* full_flat, zs_dtype param_dtype,
                                    const zs_adamw_hparams* hp, int64_t step,
                                    void* cuda_stream) {
+  const zs::CallRange range("zs_shard_step");
   return zs::traced(zs_shard_step_untraced(plan, rank, lo, hi, grad_slices, grad_dtype, master,
                                            exp_avg, exp_avg_sq, full_flat, param_dtype, hp,
                                            step, cuda_stream),
@@ -771,6 +772,7 @@ extern "C" zs_status zs_shard_step_to_shard(const zs_plan* plan, int32_t rank, i
                                             float* exp_avg_sq, void* param_shard,
                                             zs_dtype param_dtype, const zs_adamw_hparams* hp,
                                             int64_t step, void* cuda_stream) {
+  const zs::CallRange range("zs_shard_step_to_shard");
   return zs::traced(zs_shard_step_to_shard_untraced(plan, rank, lo, hi, grad_slices, grad_dtype,
                                                     master, exp_avg, exp_avg_sq, param_shard,
                                                     param_dtype, hp, step, cuda_stream),
@@ -784,6 +786,7 @@ extern "C" zs_status zs_shard_step_clipped(const zs_plan* plan, int32_t rank, in
                                            zs_dtype param_dtype, const zs_adamw_hparams* hp,
                                            int64_t step, const float* coef,
                                            const int32_t* skip, void* cuda_stream) {
+  const zs::CallRange range("zs_shard_step_clipped");
   return zs::traced(zs_shard_step_clipped_untraced(plan, rank, lo, hi, grad_slices, grad_dtype,
                                                    master, exp_avg, exp_avg_sq, full_flat,
                                                    param_dtype, hp, step, coef, skip,
@@ -799,6 +802,7 @@ extern "C" zs_status zs_shard_step_accumulated(const zs_plan* plan, int32_t rank
                                                void* full_flat, zs_dtype param_dtype,
                                                const zs_adamw_hparams* hp, int64_t step,
                                                void* cuda_stream) {
+  const zs::CallRange range("zs_shard_step_accumulated");
   return zs::traced(zs_shard_step_accumulated_untraced(plan, rank, lo, hi, grad_slices,
                                                        grad_dtype, accum, micro_steps, master,
                                                        exp_avg, exp_avg_sq, full_flat,
@@ -811,6 +815,7 @@ extern "C" zs_status zs_grad_accumulate(const zs_plan* plan, int32_t rank, int64
                                         int64_t hi, const void* const* grad_slices,
                                         zs_dtype grad_dtype, float* accum, int32_t first,
                                         void* cuda_stream) {
+  const zs::CallRange range("zs_grad_accumulate");
   return zs::traced(zs_grad_accumulate_untraced(plan, rank, lo, hi, grad_slices, grad_dtype,
                                                 accum, first, cuda_stream),
                     "zs_grad_accumulate", plan, rank, lo, hi, grad_dtype, -1, 0);
@@ -820,6 +825,7 @@ extern "C" zs_status zs_grad_sqnorm(const zs_plan* plan, int32_t rank, int64_t l
                                     const void* const* grad_slices, zs_dtype grad_dtype,
                                     void* workspace, int64_t workspace_bytes,
                                     double* sqnorm_out, void* cuda_stream) {
+  const zs::CallRange range("zs_grad_sqnorm");
   return zs::traced(zs_grad_sqnorm_untraced(plan, rank, lo, hi, grad_slices, grad_dtype,
                                             workspace, workspace_bytes, sqnorm_out,
                                             cuda_stream),
@@ -830,6 +836,7 @@ extern "C" zs_status zs_grad_sqnorm_noalloc(const zs_plan* plan, int32_t rank, i
                                             int64_t hi, const void* const* grad_slices,
                                             zs_dtype grad_dtype, double* sqnorm_out,
                                             void* cuda_stream) {
+  const zs::CallRange range("zs_grad_sqnorm_noalloc");
   return zs::traced(zs_grad_sqnorm_noalloc_untraced(plan, rank, lo, hi, grad_slices, grad_dtype,
                                                     sqnorm_out, cuda_stream),
                     "zs_grad_sqnorm_noalloc", plan, rank, lo, hi, grad_dtype, -1, 0);
@@ -838,6 +845,7 @@ extern "C" zs_status zs_grad_sqnorm_noalloc(const zs_plan* plan, int32_t rank, i
 extern "C" zs_status zs_clip_coefficient(const double* rank_sqnorms, int32_t n, double max_norm,
                                          float* coef_out, int32_t* nonfinite_out,
                                          void* cuda_stream) {
+  const zs::CallRange range("zs_clip_coefficient");
   return zs::traced(zs_clip_coefficient_untraced(rank_sqnorms, n, max_norm, coef_out,
                                                  nonfinite_out, cuda_stream),
                     "zs_clip_coefficient", nullptr, -1, 0, 0, -1, -1, 0, n);
@@ -847,6 +855,7 @@ extern "C" zs_status zs_gather_assemble(const zs_plan* plan, int32_t rank,
                                         const void* const* shard_srcs, void* full_flat,
                                         zs_dtype param_dtype, void** views_out,
                                         void* cuda_stream) {
+  const zs::CallRange range("zs_gather_assemble");
   return zs::traced(zs_gather_assemble_untraced(plan, rank, shard_srcs, full_flat, param_dtype,
                                                 views_out, cuda_stream),
                     "zs_gather_assemble", plan, rank, 0, 0, -1, param_dtype, 0);
@@ -854,12 +863,14 @@ extern "C" zs_status zs_gather_assemble(const zs_plan* plan, int32_t rank,
 
 extern "C" zs_status zs_unshard(const zs_plan* plan, const void* gathered, zs_dtype dtype,
                                 void* const* params_out, void* cuda_stream) {
+  const zs::CallRange range("zs_unshard");
   return zs::traced(zs_unshard_untraced(plan, gathered, dtype, params_out, cuda_stream),
                     "zs_unshard", plan, -1, 0, 0, -1, dtype, 0);
 }
 
 extern "C" zs_status zs_shard_rows(const zs_plan* plan, int32_t rank, const void* const* params_in,
                                    zs_dtype dtype, void* local_out, void* cuda_stream) {
+  const zs::CallRange range("zs_shard_rows");
   return zs::traced(zs_shard_rows_untraced(plan, rank, params_in, dtype, local_out, cuda_stream),
                     "zs_shard_rows", plan, rank, 0, 0, -1, dtype, 0);
 }

@@ -1021,6 +1021,7 @@ static zs_status zs_checkpoint_load_untraced(const zs_plan* plan, int32_t rank,
 extern "C" zs_status zs_checkpoint_save(const zs_plan* plan, int32_t rank, const float* master,
                                         const float* exp_avg, const float* exp_avg_sq,
                                         int64_t step, const char* path, void* cuda_stream) {
+  const zs::CallRange range("zs_checkpoint_save");
   return zs::traced(zs_checkpoint_save_untraced(plan, rank, master, exp_avg, exp_avg_sq, step,
                                                 path, cuda_stream),
                     "zs_checkpoint_save", plan, rank, 0, 0, -1, -1, step);
@@ -1030,6 +1031,7 @@ extern "C" zs_status zs_checkpoint_load(const zs_plan* plan, int32_t rank,
                                         const char* const* paths, int32_t n_paths, float* master,
                                         float* exp_avg, float* exp_avg_sq, int64_t* step,
                                         void* cuda_stream) {
+  const zs::CallRange range("zs_checkpoint_load");
   int64_t saved = -1;
   const zs_status st = zs_checkpoint_load_untraced(plan, rank, paths, n_paths, master, exp_avg,
                                                    exp_avg_sq, &saved, cuda_stream);

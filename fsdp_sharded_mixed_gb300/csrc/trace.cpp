@@ -1,4 +1,5 @@
-// trace.cpp — the per-call trace, and finding where ranks' traces diverge.
+// trace.cpp — the per-call trace, finding where ranks' traces diverge, and the
+// NVTX range around each traced call.
 //
 // "从 Data Parallel 到 ZeRO/FSDP", "训练 Hang 应按 Collective 顺序排查": ZeRO/FSDP
 // insert collectives from hooks, so ranks that enter modules in a different
@@ -30,6 +31,8 @@
 #include <mutex>
 #include <string>
 #include <vector>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "zs_internal.h"
 
@@ -148,6 +151,9 @@ std::string signature(const Record& r) {
 }  // namespace
 
 namespace zs {
+
+CallRange::CallRange(const char* name) { nvtxRangePushA(name); }
+CallRange::~CallRange() { nvtxRangePop(); }
 
 zs_status traced(zs_status st, const char* call, const zs_plan* plan, int32_t rank, int64_t lo,
                  int64_t hi, int grad_dtype, int param_dtype, int64_t step, int32_t world) {

@@ -148,6 +148,17 @@ zs_status check_device_array(const void* p, int64_t bytes, const char* fn, const
 zs_status traced(zs_status st, const char* call, const zs_plan* plan, int32_t rank, int64_t lo,
                  int64_t hi, int grad_dtype, int param_dtype, int64_t step, int32_t world = 0);
 
+// An NVTX range named after a library call, open for the object's lifetime,
+// so that profilers attribute the call's host time and launches to it. NVTX
+// costs a pointer test per call when no tool is attached.
+class CallRange {
+ public:
+  explicit CallRange(const char* name);
+  ~CallRange();
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
+
 // Which kernel runs the step: 0 = chosen per call, 1 = the register-streaming
 // kernel, 2 = the staged kernel wherever it is eligible (zs_set_step_path).
 int step_path();
