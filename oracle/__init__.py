@@ -88,6 +88,12 @@ def load(path=LIB_PATH):
     L.oracle_shard_step_accumulated.argtypes = [_I32, _I32, _I64, _I64, _I64, _P, _I32, _P, _I32,
                                                 _P, _P, _P, _P, _I32, _D, _D, _D, _D, _D, _I64]
     L.oracle_shard_step_accumulated.restype = ctypes.c_int
+    L.oracle_grad_sqnorm_accumulated.argtypes = [_I32, _I64, _I64, _I64, _P, _I32, _P, _I32]
+    L.oracle_grad_sqnorm_accumulated.restype = _D
+    L.oracle_shard_step_accumulated_clipped.argtypes = [_I32, _I32, _I64, _I64, _I64, _P, _I32,
+                                                        _P, _I32, _P, _P, _P, _P, _I32, _D, _D,
+                                                        _D, _D, _D, _I64, _F, _I32]
+    L.oracle_shard_step_accumulated_clipped.restype = ctypes.c_int
     L.oracle_rows_plan.argtypes = [_P, _P, _P, _I32, _I32, _I64, _P, _P, _P, _P]
     L.oracle_rows_plan.restype = ctypes.c_int
     L.oracle_unshard.argtypes = [_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _P, _P]
@@ -230,6 +236,25 @@ class Oracle:
                                                   param_dtype, lr, beta1, beta2, eps, wd, t)
         if rc != 0:
             raise ValueError("oracle_shard_step_accumulated rejected the input")
+
+    # -- clipping an accumulated gradient ---------------------------------
+    def grad_sqnorm_accumulated(self, *, world, S, lo, hi, grads, accum, micro_steps):
+        gdt = BF16 if grads[0].dtype == np.uint16 else FP32
+        assert accum.dtype == np.float32 and accum.size >= S
+        return self.L.oracle_grad_sqnorm_accumulated(world, S, lo, hi, self._ptrs(grads), gdt,
+                                                     accum.ctypes.data, micro_steps)
+
+    def shard_step_accumulated_clipped(self, *, world, rank, S, lo, hi, grads, accum,
+                                       micro_steps, master, m, v, full_flat, coef, skip,
+                                       param_dtype=BF16, lr=1e-3, beta1=0.9, beta2=0.999,
+                                       eps=1e-8, wd=0.01, t=1):
+        gdt = BF16 if grads[0].dtype == np.uint16 else FP32
+        rc = self.L.oracle_shard_step_accumulated_clipped(
+            world, rank, S, lo, hi, self._ptrs(grads), gdt, accum.ctypes.data, micro_steps,
+            master.ctypes.data, m.ctypes.data, v.ctypes.data, full_flat.ctypes.data, param_dtype,
+            lr, beta1, beta2, eps, wd, t, float(coef), int(skip))
+        if rc != 0:
+            raise ValueError("oracle_shard_step_accumulated_clipped rejected the input")
 
     # -- per-parameter row sharding (FSDP2) ------------------------------
     def rows_plan(self, dim0, numels, tied_to=None, world=1, align=128):

@@ -473,6 +473,63 @@ int oracle_shard_step_accumulated(int32_t world, int32_t rank, int64_t S, int64_
 }
 
 /* ---------------------------------------------------------------------------
+ * Clipping an accumulated gradient. The same section of [DP-to-ZeRO] asks both
+ * questions at once: a job that accumulates G micro-batches and clips must
+ * clip the gradient the update sees. Readings: that gradient is the micro-batch
+ * average g = (a_{G-1} + mean_G) * fp32(1/G) of oracle_shard_step_accumulated;
+ * its global norm is the sum over all shards of g^2 (each rank's part over its
+ * shard, added in rank order by oracle_clip_coef, as for the plain step); the
+ * update then sees g * coef, and a non-finite norm skips it on every rank.
+ * ------------------------------------------------------------------------- */
+
+/* Sum over i in [lo, hi), ascending, of g_i^2 in double, g_i the accumulated
+ * step's fp32 gradient (the square of an fp32 value is exact in double). */
+double oracle_grad_sqnorm_accumulated(int32_t world, int64_t S, int64_t lo, int64_t hi,
+                                      const void* const* grads, int32_t grad_dtype,
+                                      const float* accum, int32_t micro_steps) {
+  if (world < 1 || lo < 0 || hi < lo || hi > S || micro_steps < 1) return -1.0;
+  float invN = (float)(1.0 / (double)world);
+  float invG = (float)(1.0 / (double)micro_steps);
+  double sum = 0.0;
+  for (int64_t i = lo; i < hi; ++i) {
+    float acc = 0.0f;
+    for (int32_t j = 0; j < world; ++j) acc = acc + load_grad(grads[j], grad_dtype, i);
+    float mean = acc * invN;
+    float g = (accum[i] + mean) * invG;
+    sum = sum + (double)g * (double)g;
+  }
+  return sum;
+}
+
+/* The accumulated step with the clip coefficient and the shared skip. */
+int oracle_shard_step_accumulated_clipped(int32_t world, int32_t rank, int64_t S, int64_t lo,
+                                          int64_t hi, const void* const* grads,
+                                          int32_t grad_dtype, const float* accum,
+                                          int32_t micro_steps, float* master, float* m,
+                                          float* v, void* full_flat, int32_t param_dtype,
+                                          double lr, double beta1, double beta2, double eps,
+                                          double wd, int64_t t, float coef, int32_t skip) {
+  if (world < 1 || rank < 0 || rank >= world || lo < 0 || hi < lo || hi > S || t < 1 ||
+      micro_steps < 1)
+    return -1;
+  if (!elem_bytes(param_dtype) || (grad_dtype != DT_BF16 && grad_dtype != DT_FP32))
+    return -1;
+  if (skip) return 0;
+  Scalars s = make_scalars(lr, beta1, beta2, eps, wd, t, world);
+  float invG = (float)(1.0 / (double)micro_steps);
+  int64_t slot = (int64_t)rank * S;
+  for (int64_t i = lo; i < hi; ++i) {
+    float acc = 0.0f;
+    for (int32_t j = 0; j < world; ++j) acc = acc + load_grad(grads[j], grad_dtype, i);
+    float mean = acc * s.invN;
+    float g = ((accum[i] + mean) * invG) * coef;
+    adamw_element(s, g, master[i], m[i], v[i]);
+    store_param(full_flat, param_dtype, slot + i, master[i]);
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------
  * Per-parameter row sharding (FSDP2) and the gather side of a wrap unit.
  * [DP-to-ZeRO] "ZeRO 与 FSDP 的关系": FSDP2 keeps per-parameter sharded state;
  * [Lifecycle] "The parameter lifecycle, one module at a time": AllGather the

@@ -922,6 +922,149 @@ def pin_accum_ddp_equivalence(o, w=TINY, G=3, steps=2):
                                       full_st[i].view(np.uint32)), f"state {i} differs at t={t}"
 
 
+# ------------------------------------------ clipping an accumulated step ----
+def pin_accum_clip_reductions(o):
+    """Clipping an accumulated gradient reduces to the pieces it is made of:
+    G = 1 with a zero accumulator is the clipped step (norm and update, bit for
+    bit); a coefficient of 1 without skip is the accumulated step; a skip
+    leaves every buffer untouched."""
+    grads, master = _clip_inputs(n=1700, world=4, seed=53)
+    n, world = master.size, len(grads)
+    zero = np.zeros(n, np.float32)
+    assert o.grad_sqnorm_accumulated(world=world, S=n, lo=0, hi=n, grads=grads, accum=zero,
+                                     micro_steps=1) == o.grad_sqnorm(world=world, S=n, lo=0,
+                                                                     hi=n, grads=grads)
+    for coef in (np.float32(0.3125), np.float32(0.7)):
+        a = [master.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32),
+             np.zeros(n * world, np.uint16)]
+        b = [x.copy() for x in a]
+        o.shard_step_accumulated_clipped(world=world, rank=0, S=n, lo=0, hi=n, grads=grads,
+                                         accum=zero, micro_steps=1, master=a[0], m=a[1], v=a[2],
+                                         full_flat=a[3], coef=coef, skip=0, t=2, **HP)
+        o.shard_step_clipped(world=world, rank=0, S=n, lo=0, hi=n, grads=grads, master=b[0],
+                             m=b[1], v=b[2], full_flat=b[3], coef=coef, skip=0, t=2, **HP)
+        for x, y in zip(a, b):
+            assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+    rng = np.random.default_rng(54)
+    acc = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    a = [master.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32),
+         np.zeros(n * world, np.uint16)]
+    b = [x.copy() for x in a]
+    o.shard_step_accumulated_clipped(world=world, rank=1, S=n, lo=5, hi=n - 3, grads=grads,
+                                     accum=acc, micro_steps=3, master=a[0], m=a[1], v=a[2],
+                                     full_flat=a[3], coef=1.0, skip=0, t=4, **HP)
+    o.shard_step_accumulated(world=world, rank=1, S=n, lo=5, hi=n - 3, grads=grads, accum=acc,
+                             micro_steps=3, master=b[0], m=b[1], v=b[2], full_flat=b[3], t=4,
+                             **HP)
+    for x, y in zip(a, b):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+    before = [x.copy() for x in a]
+    o.shard_step_accumulated_clipped(world=world, rank=1, S=n, lo=0, hi=n, grads=grads,
+                                     accum=acc, micro_steps=3, master=a[0], m=a[1], v=a[2],
+                                     full_flat=a[3], coef=0.5, skip=1, t=5, **HP)
+    for x, y in zip(a, before):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+def pin_accum_clip_dyadic(o):
+    """Dyadic slices and accumulator, G and N powers of two: the accumulated
+    norm is the exact rational sum of ((a + mean) / G)^2 over the range, and
+    after clipping the update sees a gradient of norm
+    max_norm * norm / (norm + 1e-6) (observed as m with beta1 = 0)."""
+    rng = np.random.default_rng(55)
+    n = 777
+    for world, G in ((1, 2), (2, 4), (4, 2), (8, 8)):
+        ints = rng.integers(-64, 65, size=(world, n))
+        grads = [to_bf16_exact((ints[j] * 2.0 ** -8).astype(np.float32)) for j in range(world)]
+        a_int = rng.integers(-512, 513, size=n)
+        acc = (a_int * 2.0 ** -10).astype(np.float32)
+        want = [(Fraction(int(a_int[i]), 1024) + Fraction(int(x), 256 * world)) / G
+                for i, x in enumerate(ints.sum(axis=0))]
+        got = o.grad_sqnorm_accumulated(world=world, S=n, lo=0, hi=n, grads=grads, accum=acc,
+                                        micro_steps=G)
+        assert Fraction(got) == sum(q * q for q in want), (world, G)
+        lo, hi = 31, 700
+        part = o.grad_sqnorm_accumulated(world=world, S=n, lo=lo, hi=hi, grads=grads, accum=acc,
+                                         micro_steps=G)
+        assert Fraction(part) == sum(q * q for q in want[lo:hi]), (world, G)
+        norm = float(np.sqrt(got))
+        max_norm = 0.375 * norm
+        coef, bad = o.clip_coef([got], max_norm)
+        assert bad == 0 and coef < 1
+        m = np.zeros(n, np.float32)
+        o.shard_step_accumulated_clipped(world=world, rank=0, S=n, lo=0, hi=n, grads=grads,
+                                         accum=acc, micro_steps=G,
+                                         master=np.zeros(n, np.float32), m=m,
+                                         v=np.zeros(n, np.float32),
+                                         full_flat=np.zeros(n * world, np.uint16), coef=coef,
+                                         skip=0, t=1, lr=0.0, beta1=0.0, beta2=0.999, eps=1e-8,
+                                         wd=0.0)
+        seen = np.sqrt(np.sum(m.astype(np.float64) ** 2))
+        expect = max_norm * norm / (norm + 1e-6)
+        assert abs(seen - expect) <= 4e-7 * expect, (world, G, seen, expect)
+
+
+def pin_accum_clip_ddp_equivalence(o, w=TINY, G=3, steps=2):
+    """G micro-steps and global-norm clipping of their average: the sharded
+    pipeline (N accumulators, each rank's partial norm of its accumulated
+    gradient, the coefficient over the N partials, N clipped accumulated steps,
+    gather) equals the unsharded one over the whole flat buffer, bit for bit,
+    with the same coefficient."""
+    plan = o.plan(w.numels, w.tied_to, world=w.world, align=w.align)
+    P, P_pad, S, N = plan["P"], plan["P_pad"], plan["S"], w.world
+    master0 = synth.fill(P_pad, seed=w.seed, stream=synth.STREAM_MASTER, sigma=w.master_sigma,
+                         p_limit=P)
+    full_st = [master0.copy(), np.zeros(P_pad, np.float32), np.zeros(P_pad, np.float32)]
+    full_acc = np.zeros(P_pad, np.float32)
+    full_params = np.zeros(P_pad * N, np.uint16)
+    sh = [[master0[r * S:(r + 1) * S].copy(), np.zeros(S, np.float32), np.zeros(S, np.float32)]
+          for r in range(N)]
+    sh_acc = [np.zeros(S, np.float32) for _ in range(N)]
+    max_norm = None
+    for t in range(1, steps + 1):
+        for k in range(G):
+            local = [synth.fill(P_pad, seed=w.seed, rank=j, step=2000 * t + k,
+                                sigma=w.grad_sigma, p_limit=P, bf16=True) for j in range(N)]
+            slices = [[local[j][r * S:(r + 1) * S].copy() for j in range(N)] for r in range(N)]
+            if k < G - 1:
+                o.grad_accumulate(world=N, S=P_pad, lo=0, hi=P_pad, grads=local, accum=full_acc,
+                                  first=k == 0)
+                for r in range(N):
+                    o.grad_accumulate(world=N, S=S, lo=0, hi=S, grads=slices[r], accum=sh_acc[r],
+                                      first=k == 0)
+                continue
+            sq_full = o.grad_sqnorm_accumulated(world=N, S=P_pad, lo=0, hi=P_pad, grads=local,
+                                                accum=full_acc, micro_steps=G)
+            if max_norm is None:
+                max_norm = 0.5 * float(np.sqrt(sq_full))
+            c_full, bad_full = o.clip_coef([sq_full], max_norm)
+            o.shard_step_accumulated_clipped(world=N, rank=0, S=P_pad, lo=0, hi=P_pad,
+                                             grads=local, accum=full_acc, micro_steps=G,
+                                             master=full_st[0], m=full_st[1], v=full_st[2],
+                                             full_flat=full_params, coef=c_full, skip=bad_full,
+                                             t=t, **HP)
+            partial = [o.grad_sqnorm_accumulated(world=N, S=S, lo=0, hi=S, grads=slices[r],
+                                                 accum=sh_acc[r], micro_steps=G)
+                       for r in range(N)]
+            c_sh, bad_sh = o.clip_coef(partial, max_norm)
+            assert bad_sh == bad_full == 0 and c_sh == c_full and c_sh < 1, (c_sh, c_full)
+            fulls = []
+            for r in range(N):
+                f = np.zeros(P_pad, np.uint16)
+                o.shard_step_accumulated_clipped(world=N, rank=r, S=S, lo=0, hi=S,
+                                                 grads=slices[r], accum=sh_acc[r],
+                                                 micro_steps=G, master=sh[r][0], m=sh[r][1],
+                                                 v=sh[r][2], full_flat=f, coef=c_sh,
+                                                 skip=bad_sh, t=t, **HP)
+                fulls.append(f[r * S:(r + 1) * S].copy())
+            gathered = np.zeros(P_pad, np.uint16)
+            o.gather(world=N, S=S, elem_size=2, shards=fulls, full_flat=gathered)
+            assert np.array_equal(gathered, full_params[:P_pad]), f"params differ at t={t}"
+            for i in range(3):
+                assert np.array_equal(np.concatenate([x[i] for x in sh]).view(np.uint32),
+                                      full_st[i].view(np.uint32)), f"state {i} differs at t={t}"
+
+
 # ------------------------------------------- per-parameter row sharding ----
 def _rows_case_bits(rng, rp, numels, elem):
     """Random bit patterns for each owner parameter (uint8 views)."""
@@ -1255,7 +1398,8 @@ ALL_PINS = [
     pin_bucket_invariance, pin_sqnorm_dyadic, pin_clip_coef_closed_forms,
     pin_clip_unit_identity, pin_clip_post_norm, pin_clip_skip, pin_clip_ddp_equivalence,
     pin_accum_single_microstep_identity, pin_accum_dyadic, pin_accum_equals_merged,
-    pin_accum_first_overwrites, pin_accum_ddp_equivalence, pin_rows_bruteforce,
+    pin_accum_first_overwrites, pin_accum_ddp_equivalence, pin_accum_clip_reductions,
+    pin_accum_clip_dyadic, pin_accum_clip_ddp_equivalence, pin_rows_bruteforce,
     pin_rows_pages_layernorm, pin_rows_reshard, pin_rows_ddp_equivalence,
     pin_reshard_hand_examples, pin_reshard_invariants, pin_reshard_next_update,
     pin_ddp_equivalence_gpt2_buckets,

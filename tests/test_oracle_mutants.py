@@ -68,6 +68,21 @@ MUTANTS = [
      "float g = accum[i] + mean;"),
     ("accumulator ignored by the step", "float g = (accum[i] + mean) * invG;",
      "float g = mean * invG;"),
+    ("accumulated norm over the last micro-step only",
+     "float g = (accum[i] + mean) * invG;\n    sum = sum + (double)g * (double)g;",
+     "float g = mean * invG;\n    sum = sum + (double)g * (double)g;"),
+    ("accumulated norm not divided by G",
+     "float g = (accum[i] + mean) * invG;\n    sum = sum + (double)g * (double)g;",
+     "float g = accum[i] + mean;\n    sum = sum + (double)g * (double)g;"),
+    ("accumulated clip coefficient ignored", "float g = ((accum[i] + mean) * invG) * coef;",
+     "float g = (accum[i] + mean) * invG;"),
+    ("coefficient applied to the last micro-step only",
+     "float g = ((accum[i] + mean) * invG) * coef;", "float g = (accum[i] + mean * coef) * invG;"),
+    ("accumulated skip ignored",
+     "  if (skip) return 0;\n  Scalars s = make_scalars(lr, beta1, beta2, eps, wd, t, world);\n"
+     "  float invG",
+     "  if (false) return 0;\n  Scalars s = make_scalars(lr, beta1, beta2, eps, wd, t, world);\n"
+     "  float invG"),
     ("row chunks rounded down", "rows_per_rank[i] = (dim0[i] + world - 1) / world;",
      "rows_per_rank[i] = dim0[i] / world + (dim0[i] % world > 1 ? 1 : 0);"),
     ("segment offsets count rows, not elements",
