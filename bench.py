@@ -22,6 +22,8 @@ the same workload, on the host's cores, as the reference arm.
 Other measurements (--pipeline; the default is the step above):
     clip        global-norm pass + clip coefficient + clipped step
     accum       G-1 gradient accumulations + the accumulated step
+    accum_clip  G-1 accumulations + the accumulated gradient's norm + clip
+                coefficient + the clipped accumulated step
     gather      the AllGather's assembly of the other ranks' shards
     unshard     FSDP2 copy-out of every wrap unit's gathered parameters
     checkpoint  save, restore, and restore into world N/2 of one rank's state
@@ -303,8 +305,9 @@ def run_ours(args, w):
     hp = w.hparams
     bpe = bytes_per_elem(N)
     norm_bpe = 2 * N  # the norm pass reads the N bf16 slices once
-    clip = args.pipeline == "clip"
-    accum_mode = args.pipeline == "accum"
+    accum_clip = args.pipeline == "accum_clip"
+    clip = args.pipeline == "clip" or accum_clip
+    accum_mode = args.pipeline == "accum" or accum_clip
     G = max(1, args.micro_steps)
 
     # Inputs resident in HBM: one set of incoming slices, master from the
@@ -382,6 +385,16 @@ def run_ours(args, w):
         zs.zs_shard_step_accumulated(plan, r, 0, S, grads, zs.ZS_BF16, acc_buf, G, master, m, v,
                                      full, zs.ZS_BF16, hp, step_no[0], stream=sp)
 
+    def part_norm_accumulated(sp):
+        zs.zs_grad_sqnorm_accumulated(plan, r, 0, S, grads, zs.ZS_BF16, acc_buf, G, ws,
+                                      parts.narrow(0, r, 1), stream=sp)
+        zs.zs_clip_coefficient(parts, N, max_norm, coef, bad, stream=sp)
+
+    def part_accumulated_clipped(sp):
+        zs.zs_shard_step_accumulated_clipped(plan, r, 0, S, grads, zs.ZS_BF16, acc_buf, G, master,
+                                             m, v, full, zs.ZS_BF16, hp, step_no[0], coef=coef,
+                                             skip=bad, stream=sp)
+
     units = []
     up_dims = {}
     unit_params = []
@@ -431,6 +444,15 @@ def run_ours(args, w):
         launches_per_step = 0
         for up, _, outs in units:   # one launch per 256 (parameter, rank) row segments
             launches_per_step += -(-_segments(up, outs) // 256)
+    elif accum_clip:
+        # micro-steps 1 .. G-1 accumulated; the norm of the accumulated
+        # gradient (slices + accumulator) and the coefficient; the clipped
+        # accumulated step.
+        acc_bytes = (2 * N + 4) + (G - 2) * (2 * N + 8) if G > 1 else 0
+        pipeline = ([("accumulate_kernel", part_accumulate, acc_bytes)] if G > 1 else []) + \
+                   [("grad_sqnorm_kernel+clip_coef_kernel", part_norm_accumulated, norm_bpe + 4),
+                    ("shard_step_kernel", part_accumulated_clipped, bpe + 4)]
+        launches_per_step = G + 2
     elif clip:
         pipeline = [("grad_sqnorm_kernel+clip_coef_kernel", part_norm, norm_bpe),
                     ("shard_step_kernel", part_clipped, bpe)]
@@ -984,12 +1006,13 @@ def main(argv=None):
     ap.add_argument("--graph", action="store_true",
                     help="time one replay of a CUDA graph holding the K launches")
     ap.add_argument("--pipeline",
-                    choices=["step", "clip", "accum", "unshard", "gather", "checkpoint",
-                             "sweep"],
+                    choices=["step", "clip", "accum", "accum_clip", "unshard", "gather",
+                             "checkpoint", "sweep"],
                     default="step",
                     help="step: the fused shard step; clip: global-norm pass + clip "
                          "coefficient + clipped step; accum: G-1 accumulations + the "
-                         "accumulated step; gather: the emulated AllGather's assembly of "
+                         "accumulated step; accum_clip: accum with the norm of the "
+                         "accumulated gradient and a clipped accumulated step; gather: the emulated AllGather's assembly of "
                          "the other ranks' shards into the flat buffer; unshard: FSDP2 "
                          "copy-out of every wrap unit's "
                          "gathered parameters; checkpoint: save / restore / resharding "

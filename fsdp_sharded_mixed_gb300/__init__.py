@@ -134,6 +134,12 @@ EXPORTS = {
     "zs_shard_step_accumulated": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _I32, _P, _P, _P,
                                    _P, ctypes.c_int, ctypes.POINTER(AdamWHparams), _I64, _P],
                                   ctypes.c_int),
+    "zs_grad_sqnorm_accumulated": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _I32, _P, _I64,
+                                    _P, _P], ctypes.c_int),
+    "zs_shard_step_accumulated_clipped": ([_P, _I32, _I64, _I64, _P, ctypes.c_int, _P, _I32, _P,
+                                           _P, _P, _P, ctypes.c_int,
+                                           ctypes.POINTER(AdamWHparams), _I64, _P, _P, _P],
+                                          ctypes.c_int),
     "zs_rows_plan": ([_P, _P, _P, _I32, _I32, _I64, _P], ctypes.c_int),
     "zs_plan_rows": ([_P, _P, _P, _I32], ctypes.c_int),
     "zs_unshard": ([_P, _P, ctypes.c_int, _P, _P], ctypes.c_int),
@@ -349,6 +355,30 @@ def zs_shard_step_accumulated(plan, rank, lo, hi, grad_slices, grad_dtype, accum
                                            _ptr(accum), micro_steps, _ptr(master),
                                            _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(full_flat),
                                            param_dtype, ctypes.byref(h), step, _stream(stream)))
+
+
+def zs_grad_sqnorm_accumulated(plan, rank, lo, hi, grad_slices, grad_dtype, accum, micro_steps,
+                               workspace, sqnorm_out, stream=None):
+    """Enqueue the shard's sum of squares of the accumulated step's gradient
+    ((accum + mean) * (1/G)) into the device double ``sqnorm_out``."""
+    ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
+    nbytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") \
+        else zs_grad_norm_workspace_bytes()
+    _check(lib().zs_grad_sqnorm_accumulated(plan.handle, rank, lo, hi, ptrs, grad_dtype,
+                                            _ptr(accum), micro_steps, _ptr(workspace), nbytes,
+                                            _ptr(sqnorm_out), _stream(stream)))
+
+
+def zs_shard_step_accumulated_clipped(plan, rank, lo, hi, grad_slices, grad_dtype, accum,
+                                      micro_steps, master, exp_avg, exp_avg_sq, full_flat,
+                                      param_dtype, hp, step, coef=None, skip=None, stream=None):
+    """The accumulated step with a device clip coefficient and skip flag."""
+    ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
+    h = AdamWHparams(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"])
+    _check(lib().zs_shard_step_accumulated_clipped(
+        plan.handle, rank, lo, hi, ptrs, grad_dtype, _ptr(accum), micro_steps, _ptr(master),
+        _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(full_flat), param_dtype, ctypes.byref(h), step,
+        _ptr(coef), _ptr(skip), _stream(stream)))
 
 
 def zs_grad_norm_workspace_bytes():

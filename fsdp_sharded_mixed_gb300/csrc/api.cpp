@@ -361,11 +361,13 @@ static zs_status zs_grad_accumulate_untraced(const zs_plan* plan, int32_t rank, 
 
 extern "C" int64_t zs_grad_norm_workspace_bytes(void) { return zs::kNormWorkspaceBytes; }
 
-static zs_status zs_grad_sqnorm_untraced(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
-                                    const void* const* grad_slices, zs_dtype grad_dtype,
-                                    void* workspace, int64_t workspace_bytes, double* sqnorm_out,
-                                    void* cuda_stream) {
-  static const char* fn = "zs_grad_sqnorm";
+namespace {
+// The norm pass with caller scratch; accum (with micro_steps) selects the norm
+// of the accumulated step's gradient.
+zs_status sqnorm_impl(const char* fn, const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                      const void* const* grad_slices, zs_dtype grad_dtype, const float* accum,
+                      int32_t micro_steps, void* workspace, int64_t workspace_bytes,
+                      double* sqnorm_out, void* cuda_stream) {
   zs::clear_error();
   if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
   const int32_t N = plan->world;
@@ -392,6 +394,11 @@ static zs_status zs_grad_sqnorm_untraced(const zs_plan* plan, int32_t rank, int6
     all32 = all32 && (uintptr_t)g % 32 == 0;
     ranges.push_back({(uintptr_t)g, (uintptr_t)g + (uint64_t)S * gb, "grad_slices", j, false});
   }
+  if (accum && hi > lo) {
+    if (!aligned16(accum)) return zs::fail(ZS_ERR_ALIGN, "%s: accum is not 16-byte aligned", fn);
+    all32 = all32 && (uintptr_t)accum % 32 == 0;
+    ranges.push_back({(uintptr_t)accum, (uintptr_t)accum + (uint64_t)S * 4, "accum", 0, false});
+  }
   ranges.push_back({(uintptr_t)workspace, (uintptr_t)workspace + (uint64_t)zs::kNormWorkspaceBytes,
                     "workspace", 0, true});
   ranges.push_back({(uintptr_t)sqnorm_out, (uintptr_t)sqnorm_out + 8, "sqnorm_out", 0, true});
@@ -399,7 +406,9 @@ static zs_status zs_grad_sqnorm_untraced(const zs_plan* plan, int32_t rank, int6
   if (zs_status st = check_device_buffer(workspace, zs::kNormWorkspaceBytes, fn, "workspace", 0)) return st;
   for (int32_t j = 0; j < N && hi > lo; ++j)
     if (zs_status st = check_device_buffer(grad_slices[j], S * gb, fn, "grad_slices", j)) return st;
-  zs::NormLaunch a;
+  if (accum && hi > lo)
+    if (zs_status st = check_device_buffer(accum, S * 4, fn, "accum", 0)) return st;
+  zs::NormLaunch a = {};
   a.grads = grad_slices;
   a.world = N;
   a.grad_dtype = grad_dtype;
@@ -408,6 +417,8 @@ static zs_status zs_grad_sqnorm_untraced(const zs_plan* plan, int32_t rank, int6
   a.win = zs::step_window(lo, hi);
   a.vec = all32;
   a.invN = (float)(1.0 / (double)N);
+  a.accum = hi > lo ? accum : nullptr;
+  a.invG = (float)(1.0 / (double)(micro_steps > 0 ? micro_steps : 1));
   a.partials = static_cast<double*>(workspace);
   a.ticket = reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(workspace) +
                                              zs::kNormTicketOffset);
@@ -416,6 +427,45 @@ static zs_status zs_grad_sqnorm_untraced(const zs_plan* plan, int32_t rank, int6
   if (e != cudaSuccess)
     return zs::fail(ZS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return ZS_OK;
+}
+}  // namespace
+
+static zs_status zs_grad_sqnorm_untraced(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                                         const void* const* grad_slices, zs_dtype grad_dtype,
+                                         void* workspace, int64_t workspace_bytes,
+                                         double* sqnorm_out, void* cuda_stream) {
+  return sqnorm_impl("zs_grad_sqnorm", plan, rank, lo, hi, grad_slices, grad_dtype, nullptr, 1,
+                     workspace, workspace_bytes, sqnorm_out, cuda_stream);
+}
+
+static zs_status zs_grad_sqnorm_accumulated_untraced(
+    const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi, const void* const* grad_slices,
+    zs_dtype grad_dtype, const float* accum, int32_t micro_steps, void* workspace,
+    int64_t workspace_bytes, double* sqnorm_out, void* cuda_stream) {
+  static const char* fn = "zs_grad_sqnorm_accumulated";
+  zs::clear_error();
+  if (micro_steps < 1) return zs::fail(ZS_ERR_RANGE, "%s: micro_steps %d < 1", fn, micro_steps);
+  if (!accum && hi > lo) return zs::fail(ZS_ERR_INVAL, "%s: accum is NULL", fn);
+  return sqnorm_impl(fn, plan, rank, lo, hi, grad_slices, grad_dtype, accum, micro_steps,
+                     workspace, workspace_bytes, sqnorm_out, cuda_stream);
+}
+
+static zs_status zs_shard_step_accumulated_clipped_untraced(
+    const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi, const void* const* grad_slices,
+    zs_dtype grad_dtype, const float* accum, int32_t micro_steps, float* master, float* exp_avg,
+    float* exp_avg_sq, void* full_flat, zs_dtype param_dtype, const zs_adamw_hparams* hp,
+    int64_t step, const float* coef, const int32_t* skip, void* cuda_stream) {
+  static const char* fn = "zs_shard_step_accumulated_clipped";
+  zs::clear_error();
+  if (micro_steps < 1) return zs::fail(ZS_ERR_RANGE, "%s: micro_steps %d < 1", fn, micro_steps);
+  if (!accum && hi > lo) return zs::fail(ZS_ERR_INVAL, "%s: accum is NULL", fn);
+  if (coef)
+    if (zs_status st = check_device_scalar(coef, 4, fn, "coef")) return st;
+  if (skip)
+    if (zs_status st = check_device_scalar(skip, 4, fn, "skip")) return st;
+  return shard_step_impl(fn, plan, rank, lo, hi, grad_slices, grad_dtype, master, exp_avg,
+                         exp_avg_sq, full_flat, param_dtype, hp, step, coef, skip, accum,
+                         micro_steps, cuda_stream);
 }
 
 static zs_status zs_grad_sqnorm_noalloc_untraced(const zs_plan* plan, int32_t rank, int64_t lo,
@@ -453,7 +503,7 @@ static zs_status zs_grad_sqnorm_noalloc_untraced(const zs_plan* plan, int32_t ra
   if (zs_status st = check_overlaps(ranges, fn)) return st;
   for (int32_t j = 0; j < N && hi > lo; ++j)
     if (zs_status st = check_device_buffer(grad_slices[j], S * gb, fn, "grad_slices", j)) return st;
-  zs::NormLaunch a;
+  zs::NormLaunch a = {};
   a.grads = grad_slices;
   a.world = N;
   a.grad_dtype = grad_dtype;
@@ -830,6 +880,34 @@ extern "C" zs_status zs_grad_sqnorm(const zs_plan* plan, int32_t rank, int64_t l
                                             workspace, workspace_bytes, sqnorm_out,
                                             cuda_stream),
                     "zs_grad_sqnorm", plan, rank, lo, hi, grad_dtype, -1, 0);
+}
+
+extern "C" zs_status zs_grad_sqnorm_accumulated(const zs_plan* plan, int32_t rank, int64_t lo,
+                                                int64_t hi, const void* const* grad_slices,
+                                                zs_dtype grad_dtype, const float* accum,
+                                                int32_t micro_steps, void* workspace,
+                                                int64_t workspace_bytes, double* sqnorm_out,
+                                                void* cuda_stream) {
+  const zs::CallRange range("zs_grad_sqnorm_accumulated");
+  return zs::traced(zs_grad_sqnorm_accumulated_untraced(plan, rank, lo, hi, grad_slices,
+                                                        grad_dtype, accum, micro_steps,
+                                                        workspace, workspace_bytes, sqnorm_out,
+                                                        cuda_stream),
+                    "zs_grad_sqnorm_accumulated", plan, rank, lo, hi, grad_dtype, -1, 0);
+}
+
+extern "C" zs_status zs_shard_step_accumulated_clipped(
+    const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi, const void* const* grad_slices,
+    zs_dtype grad_dtype, const float* accum, int32_t micro_steps, float* master, float* exp_avg,
+    float* exp_avg_sq, void* full_flat, zs_dtype param_dtype, const zs_adamw_hparams* hp,
+    int64_t step, const float* coef, const int32_t* skip, void* cuda_stream) {
+  const zs::CallRange range("zs_shard_step_accumulated_clipped");
+  return zs::traced(zs_shard_step_accumulated_clipped_untraced(
+                        plan, rank, lo, hi, grad_slices, grad_dtype, accum, micro_steps, master,
+                        exp_avg, exp_avg_sq, full_flat, param_dtype, hp, step, coef, skip,
+                        cuda_stream),
+                    "zs_shard_step_accumulated_clipped", plan, rank, lo, hi, grad_dtype,
+                    param_dtype, step);
 }
 
 extern "C" zs_status zs_grad_sqnorm_noalloc(const zs_plan* plan, int32_t rank, int64_t lo,

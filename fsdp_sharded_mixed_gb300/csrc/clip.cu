@@ -12,7 +12,9 @@
 // GPU); the step multiplies the mean gradient by it, and a non-finite norm
 // makes the step leave every buffer untouched.
 //
-// The norm pass reads the N slices once (g*N bytes per element). Squares are
+// The norm pass reads the N slices once (g*N bytes per element); for a step
+// that ends gradient accumulation it takes the norm of the gradient that step
+// sees, (accum + mean) * (1/G), and also reads the accumulator (4 more bytes). Squares are
 // formed in fp32 with their exact rounding residue (an FMA), summed per
 // 16-element group with a compensated (two-sum) fp32 accumulator, and folded
 // into a per-thread double; double work is one add per group, because GB300's
@@ -47,6 +49,8 @@ struct NormArgs {
   double* out;
   int64_t win_lo, win_hi;  // checked build: the elements any read may touch
   unsigned int* err;       // checked build: the device error word
+  const float* accum;      // ACC: fp32 sum of the earlier micro-steps' mean gradients
+  float invG;              // ACC: fp32(1/G)
 };
 
 __device__ __forceinline__ void ld32_nc(const void* p, uint32_t* r) {
@@ -69,7 +73,9 @@ __device__ __forceinline__ void acc_square(float g, float& s, float& c) {
   c = __fadd_rn(c, __fadd_rn(err, lo));
 }
 
-template <bool BF16G, int MAXN>
+// The gradient the step sees at element i: the mean of the slices; with ACC,
+// the micro-batch average (accum + mean) * (1/G).
+template <bool BF16G, bool ACC, int MAXN>
 __device__ __forceinline__ float mean_grad(const NormArgs<MAXN>& a, int64_t i) {
   if (!within(i, i + 1, a.win_lo, a.win_hi, a.err)) return 0.0f;
   float acc = 0.0f;
@@ -79,12 +85,14 @@ __device__ __forceinline__ float mean_grad(const NormArgs<MAXN>& a, int64_t i) {
                           : static_cast<const float*>(a.grads[j])[i];
     acc = __fadd_rn(acc, x);
   }
-  return __fmul_rn(acc, a.invN);
+  const float mean = __fmul_rn(acc, a.invN);
+  return ACC ? __fmul_rn(__fadd_rn(a.accum[i], mean), a.invG) : mean;
 }
 
-// VEC: 16-element groups with 32-byte loads (all slices 32-byte aligned);
-// otherwise element by element.
-template <bool BF16G, bool VEC, int MAXN>
+// VEC: 16-element groups with 32-byte loads (all slices, and with ACC the
+// accumulator, 32-byte aligned); otherwise element by element. ACC: the norm
+// of the accumulated step's gradient (accum + mean) * (1/G).
+template <bool BF16G, bool VEC, int MAXN, bool ACC>
 __global__ void __launch_bounds__(kThreads, 2) grad_sqnorm_kernel(const __grid_constant__ NormArgs<MAXN> a) {
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
@@ -96,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 2) grad_sqnorm_kernel(const __grid_c
   }
   if (g0 >= g1) {
     for (int64_t i = a.lo + tid; i < a.hi; i += stride) {
-      const float g = mean_grad<BF16G>(a, i);
+      const float g = mean_grad<BF16G, ACC>(a, i);
       float s = 0.0f, c = 0.0f;
       acc_square(g, s, c);
       sum += (double)s + (double)c;
@@ -105,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 2) grad_sqnorm_kernel(const __grid_c
     const int64_t head = g0 * kGW - a.lo, tail = a.hi - g1 * kGW;
     if (tid < head + tail) {
       const int64_t i = tid < head ? a.lo + tid : g1 * kGW + (tid - head);
-      const float g = mean_grad<BF16G>(a, i);
+      const float g = mean_grad<BF16G, ACC>(a, i);
       float s = 0.0f, c = 0.0f;
       acc_square(g, s, c);
       sum += (double)s + (double)c;
@@ -144,9 +152,18 @@ __global__ void __launch_bounds__(kThreads, 2) grad_sqnorm_kernel(const __grid_c
           }
         }
       }
+      float prev[ACC ? kGW : 1];
+      if constexpr (ACC) {
+        const float* ap = a.accum + kGW * g;
+        ld32_nc(ap, reinterpret_cast<uint32_t*>(prev));
+        ld32_nc(ap + 8, reinterpret_cast<uint32_t*>(prev) + 8);
+      }
       float s = 0.0f, c = 0.0f;
 #pragma unroll
-      for (int k = 0; k < kGW; ++k) acc_square(__fmul_rn(acc[k], a.invN), s, c);
+      for (int k = 0; k < kGW; ++k) {
+        const float mean = __fmul_rn(acc[k], a.invN);
+        acc_square(ACC ? __fmul_rn(__fadd_rn(prev[k], mean), a.invG) : mean, s, c);
+      }
       sum += (double)s + (double)c;
     }
   }
@@ -189,7 +206,7 @@ __global__ void clip_coef_kernel(const double* rank_sqnorms, int n, double max_n
   *coef = bad ? 1.0f : (float)(c < 1.0 ? c : 1.0);
 }
 
-template <bool BF16G, bool VEC, int MAXN>
+template <bool BF16G, bool VEC, int MAXN, bool ACC>
 cudaError_t launch_norm(const NormLaunch& in, cudaStream_t stream) {
   NormArgs<MAXN> a;
   for (int j = 0; j < MAXN; ++j) a.grads[j] = (in.grads && j < in.world) ? in.grads[j] : nullptr;
@@ -204,25 +221,35 @@ cudaError_t launch_norm(const NormLaunch& in, cudaStream_t stream) {
   a.win_hi = in.win.hi;
   a.err = ZS_BOUNDS_CHECK ? device_error_word() : nullptr;
   if (ZS_BOUNDS_CHECK && !a.err) return cudaErrorInvalidSymbol;
+  a.accum = in.accum;
+  a.invG = in.invG;
   cudaError_t e = cudaMemsetAsync(in.ticket, 0, sizeof(unsigned int), stream);
   if (e != cudaSuccess) return e;
-  grad_sqnorm_kernel<BF16G, VEC, MAXN><<<kNormPartials, kThreads, 0, stream>>>(a);
+  grad_sqnorm_kernel<BF16G, VEC, MAXN, ACC><<<kNormPartials, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_grad_sqnorm(const NormLaunch& a, cudaStream_t stream) {
+template <bool ACC>
+cudaError_t dispatch_norm(const NormLaunch& a, cudaStream_t stream) {
   const bool bf16g = a.grad_dtype == ZS_BF16;
   if (a.world <= 16) {
-    if (a.vec) return bf16g ? launch_norm<true, true, 16>(a, stream) : launch_norm<false, true, 16>(a, stream);
-    return bf16g ? launch_norm<true, false, 16>(a, stream) : launch_norm<false, false, 16>(a, stream);
+    if (a.vec)
+      return bf16g ? launch_norm<true, true, 16, ACC>(a, stream)
+                   : launch_norm<false, true, 16, ACC>(a, stream);
+    return bf16g ? launch_norm<true, false, 16, ACC>(a, stream)
+                 : launch_norm<false, false, 16, ACC>(a, stream);
   }
   if (a.vec)
-    return bf16g ? launch_norm<true, true, ZS_MAX_WORLD>(a, stream)
-                 : launch_norm<false, true, ZS_MAX_WORLD>(a, stream);
-  return bf16g ? launch_norm<true, false, ZS_MAX_WORLD>(a, stream)
-               : launch_norm<false, false, ZS_MAX_WORLD>(a, stream);
+    return bf16g ? launch_norm<true, true, ZS_MAX_WORLD, ACC>(a, stream)
+                 : launch_norm<false, true, ZS_MAX_WORLD, ACC>(a, stream);
+  return bf16g ? launch_norm<true, false, ZS_MAX_WORLD, ACC>(a, stream)
+               : launch_norm<false, false, ZS_MAX_WORLD, ACC>(a, stream);
+}
+
+cudaError_t launch_grad_sqnorm(const NormLaunch& a, cudaStream_t stream) {
+  return a.accum ? dispatch_norm<true>(a, stream) : dispatch_norm<false>(a, stream);
 }
 
 cudaError_t launch_clip_coef(const double* rank_sqnorms, int n, double max_norm, float* coef,

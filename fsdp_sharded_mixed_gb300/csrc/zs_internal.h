@@ -107,6 +107,8 @@ struct NormLaunch {
   unsigned int* ticket;
   double* out;
   Window win;           // checked build: every element the pass reads lies in it
+  const float* accum;   // fp32 [S] accumulator: the norm of (accum + mean) * invG; or NULL
+  float invG;           // fp32(1/G) with accum
 };
 cudaError_t launch_grad_sqnorm(const NormLaunch& a, cudaStream_t stream);
 // The same norm pass with its scratch in a file-scope device array of

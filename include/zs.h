@@ -294,6 +294,36 @@ zs_status zs_shard_step_accumulated(const zs_plan* plan, int32_t rank, int64_t l
                                     zs_dtype param_dtype, const zs_adamw_hparams* hp,
                                     int64_t step, void* cuda_stream);
 
+/* Clipping an accumulated gradient (both questions of the section above at
+ * once). The clip acts on the gradient the update sees, the micro-batch
+ * average g = (accum + mean) * fp32(1/G): its global norm, not the last
+ * micro-step's, decides the coefficient. Per optimizer step, after micro-steps
+ * 1 .. G-1 went through zs_grad_accumulate:
+ *   1. each rank: zs_grad_sqnorm_accumulated -> its shard's sum of g_i^2;
+ *   2. zs_clip_coefficient over the N partial sums, as for the plain step;
+ *   3. each rank: zs_shard_step_accumulated_clipped with coef and skip.
+ *
+ * zs_grad_sqnorm with g_i = (accum[i] + mean_j x_j[i]) * fp32(1/micro_steps),
+ * formed as zs_shard_step_accumulated forms it. accum: device fp32 [S], read
+ * only. Errors as zs_grad_sqnorm and zs_shard_step_accumulated. */
+zs_status zs_grad_sqnorm_accumulated(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
+                                     const void* const* grad_slices, zs_dtype grad_dtype,
+                                     const float* accum, int32_t micro_steps, void* workspace,
+                                     int64_t workspace_bytes, double* sqnorm_out,
+                                     void* cuda_stream);
+/* zs_shard_step_accumulated on g * (*coef) (coef NULL: no scaling), and no
+ * change to any buffer when skip is not NULL and *skip != 0; coef and skip as
+ * in zs_shard_step_clipped. With coef == skip == NULL it is
+ * zs_shard_step_accumulated. */
+zs_status zs_shard_step_accumulated_clipped(const zs_plan* plan, int32_t rank, int64_t lo,
+                                            int64_t hi, const void* const* grad_slices,
+                                            zs_dtype grad_dtype, const float* accum,
+                                            int32_t micro_steps, float* master, float* exp_avg,
+                                            float* exp_avg_sq, void* full_flat,
+                                            zs_dtype param_dtype, const zs_adamw_hparams* hp,
+                                            int64_t step, const float* coef,
+                                            const int32_t* skip, void* cuda_stream);
+
 /* ---------------------------------------------------------------------------
  * Per-parameter row sharding (FSDP2) and the gather side of a wrap unit.
  * [DP-to-ZeRO] "ZeRO 与 FSDP 的关系": FSDP2's fully_shard keeps per-parameter
