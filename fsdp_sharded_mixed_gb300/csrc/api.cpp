@@ -362,12 +362,13 @@ static zs_status zs_grad_accumulate_untraced(const zs_plan* plan, int32_t rank, 
 extern "C" int64_t zs_grad_norm_workspace_bytes(void) { return zs::kNormWorkspaceBytes; }
 
 namespace {
-// The norm pass with caller scratch; accum (with micro_steps) selects the norm
-// of the accumulated step's gradient.
+// The norm pass. Scratch: the caller's workspace, or (noalloc) the library's
+// static device array. accum (with micro_steps) selects the norm of the
+// accumulated step's gradient.
 zs_status sqnorm_impl(const char* fn, const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
                       const void* const* grad_slices, zs_dtype grad_dtype, const float* accum,
-                      int32_t micro_steps, void* workspace, int64_t workspace_bytes,
-                      double* sqnorm_out, void* cuda_stream) {
+                      int32_t micro_steps, bool noalloc, void* workspace,
+                      int64_t workspace_bytes, double* sqnorm_out, void* cuda_stream) {
   zs::clear_error();
   if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
   const int32_t N = plan->world;
@@ -378,10 +379,18 @@ zs_status sqnorm_impl(const char* fn, const zs_plan* plan, int32_t rank, int64_t
                     (long long)lo, (long long)hi, (long long)S);
   if (grad_dtype != ZS_BF16 && grad_dtype != ZS_FP32)
     return zs::fail(ZS_ERR_INVAL, "%s: gradient dtype %d is not bf16 or fp32", fn, (int)grad_dtype);
-  if (!workspace || workspace_bytes < zs::kNormWorkspaceBytes)
-    return zs::fail(ZS_ERR_RANGE, "%s: workspace must hold %lld bytes", fn,
-                    (long long)zs::kNormWorkspaceBytes);
-  if (!aligned16(workspace)) return zs::fail(ZS_ERR_ALIGN, "%s: workspace is not 16-byte aligned", fn);
+  if (noalloc) {
+    // The scratch this call needs must fit the library's static array.
+    if (zs::kNormWorkspaceBytes > zs::kNoAllocScratchBytes)
+      return zs::fail(ZS_ERR_RANGE, "%s: needs %lld bytes of scratch, the static array holds %lld",
+                      fn, (long long)zs::kNormWorkspaceBytes, (long long)zs::kNoAllocScratchBytes);
+  } else {
+    if (!workspace || workspace_bytes < zs::kNormWorkspaceBytes)
+      return zs::fail(ZS_ERR_RANGE, "%s: workspace must hold %lld bytes", fn,
+                      (long long)zs::kNormWorkspaceBytes);
+    if (!aligned16(workspace))
+      return zs::fail(ZS_ERR_ALIGN, "%s: workspace is not 16-byte aligned", fn);
+  }
   if (zs_status st = check_device_scalar(sqnorm_out, 8, fn, "sqnorm_out")) return st;
   if (hi > lo && !grad_slices) return zs::fail(ZS_ERR_INVAL, "%s: grad_slices is NULL", fn);
   const int gb = grad_dtype == ZS_BF16 ? 2 : 4;
@@ -399,11 +408,15 @@ zs_status sqnorm_impl(const char* fn, const zs_plan* plan, int32_t rank, int64_t
     all32 = all32 && (uintptr_t)accum % 32 == 0;
     ranges.push_back({(uintptr_t)accum, (uintptr_t)accum + (uint64_t)S * 4, "accum", 0, false});
   }
-  ranges.push_back({(uintptr_t)workspace, (uintptr_t)workspace + (uint64_t)zs::kNormWorkspaceBytes,
-                    "workspace", 0, true});
+  if (!noalloc)
+    ranges.push_back({(uintptr_t)workspace,
+                      (uintptr_t)workspace + (uint64_t)zs::kNormWorkspaceBytes, "workspace", 0,
+                      true});
   ranges.push_back({(uintptr_t)sqnorm_out, (uintptr_t)sqnorm_out + 8, "sqnorm_out", 0, true});
   if (zs_status st = check_overlaps(ranges, fn)) return st;
-  if (zs_status st = check_device_buffer(workspace, zs::kNormWorkspaceBytes, fn, "workspace", 0)) return st;
+  if (!noalloc)
+    if (zs_status st = check_device_buffer(workspace, zs::kNormWorkspaceBytes, fn, "workspace", 0))
+      return st;
   for (int32_t j = 0; j < N && hi > lo; ++j)
     if (zs_status st = check_device_buffer(grad_slices[j], S * gb, fn, "grad_slices", j)) return st;
   if (accum && hi > lo)
@@ -419,13 +432,20 @@ zs_status sqnorm_impl(const char* fn, const zs_plan* plan, int32_t rank, int64_t
   a.invN = (float)(1.0 / (double)N);
   a.accum = hi > lo ? accum : nullptr;
   a.invG = (float)(1.0 / (double)(micro_steps > 0 ? micro_steps : 1));
-  a.partials = static_cast<double*>(workspace);
-  a.ticket = reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(workspace) +
-                                             zs::kNormTicketOffset);
   a.out = sqnorm_out;
-  cudaError_t e = zs::launch_grad_sqnorm(a, static_cast<cudaStream_t>(cuda_stream));
+  cudaError_t e;
+  if (noalloc) {
+    // partials and ticket: set to the static array by the launcher
+    e = zs::launch_grad_sqnorm_noalloc(a, static_cast<cudaStream_t>(cuda_stream));
+  } else {
+    a.partials = static_cast<double*>(workspace);
+    a.ticket = reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(workspace) +
+                                               zs::kNormTicketOffset);
+    e = zs::launch_grad_sqnorm(a, static_cast<cudaStream_t>(cuda_stream));
+  }
   if (e != cudaSuccess)
-    return zs::fail(ZS_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+    return zs::fail(ZS_ERR_CUDA, "%s: %s failed: %s", fn, noalloc ? "set-up or launch" : "launch",
+                    cudaGetErrorString(e));
   return ZS_OK;
 }
 }  // namespace
@@ -435,7 +455,7 @@ static zs_status zs_grad_sqnorm_untraced(const zs_plan* plan, int32_t rank, int6
                                          void* workspace, int64_t workspace_bytes,
                                          double* sqnorm_out, void* cuda_stream) {
   return sqnorm_impl("zs_grad_sqnorm", plan, rank, lo, hi, grad_slices, grad_dtype, nullptr, 1,
-                     workspace, workspace_bytes, sqnorm_out, cuda_stream);
+                     false, workspace, workspace_bytes, sqnorm_out, cuda_stream);
 }
 
 static zs_status zs_grad_sqnorm_accumulated_untraced(
@@ -446,7 +466,7 @@ static zs_status zs_grad_sqnorm_accumulated_untraced(
   zs::clear_error();
   if (micro_steps < 1) return zs::fail(ZS_ERR_RANGE, "%s: micro_steps %d < 1", fn, micro_steps);
   if (!accum && hi > lo) return zs::fail(ZS_ERR_INVAL, "%s: accum is NULL", fn);
-  return sqnorm_impl(fn, plan, rank, lo, hi, grad_slices, grad_dtype, accum, micro_steps,
+  return sqnorm_impl(fn, plan, rank, lo, hi, grad_slices, grad_dtype, accum, micro_steps, false,
                      workspace, workspace_bytes, sqnorm_out, cuda_stream);
 }
 
@@ -469,56 +489,11 @@ static zs_status zs_shard_step_accumulated_clipped_untraced(
 }
 
 static zs_status zs_grad_sqnorm_noalloc_untraced(const zs_plan* plan, int32_t rank, int64_t lo,
-                                            int64_t hi, const void* const* grad_slices,
-                                            zs_dtype grad_dtype, double* sqnorm_out,
-                                            void* cuda_stream) {
-  static const char* fn = "zs_grad_sqnorm_noalloc";
-  zs::clear_error();
-  if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
-  const int32_t N = plan->world;
-  const int64_t S = plan->S;
-  if (rank < 0 || rank >= N) return zs::fail(ZS_ERR_RANGE, "%s: rank %d not in [0, %d)", fn, rank, N);
-  if (lo < 0 || hi < lo || hi > S)
-    return zs::fail(ZS_ERR_RANGE, "%s: [lo, hi) = [%lld, %lld) not inside [0, %lld)", fn,
-                    (long long)lo, (long long)hi, (long long)S);
-  if (grad_dtype != ZS_BF16 && grad_dtype != ZS_FP32)
-    return zs::fail(ZS_ERR_INVAL, "%s: gradient dtype %d is not bf16 or fp32", fn, (int)grad_dtype);
-  // The scratch this call needs must fit the library's static array.
-  if (zs::kNormWorkspaceBytes > zs::kNoAllocScratchBytes)
-    return zs::fail(ZS_ERR_RANGE, "%s: needs %lld bytes of scratch, the static array holds %lld",
-                    fn, (long long)zs::kNormWorkspaceBytes, (long long)zs::kNoAllocScratchBytes);
-  if (zs_status st = check_device_scalar(sqnorm_out, 8, fn, "sqnorm_out")) return st;
-  if (hi > lo && !grad_slices) return zs::fail(ZS_ERR_INVAL, "%s: grad_slices is NULL", fn);
-  const int gb = grad_dtype == ZS_BF16 ? 2 : 4;
-  std::vector<Range> ranges;
-  bool all32 = true;
-  for (int32_t j = 0; j < N && hi > lo; ++j) {
-    const void* g = grad_slices[j];
-    if (!g) return zs::fail(ZS_ERR_INVAL, "%s: grad_slices[%d] is NULL", fn, j);
-    if (!aligned16(g)) return zs::fail(ZS_ERR_ALIGN, "%s: grad_slices[%d] is not 16-byte aligned", fn, j);
-    all32 = all32 && (uintptr_t)g % 32 == 0;
-    ranges.push_back({(uintptr_t)g, (uintptr_t)g + (uint64_t)S * gb, "grad_slices", j, false});
-  }
-  ranges.push_back({(uintptr_t)sqnorm_out, (uintptr_t)sqnorm_out + 8, "sqnorm_out", 0, true});
-  if (zs_status st = check_overlaps(ranges, fn)) return st;
-  for (int32_t j = 0; j < N && hi > lo; ++j)
-    if (zs_status st = check_device_buffer(grad_slices[j], S * gb, fn, "grad_slices", j)) return st;
-  zs::NormLaunch a = {};
-  a.grads = grad_slices;
-  a.world = N;
-  a.grad_dtype = grad_dtype;
-  a.lo = lo;
-  a.hi = hi;
-  a.win = zs::step_window(lo, hi);
-  a.vec = all32;
-  a.invN = (float)(1.0 / (double)N);
-  a.partials = nullptr;  // set to the static array by the launcher
-  a.ticket = nullptr;
-  a.out = sqnorm_out;
-  cudaError_t e = zs::launch_grad_sqnorm_noalloc(a, static_cast<cudaStream_t>(cuda_stream));
-  if (e != cudaSuccess)
-    return zs::fail(ZS_ERR_CUDA, "%s: set-up or launch failed: %s", fn, cudaGetErrorString(e));
-  return ZS_OK;
+                                                 int64_t hi, const void* const* grad_slices,
+                                                 zs_dtype grad_dtype, double* sqnorm_out,
+                                                 void* cuda_stream) {
+  return sqnorm_impl("zs_grad_sqnorm_noalloc", plan, rank, lo, hi, grad_slices, grad_dtype,
+                     nullptr, 1, true, nullptr, 0, sqnorm_out, cuda_stream);
 }
 
 static zs_status zs_clip_coefficient_untraced(const double* rank_sqnorms, int32_t n, double max_norm,
