@@ -147,6 +147,7 @@ EXPORTS = {
     "zs_checkpoint_save": ([_P, _I32, _P, _P, _P, _I64, ctypes.c_char_p, _P], ctypes.c_int),
     "zs_checkpoint_load": ([_P, _I32, _P, _I32, _P, _P, _P, _P, _P], ctypes.c_int),
     "zs_checkpoint_info": ([ctypes.c_char_p, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "zs_checkpoint_release_staging": ([], ctypes.c_int),
     "zs_set_trace": ([ctypes.c_char_p], ctypes.c_int),
     "zs_trace_first_divergence": ([_P, _I32, _P, ctypes.c_char_p, _I64], ctypes.c_int),
     "zs_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -452,6 +453,11 @@ def zs_checkpoint_load(plan, rank, paths, master, exp_avg, exp_avg_sq, stream=No
                                     _ptr(exp_avg), _ptr(exp_avg_sq), ctypes.byref(step),
                                     _io_stream(stream)))
     return step.value
+
+
+def zs_checkpoint_release_staging():
+    """Free the pinned staging kept between checkpoint calls."""
+    _check(lib().zs_checkpoint_release_staging())
 
 
 def zs_checkpoint_info(path):

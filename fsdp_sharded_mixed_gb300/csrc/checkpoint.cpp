@@ -450,37 +450,80 @@ zs_status check_state(const char* fn, int64_t S, void* const* arrays, bool outpu
   return ZS_OK;
 }
 
+// Pinned staging kept from one checkpoint call to the next: allocating and
+// pinning kSlots x 64 MiB costs about 8 ms on a Grace host (measured), close
+// to a tenth of a restore from the page cache. One set is kept (the last one
+// returned, for one device and size); zs_checkpoint_release_staging frees it.
+struct StagingCache {
+  std::mutex mu;
+  unsigned char* buf[kSlots] = {};  // guarded by mu; buf[0] == NULL: empty
+  int64_t bytes = 0;
+  int dev = -1;
+};
+StagingCache& staging_cache() {
+  static StagingCache* c = new StagingCache;  // never destroyed: no CUDA calls at exit
+  return *c;
+}
+
 // Staging buffers (pinned for device-resident state) and their events.
 struct Staging {
   unsigned char* buf[kSlots] = {};
   cudaEvent_t ev[kSlots] = {};
-  bool used[kSlots] = {};
   bool pinned = false;
+  int64_t bytes = 0;
+  int dev = -1;
   std::vector<unsigned char> host;
   Staging() = default;
   Staging(const Staging&) = delete;
   Staging& operator=(const Staging&) = delete;
   ~Staging() {
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < kSlots; ++s)
       if (ev[s]) cudaEventDestroy(ev[s]);
-      if (pinned && buf[s]) cudaFreeHost(buf[s]);
+    if (!pinned) return;
+    bool all = true;
+    for (int s = 0; s < kSlots; ++s) all = all && buf[s];
+    if (all) {
+      StagingCache& c = staging_cache();
+      std::lock_guard<std::mutex> l(c.mu);
+      if (!c.buf[0]) {  // keep this set for the next call
+        for (int s = 0; s < kSlots; ++s) c.buf[s] = buf[s];
+        c.bytes = bytes;
+        c.dev = dev;
+        return;
+      }
     }
+    for (int s = 0; s < kSlots; ++s)
+      if (buf[s]) cudaFreeHost(buf[s]);
   }
-  zs_status init(bool device, int64_t bytes, const char* fn) {
+  zs_status init(bool device, int64_t n, const char* fn) {
     if (!device) {
       try {
-        host.resize((size_t)bytes * kSlots);
+        host.resize((size_t)n * kSlots);
       } catch (...) {
         return zs::fail(ZS_ERR_NOMEM, "%s: no host memory for %lld bytes of staging", fn,
-                        (long long)(bytes * kSlots));
+                        (long long)(n * kSlots));
       }
-      for (int s = 0; s < kSlots; ++s) buf[s] = host.data() + (size_t)bytes * s;
+      for (int s = 0; s < kSlots; ++s) buf[s] = host.data() + (size_t)n * s;
       return ZS_OK;
     }
     pinned = true;
+    bytes = n;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+      return zs::fail(ZS_ERR_CUDA, "%s: staging: no current device", fn);
+    {
+      StagingCache& c = staging_cache();
+      std::lock_guard<std::mutex> l(c.mu);
+      if (c.buf[0] && c.bytes == n && c.dev == dev) {
+        for (int s = 0; s < kSlots; ++s) {
+          buf[s] = c.buf[s];
+          c.buf[s] = nullptr;
+        }
+      }
+    }
     for (int s = 0; s < kSlots; ++s) {
-      cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&buf[s]), (size_t)bytes,
-                                    cudaHostAllocDefault);
+      cudaError_t e = cudaSuccess;
+      if (!buf[s])
+        e = cudaHostAlloc(reinterpret_cast<void**>(&buf[s]), (size_t)n, cudaHostAllocDefault);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev[s], cudaEventDisableTiming);
       if (e != cudaSuccess)
         return zs::fail(ZS_ERR_CUDA, "%s: staging: %s", fn, cudaGetErrorString(e));
@@ -930,72 +973,145 @@ static zs_status zs_checkpoint_load_untraced(const zs_plan* plan, int32_t rank,
   Pool pool(pool_threads());
   const int64_t items = (int64_t)units.size() * kArrays;
   const int64_t piece_blocks = std::max<int64_t>(1, kPiece / B);
+  // Every (item, piece) is one task of one pool run, items in order (item i =
+  // array i % 3 of unit i / 3), so the next items' reads go on while an
+  // item's last pieces finish: no barrier per item. Item i stages in slot
+  // i % kSlots once item i - kSlots has left it (issued, and on the device
+  // its copies done); the task that reads an item's last piece issues, in
+  // item order, the copies of every item that is then complete.
+  std::vector<int64_t> first((size_t)items + 1, 0);
   for (int64_t i = 0; i < items; ++i) {
+    const Unit& u = units[(size_t)(i / kArrays)];
+    first[(size_t)i + 1] = first[(size_t)i] + n_blocks(u.blk_hi - u.blk_lo, piece_blocks);
+  }
+  std::mutex mu;
+  std::condition_variable cv;
+  std::vector<int64_t> left((size_t)items);  // guarded by mu: pieces not yet read
+  for (int64_t i = 0; i < items; ++i)
+    left[(size_t)i] = first[(size_t)i + 1] - first[(size_t)i];
+  std::vector<char> issued((size_t)items, 0);  // guarded by mu
+  int64_t next_issue = 0;                      // guarded by mu
+  bool stop = false;                           // guarded by mu: a failure; tasks return
+  bool io_bad = false;
+  int64_t bad_block = -1;
+  int bad_k = 0, bad_a = 0;
+  cudaError_t cuda_bad = cudaSuccess;
+  int dev = 0;
+  if (device && cudaGetDevice(&dev) != cudaSuccess) {
+    cudaStreamSynchronize(stream);
+    return zs::fail(ZS_ERR_CUDA, "%s: no current device", fn);
+  }
+  // Copies item i out of its slot (device: enqueued, with the checksums of
+  // the blocks the device checks and the slot's event). Called with mu held.
+  auto issue = [&](int64_t i) -> cudaError_t {
     const size_t ui = (size_t)(i / kArrays);
     const Unit& u = units[ui];
     const int a = (int)(i % kArrays);
     const int s = (int)(i % kSlots);
-    if (device && stg.used[s]) {
-      const cudaError_t e = cudaEventSynchronize(stg.ev[s]);
-      if (e != cudaSuccess) {
-        cudaStreamSynchronize(stream);
-        return cuda_fail(fn, "copy to device", e);
-      }
-    }
-    // Read the unit's blocks and check each one, in parallel pieces.
-    const int64_t base = h0.data_offset + a * h0.array_stride;
-    std::atomic<int64_t> bad{-1};
-    std::atomic<bool> io_bad{false};
-    pool.run(n_blocks(u.blk_hi - u.blk_lo, piece_blocks), [&](int64_t p) {
-      const int64_t b0 = u.blk_lo + p * piece_blocks;
-      const int64_t b1 = std::min(u.blk_hi, b0 + piece_blocks);
-      const int64_t off = b0 * B, len = std::min(b1 * B, ob) - off;
-      unsigned char* dst = stg.buf[s] + (off - u.blk_lo * B);
-      if (!pread_full(files[(size_t)u.k].fd, dst, len, base + off)) {
-        io_bad.store(true);
-        return;
-      }
-      for (int64_t b = b0; b < b1; ++b) {
-        if (!host_check[ui][(size_t)(b - u.blk_lo)]) continue;
-        const int64_t l = std::min(B, ob - b * B);
-        if (host_hash(dst + (b - b0) * B, l, b, B, (uint32_t)a) !=
-            tables[(size_t)u.k][(size_t)(a * onb + b)]) {
-          int64_t none = -1;
-          bad.compare_exchange_strong(none, b);
-        }
-      }
-    });
-    if (io_bad.load() || bad.load() >= 0) {
-      if (device) cudaStreamSynchronize(stream);
-      if (io_bad.load()) return zs::fail(ZS_ERR_IO, "%s: reading %s failed", fn, paths[u.k]);
-      return zs::fail(ZS_ERR_CORRUPT, "%s: %s: %s block %lld checksum mismatch (the state "
-                      "arrays now hold partial data)", fn, paths[u.k], kArrayName[a],
-                      (long long)bad.load());
-    }
     unsigned char* out = static_cast<unsigned char*>(arrays[a]);
-    if (device) {
-      cudaError_t e = cudaSuccess;
-      for (const Copy& c : u.copies) {
-        e = cudaMemcpyAsync(out + c.dst, stg.buf[s] + c.stage, (size_t)c.bytes,
-                            cudaMemcpyHostToDevice, stream);
-        if (e != cudaSuccess) break;
-      }
-      for (const Span& sp : spans[ui]) {
-        if (e != cudaSuccess) break;
-        e = zs::launch_block_hash(out + sp.dst, std::min(sp.fb1 * B, ob) - sp.fb0 * B, sp.fb0, B,
-                                  (uint32_t)a, sp.parts, dev_sums_d + a * n_dev + sp.slot,
-                                  stream);
-      }
-      if (e == cudaSuccess) e = cudaEventRecord(stg.ev[s], stream);
-      if (e != cudaSuccess) {
-        cudaStreamSynchronize(stream);
-        return cuda_fail(fn, "copy to device", e);
-      }
-      stg.used[s] = true;
-    } else {
+    if (!device) {
       for (const Copy& c : u.copies)
         std::memcpy(out + c.dst, stg.buf[s] + c.stage, (size_t)c.bytes);
+      return cudaSuccess;
     }
+    cudaError_t e = cudaSuccess;
+    for (const Copy& c : u.copies) {
+      e = cudaMemcpyAsync(out + c.dst, stg.buf[s] + c.stage, (size_t)c.bytes,
+                          cudaMemcpyHostToDevice, stream);
+      if (e != cudaSuccess) return e;
+    }
+    for (const Span& sp : spans[ui]) {
+      e = zs::launch_block_hash(out + sp.dst, std::min(sp.fb1 * B, ob) - sp.fb0 * B, sp.fb0, B,
+                                (uint32_t)a, sp.parts, dev_sums_d + a * n_dev + sp.slot,
+                                stream);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaEventRecord(stg.ev[s], stream);
+  };
+  pool.run(first[(size_t)items], [&](int64_t p) {
+    const int64_t i =
+        (int64_t)(std::upper_bound(first.begin(), first.end(), p) - first.begin()) - 1;
+    const size_t ui = (size_t)(i / kArrays);
+    const Unit& u = units[ui];
+    const int a = (int)(i % kArrays);
+    const int s = (int)(i % kSlots);
+    if (device) cudaSetDevice(dev);  // worker threads: the caller's device
+    if (i >= kSlots) {
+      std::unique_lock<std::mutex> l(mu);
+      cv.wait(l, [&] { return stop || issued[(size_t)(i - kSlots)]; });
+      if (stop) return;
+    } else {
+      std::lock_guard<std::mutex> l(mu);
+      if (stop) return;
+    }
+    if (device && i >= kSlots) {
+      // The slot's last user's copies (its event is not recorded again before
+      // this item's pieces are all read).
+      const cudaError_t e = cudaEventSynchronize(stg.ev[s]);
+      if (e != cudaSuccess) {
+        std::lock_guard<std::mutex> l(mu);
+        stop = true;
+        cuda_bad = e;
+        cv.notify_all();
+        return;
+      }
+    }
+    // Read this piece's blocks and check the ones the host checks.
+    const int64_t base = h0.data_offset + a * h0.array_stride;
+    const int64_t b0 = u.blk_lo + (p - first[(size_t)i]) * piece_blocks;
+    const int64_t b1 = std::min(u.blk_hi, b0 + piece_blocks);
+    const int64_t off = b0 * B, len = std::min(b1 * B, ob) - off;
+    unsigned char* dst = stg.buf[s] + (off - u.blk_lo * B);
+    bool read_ok = pread_full(files[(size_t)u.k].fd, dst, len, base + off);
+    int64_t bad = -1;
+    for (int64_t b = b0; read_ok && b < b1 && bad < 0; ++b) {
+      if (!host_check[ui][(size_t)(b - u.blk_lo)]) continue;
+      const int64_t l = std::min(B, ob - b * B);
+      if (host_hash(dst + (b - b0) * B, l, b, B, (uint32_t)a) !=
+          tables[(size_t)u.k][(size_t)(a * onb + b)])
+        bad = b;
+    }
+    std::lock_guard<std::mutex> l(mu);
+    if (!read_ok || bad >= 0) {
+      if (!stop) {
+        io_bad = !read_ok;
+        bad_block = bad;
+        bad_k = u.k;
+        bad_a = a;
+      }
+      stop = true;
+      cv.notify_all();
+      return;
+    }
+    if (--left[(size_t)i] > 0 || stop) return;
+    while (next_issue < items && left[(size_t)next_issue] == 0) {
+      const cudaError_t e = issue(next_issue);
+      if (e != cudaSuccess) {
+        stop = true;
+        cuda_bad = e;
+        break;
+      }
+      issued[(size_t)next_issue] = 1;
+      ++next_issue;
+    }
+    cv.notify_all();
+  });
+  // Items without pieces (none in practice) are issued here.
+  while (!stop && next_issue < items) {
+    const cudaError_t e = issue(next_issue++);
+    if (e != cudaSuccess) {
+      stop = true;
+      cuda_bad = e;
+    }
+  }
+  if (stop) {
+    if (device) cudaStreamSynchronize(stream);
+    if (io_bad) return zs::fail(ZS_ERR_IO, "%s: reading %s failed", fn, paths[bad_k]);
+    if (bad_block >= 0)
+      return zs::fail(ZS_ERR_CORRUPT, "%s: %s: %s block %lld checksum mismatch (the state "
+                      "arrays now hold partial data)", fn, paths[bad_k], kArrayName[bad_a],
+                      (long long)bad_block);
+    return cuda_fail(fn, "copy to device", cuda_bad);
   }
   if (device) {
     const cudaError_t e = cudaStreamSynchronize(stream);
@@ -1037,4 +1153,22 @@ extern "C" zs_status zs_checkpoint_load(const zs_plan* plan, int32_t rank,
                                                    exp_avg_sq, &saved, cuda_stream);
   if (st == ZS_OK && step) *step = saved;
   return zs::traced(st, "zs_checkpoint_load", plan, rank, 0, 0, -1, -1, saved);
+}
+
+extern "C" zs_status zs_checkpoint_release_staging(void) {
+  zs::clear_error();
+  StagingCache& c = staging_cache();
+  std::lock_guard<std::mutex> l(c.mu);
+  cudaError_t first = cudaSuccess;
+  for (int s = 0; s < kSlots; ++s) {
+    if (!c.buf[s]) continue;
+    const cudaError_t e = cudaFreeHost(c.buf[s]);
+    if (first == cudaSuccess) first = e;
+    c.buf[s] = nullptr;
+  }
+  c.bytes = 0;
+  c.dev = -1;
+  if (first != cudaSuccess)
+    return zs::fail(ZS_ERR_CUDA, "zs_checkpoint_release_staging: %s", cudaGetErrorString(first));
+  return ZS_OK;
 }

@@ -17,8 +17,8 @@
  *   - Returns zs_status: 0 on success, a negative code on error. No call
  *     aborts or exits; zs_last_error() gives a one-line detail (per thread).
  *   - Device buffers and CUDA streams are owned by the caller. The library
- *     allocates host memory for plans (and staging inside the checkpoint
- *     calls); it never allocates device memory.
+ *     allocates host memory for plans and pinned staging for the checkpoint
+ *     calls (kept for the next one); it never allocates device memory.
  *   - Calls that take a stream enqueue work on it and return without
  *     synchronising (but for the checkpoint calls, which block); `cuda_stream`
  *     is a cudaStream_t (NULL = legacy default).
@@ -380,8 +380,10 @@ zs_status zs_shard_rows(const zs_plan* plan, int32_t rank, const void* const* pa
  *
  * State arrays are all device memory (current device, 16-byte aligned) or
  * all host memory. Device-resident state moves through pinned host staging
- * (these calls allocate pinned host memory for their duration and no device
- * memory); saving hashes the blocks on the device, and so does loading for
+ * (three 64 MiB buffers; no device memory is allocated). The first call on
+ * device state allocates the staging and the library keeps one set for the
+ * next call on the same device, until zs_checkpoint_release_staging; saving
+ * hashes the blocks on the device, and so does loading for
  * every block that lands whole in the device arrays. Both calls block until
  * done, enqueueing their device work on `cuda_stream` and synchronising it.
  * Not thread-safe for one path. Errors: ZS_ERR_IO (open/read/write),
@@ -406,6 +408,9 @@ zs_status zs_checkpoint_save(const zs_plan* plan, int32_t rank, const float* mas
 zs_status zs_checkpoint_load(const zs_plan* plan, int32_t rank, const char* const* paths,
                              int32_t n_paths, float* master, float* exp_avg, float* exp_avg_sq,
                              int64_t* step, void* cuda_stream);
+/* Frees the pinned staging the checkpoint calls keep between calls (none
+ * kept: nothing to do). Not to be called while a checkpoint call runs. */
+zs_status zs_checkpoint_release_staging(void);
 /* The header of a checkpoint file, checked (any output may be NULL). layout:
  * 0 flat, 1 rows. */
 zs_status zs_checkpoint_info(const char* path, int32_t* world, int32_t* rank, int32_t* layout,

@@ -234,3 +234,36 @@ def test_device_argument_errors(tmp_path):
     # so it is not repeated here.)
     assert not os.path.exists(str(tmp_path / "x"))
     plan.free()
+
+
+def test_staging_kept_and_released(tmp_path):
+    """The pinned staging one call leaves for the next: repeated saves and
+    restores through the kept set, a release, and a restore that allocates
+    again all give the same bytes; releasing with nothing kept is a no-op.
+    The state spans several 64 MiB staging units so that every slot is used."""
+    zs.zs_checkpoint_release_staging()
+    zs.zs_checkpoint_release_staging()
+    S0 = 3 * (1 << 24) + 4096          # 3 arrays x ~201 MB: many staging items, no padding
+    plan = zs.zs_flatten_plan([2 * S0], world=2, align_elems=128)
+    S = plan.S
+    assert S == S0
+    rng = np.random.default_rng(77)
+    src = [torch.from_numpy(rng.integers(0, 2 ** 32, size=S, dtype=np.uint32).view(np.int32))
+           .to(DEV) for _ in range(3)]
+    path = str(tmp_path / "r1")
+    for rep in range(3):
+        zs.zs_checkpoint_save(plan, 1, *src, 40 + rep, path)
+        if rep == 1:
+            zs.zs_checkpoint_release_staging()
+        dst = [torch.zeros(S, dtype=torch.int32, device=DEV) for _ in range(3)]
+        paths = [None, path]
+        # rank 1 of the same world reads only old rank 1's file; paths[0] must
+        # still name a file of the old world: save rank 0 as well
+        zs.zs_checkpoint_save(plan, 0, *src, 40 + rep, str(tmp_path / "r0"))
+        paths[0] = str(tmp_path / "r0")
+        assert zs.zs_checkpoint_load(plan, 1, paths, *dst) == 40 + rep
+        for a, b in zip(src, dst):
+            assert torch.equal(a, b)
+        del dst
+    zs.zs_checkpoint_release_staging()
+    plan.free()
