@@ -69,12 +69,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 template <int GW, bool BF16G, int MAXN>
 cudaError_t launch_acc(const ShardStepLaunch& in, int first, cudaStream_t stream) {
-  static int max_blocks_by_dev[64];
+  static std::atomic<int> max_blocks_by_dev[64];
   auto kernel = accumulate_kernel<GW, BF16G, MAXN>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int& max_blocks = max_blocks_by_dev[dev & 63];
+  int max_blocks = max_blocks_by_dev[dev & 63].load(std::memory_order_relaxed);
   if (max_blocks == 0) {
     int sms = 0, per_sm = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -82,6 +82,7 @@ cudaError_t launch_acc(const ShardStepLaunch& in, int first, cudaStream_t stream
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
     if (e != cudaSuccess) return e;
     max_blocks = 2 * sms * (per_sm > 0 ? per_sm : 1);
+    max_blocks_by_dev[dev & 63].store(max_blocks, std::memory_order_relaxed);
   }
   StepArgs<MAXN> a;
   for (int j = 0; j < MAXN; ++j) a.grads[j] = j < in.world ? in.grads[j] : nullptr;

@@ -67,14 +67,15 @@ cudaError_t launch_wait_timeout(uint32_t polls, cudaStream_t stream) {
 }
 
 unsigned int* device_error_word() {
-  static unsigned int* by_dev[64];
+  static std::atomic<unsigned int*> by_dev[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  unsigned int*& w = by_dev[dev & 63];
+  unsigned int* w = by_dev[dev & 63].load(std::memory_order_acquire);
   if (!w) {
     void* addr = nullptr;
     if (cudaGetSymbolAddress(&addr, g_error_word) != cudaSuccess) return nullptr;
     w = static_cast<unsigned int*>(addr);
+    by_dev[dev & 63].store(w, std::memory_order_release);
   }
   return w;
 }

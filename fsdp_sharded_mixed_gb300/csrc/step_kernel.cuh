@@ -8,6 +8,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "bounds.cuh"
 #include "zs_internal.h"
 
@@ -568,14 +571,21 @@ cudaError_t launch_staged(const ShardStepLaunch& in, uint32_t stage_bytes, int s
                           int blocks_per_sm, int sms, cudaStream_t stream) {
   auto kernel = staged_step_kernel<BF16G, PD, ACC>;
   const size_t smem = (size_t)stages * stage_bytes + 16 * (size_t)stages;
-  static size_t smem_set_by_dev[64];  // this instantiation's opt-in so far, per device
+  // This instantiation's shared-memory opt-in so far, per device; raised
+  // under a lock so that concurrent first calls cannot leave it recorded
+  // above what the attribute holds.
+  static std::atomic<size_t> smem_set_by_dev[64];
+  static std::mutex smem_mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (smem > smem_set_by_dev[dev & 63]) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    smem_set_by_dev[dev & 63] = smem;
+  if (smem > smem_set_by_dev[dev & 63].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(smem_mu);
+    if (smem > smem_set_by_dev[dev & 63].load(std::memory_order_relaxed)) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      smem_set_by_dev[dev & 63].store(smem, std::memory_order_release);
+    }
   }
   StagedArgs sa;
   for (int j = 0; j < in.world; ++j) sa.a.grads[j] = in.grads[j];
@@ -615,12 +625,12 @@ template <int GW, bool BF16G, int PD, int MAXN, bool ACC>
 cudaError_t launch_one(const ShardStepLaunch& in, cudaStream_t stream) {
   // Resident blocks on the whole GPU for this instantiation, per device; the
   // grid is twice that, so the tail of one wave overlaps the next.
-  static int max_blocks_by_dev[64];
+  static std::atomic<int> max_blocks_by_dev[64];
   auto kernel = shard_step_kernel<GW, BF16G, PD, MAXN, ACC>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int& max_blocks = max_blocks_by_dev[dev & 63];
+  int max_blocks = max_blocks_by_dev[dev & 63].load(std::memory_order_relaxed);
   if (max_blocks == 0) {
     int sms = 0, per_sm = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -628,6 +638,7 @@ cudaError_t launch_one(const ShardStepLaunch& in, cudaStream_t stream) {
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
     if (e != cudaSuccess) return e;
     max_blocks = 2 * sms * (per_sm > 0 ? per_sm : 1);
+    max_blocks_by_dev[dev & 63].store(max_blocks, std::memory_order_relaxed);
   }
   StepArgs<MAXN> a;
   for (int j = 0; j < in.world; ++j) a.grads[j] = in.grads[j];
@@ -669,12 +680,16 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
   for (int j = 0; j < a.world; ++j) ptrs |= (uintptr_t)a.grads[j];
   const uintptr_t slot_align = PD == kParamBf16 ? 8 : PD == kParamFp32 ? 16 : 4;
   if (ptrs % 16 != 0 || (uintptr_t)a.slot % slot_align != 0) return false;
-  static int shape_by_dev[64][2];  // smem per SM, per block (opt-in), per device
+  // Per device: shared memory per SM (0 = not looked up yet), the opt-in
+  // shared memory per block, the SM count.
+  struct Shape {
+    std::atomic<int> per_sm{0}, per_block{0}, sms{0};
+  };
+  static Shape shape_by_dev[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  int* sh = shape_by_dev[dev & 63];
-  static int sms_by_dev[64];
-  if (sh[0] == 0) {
+  Shape& sh = shape_by_dev[dev & 63];
+  if (sh.per_sm.load(std::memory_order_acquire) == 0) {
     int per_sm = 0, per_block = 0, sms = 0;
     if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
             cudaSuccess ||
@@ -684,9 +699,9 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
       cudaGetLastError();
       return false;
     }
-    sh[1] = per_block;
-    sms_by_dev[dev & 63] = sms;
-    sh[0] = per_sm;
+    sh.per_block.store(per_block, std::memory_order_relaxed);
+    sh.sms.store(sms, std::memory_order_relaxed);
+    sh.per_sm.store(per_sm, std::memory_order_release);
   }
   const uint32_t stage_bytes =
       (uint32_t)a.world * tile_grad_bytes<BF16G>() + (ACC ? 4u : 3u) * kTile * 4u;
@@ -701,10 +716,11 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
                      (a.world <= 2 && PD == kParamFp24)))
     return false;
   int stages = 0, per_sm_blocks = 0;
-  staged_shape(stage_bytes, sh[0], sh[1], &stages, &per_sm_blocks);
+  staged_shape(stage_bytes, sh.per_sm.load(std::memory_order_relaxed),
+               sh.per_block.load(std::memory_order_relaxed), &stages, &per_sm_blocks);
   if (stages == 0) return false;
   *result = launch_staged<BF16G, PD, ACC>(a, stage_bytes, stages, per_sm_blocks,
-                                          sms_by_dev[dev & 63], stream);
+                                          sh.sms.load(std::memory_order_relaxed), stream);
   return true;
 }
 
