@@ -192,13 +192,19 @@ def _check(status):
 
 
 def _ptr(x):
-    """Address of a tensor or a numpy array (or an int address / None)."""
+    """Address of a tensor or a numpy array (or an int address / None). The
+    library reads and writes buffers as dense runs of bytes, so a strided
+    view is refused rather than passed by its first element's address."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
     if hasattr(x, "data_ptr"):
+        if not x.is_contiguous():
+            raise ValueError("zs: tensor arguments must be contiguous")
         return x.data_ptr()
+    if not x.flags["C_CONTIGUOUS"]:
+        raise ValueError("zs: array arguments must be C-contiguous")
     return x.ctypes.data
 
 

@@ -184,3 +184,18 @@ def test_checked_library_exports_and_flags():
     L = zs.lib()
     assert zs.lib_path() == zs.LIB_PATH and not zs.zs_bounds_checked()
     assert L.zs_selftest_bounds_window(3) == zs.ZS_ERR_UNSUPPORTED
+
+
+def test_strided_buffers_refused():
+    """The binding passes dense buffers only: a strided view is refused before
+    the library is called."""
+    import numpy as np
+    import torch
+    plan = zs.zs_flatten_plan([1000], world=4)
+    a = np.zeros((plan.S, 2), np.float32)[:, 0]
+    with pytest.raises(ValueError):
+        zs.zs_checkpoint_save(plan, 0, a, a, a, 1, "/nonexistent/never-written", stream=0)
+    t = torch.zeros(plan.S * 2)[::2]
+    with pytest.raises(ValueError):
+        _step(plan, master=t)
+    plan.free()
