@@ -208,6 +208,41 @@ def _ptr(x):
     return x.ctypes.data
 
 
+def _nbytes(x):
+    """Byte size of a tensor or array argument; None for a raw address."""
+    if x is None or isinstance(x, int):
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.numel() * x.element_size()
+    return x.nbytes
+
+
+def _need(x, nbytes, fn, name):
+    """A tensor or array argument must hold the bytes the call touches (raw
+    addresses are the caller's responsibility; the library checks device
+    allocations where the driver can tell)."""
+    have = _nbytes(x)
+    if have is not None and have < nbytes:
+        raise ValueError(f"{fn}: {name} holds {have} bytes, the call needs {nbytes}")
+
+
+def _step_sizes(fn, plan, lo, hi, grad_slices, grad_dtype, states, out, param_dtype,
+                out_elems, accum=None):
+    """The byte sizes the step family needs: N slices of S gradient elements,
+    fp32 [S] states (and accumulator), the output of out_elems parameters."""
+    if hi <= lo:
+        return
+    S = plan.S
+    for j, g in enumerate(grad_slices):
+        _need(g, S * ELEM_BYTES[grad_dtype], fn, f"grad_slices[{j}]")
+    for name, x in zip(("master", "exp_avg", "exp_avg_sq"), states):
+        _need(x, S * 4, fn, name)
+    if out is not None:
+        _need(out, out_elems * ELEM_BYTES.get(param_dtype, 0), fn, "output")
+    if accum is not None:
+        _need(accum, S * 4, fn, "accum")
+
+
 def _stream(stream):
     if stream is None:
         import torch
@@ -314,6 +349,8 @@ def zs_shard_step(plan, rank, lo, hi, grad_slices, grad_dtype, master, exp_avg, 
     ``exp_avg_sq``: fp32 [S]; ``full_flat``: N*S elements of ``param_dtype``;
     ``hp``: dict with lr, beta1, beta2, eps, weight_decay; ``step`` >= 1.
     """
+    _step_sizes("zs_shard_step", plan, lo, hi, grad_slices, grad_dtype,
+                (master, exp_avg, exp_avg_sq), full_flat, param_dtype, plan.P_pad)
     ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
     h = AdamWHparams(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"])
     _check(lib().zs_shard_step(plan.handle, rank, lo, hi, ptrs, grad_dtype, _ptr(master),
@@ -325,6 +362,8 @@ def zs_shard_step_to_shard(plan, rank, lo, hi, grad_slices, grad_dtype, master, 
                            exp_avg_sq, param_shard, param_dtype, hp, step, stream=None):
     """``zs_shard_step`` writing the cast parameters into ``param_shard`` (S
     elements of ``param_dtype``) instead of the rank's slot of the flat buffer."""
+    _step_sizes("zs_shard_step_to_shard", plan, lo, hi, grad_slices, grad_dtype,
+                (master, exp_avg, exp_avg_sq), param_shard, param_dtype, plan.S)
     ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
     h = AdamWHparams(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"])
     _check(lib().zs_shard_step_to_shard(plan.handle, rank, lo, hi, ptrs, grad_dtype, _ptr(master),
@@ -337,6 +376,8 @@ def zs_shard_step_clipped(plan, rank, lo, hi, grad_slices, grad_dtype, master, e
                           stream=None):
     """``zs_shard_step`` with a device clip coefficient and skip flag (tensors
     or addresses of a device fp32 and a device int32; None = not used)."""
+    _step_sizes("zs_shard_step_clipped", plan, lo, hi, grad_slices, grad_dtype,
+                (master, exp_avg, exp_avg_sq), full_flat, param_dtype, plan.P_pad)
     ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
     h = AdamWHparams(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"])
     _check(lib().zs_shard_step_clipped(plan.handle, rank, lo, hi, ptrs, grad_dtype, _ptr(master),
@@ -347,6 +388,8 @@ def zs_shard_step_clipped(plan, rank, lo, hi, grad_slices, grad_dtype, master, e
 
 def zs_grad_accumulate(plan, rank, lo, hi, grad_slices, grad_dtype, accum, first, stream=None):
     """Enqueue accum = (first ? 0 : accum) + mean of the slices (fp32 [S])."""
+    _step_sizes("zs_grad_accumulate", plan, lo, hi, grad_slices, grad_dtype, (), None, 0, 0,
+                accum)
     ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
     _check(lib().zs_grad_accumulate(plan.handle, rank, lo, hi, ptrs, grad_dtype, _ptr(accum),
                                     1 if first else 0, _stream(stream)))
@@ -356,6 +399,8 @@ def zs_shard_step_accumulated(plan, rank, lo, hi, grad_slices, grad_dtype, accum
                               master, exp_avg, exp_avg_sq, full_flat, param_dtype, hp, step,
                               stream=None):
     """The step on ((accum + mean of the slices) / micro_steps)."""
+    _step_sizes("zs_shard_step_accumulated", plan, lo, hi, grad_slices, grad_dtype,
+                (master, exp_avg, exp_avg_sq), full_flat, param_dtype, plan.P_pad, accum)
     ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
     h = AdamWHparams(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"])
     _check(lib().zs_shard_step_accumulated(plan.handle, rank, lo, hi, ptrs, grad_dtype,
@@ -368,6 +413,8 @@ def zs_grad_sqnorm_accumulated(plan, rank, lo, hi, grad_slices, grad_dtype, accu
                                workspace, sqnorm_out, stream=None):
     """Enqueue the shard's sum of squares of the accumulated step's gradient
     ((accum + mean) * (1/G)) into the device double ``sqnorm_out``."""
+    _step_sizes("zs_grad_sqnorm_accumulated", plan, lo, hi, grad_slices, grad_dtype, (), None,
+                0, 0, accum)
     ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
     nbytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") \
         else zs_grad_norm_workspace_bytes()
@@ -380,6 +427,8 @@ def zs_shard_step_accumulated_clipped(plan, rank, lo, hi, grad_slices, grad_dtyp
                                       micro_steps, master, exp_avg, exp_avg_sq, full_flat,
                                       param_dtype, hp, step, coef=None, skip=None, stream=None):
     """The accumulated step with a device clip coefficient and skip flag."""
+    _step_sizes("zs_shard_step_accumulated_clipped", plan, lo, hi, grad_slices, grad_dtype,
+                (master, exp_avg, exp_avg_sq), full_flat, param_dtype, plan.P_pad, accum)
     ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
     h = AdamWHparams(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"])
     _check(lib().zs_shard_step_accumulated_clipped(
@@ -396,6 +445,7 @@ def zs_grad_sqnorm(plan, rank, lo, hi, grad_slices, grad_dtype, workspace, sqnor
                    stream=None):
     """Enqueue the shard's sum of squared mean gradients into the device
     double ``sqnorm_out``; ``workspace`` is caller-owned device scratch."""
+    _step_sizes("zs_grad_sqnorm", plan, lo, hi, grad_slices, grad_dtype, (), None, 0, 0)
     ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
     nbytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") \
         else zs_grad_norm_workspace_bytes()
@@ -408,6 +458,7 @@ def zs_grad_sqnorm_noalloc(plan, rank, lo, hi, grad_slices, grad_dtype, sqnorm_o
     """``zs_grad_sqnorm`` for callers that cannot allocate device memory: the
     scratch is the library's own static device array (see include/zs.h for
     the first-call set-up and for why overlapping calls must not be issued)."""
+    _step_sizes("zs_grad_sqnorm_noalloc", plan, lo, hi, grad_slices, grad_dtype, (), None, 0, 0)
     ptrs = (ctypes.c_void_p * max(len(grad_slices), 1))(*[_ptr(g) for g in grad_slices])
     _check(lib().zs_grad_sqnorm_noalloc(plan.handle, rank, lo, hi, ptrs, grad_dtype,
                                         _ptr(sqnorm_out), _stream(stream)))
@@ -421,6 +472,10 @@ def zs_clip_coefficient(rank_sqnorms, n, max_norm, coef_out, nonfinite_out, stre
 def zs_gather_assemble(plan, rank, shard_srcs, full_flat, param_dtype, stream=None):
     """Enqueue the assembly of the other ranks' shards into ``full_flat``;
     return the per-parameter device addresses (the unflattened views)."""
+    eb = ELEM_BYTES.get(param_dtype, 0)
+    for j, x in enumerate(shard_srcs):
+        _need(x, plan.S * eb, "zs_gather_assemble", f"shard_srcs[{j}]")
+    _need(full_flat, plan.P_pad * eb, "zs_gather_assemble", "full_flat")
     srcs = (ctypes.c_void_p * max(len(shard_srcs), 1))(*[_ptr(s) for s in shard_srcs])
     views = None if plan.rows else (ctypes.c_void_p * max(plan.n_params, 1))()
     _check(lib().zs_gather_assemble(plan.handle, rank, srcs, _ptr(full_flat), param_dtype,
@@ -443,6 +498,8 @@ def zs_checkpoint_save(plan, rank, master, exp_avg, exp_avg_sq, step, path, stre
     """Write rank ``rank``'s fp32 master/exp_avg/exp_avg_sq shard (S elements
     each; device tensors, or host tensors / numpy arrays) and the global step
     to ``path``. Blocks until the file is complete."""
+    for name, x in zip(("master", "exp_avg", "exp_avg_sq"), (master, exp_avg, exp_avg_sq)):
+        _need(x, plan.S * 4, "zs_checkpoint_save", name)
     _check(lib().zs_checkpoint_save(plan.handle, rank, _ptr(master), _ptr(exp_avg),
                                     _ptr(exp_avg_sq), step, os.fsencode(path),
                                     _io_stream(stream)))
@@ -452,6 +509,8 @@ def zs_checkpoint_load(plan, rank, paths, master, exp_avg, exp_avg_sq, stream=No
     """Fill rank ``rank``'s shard of ``plan`` from the files of the old ranks
     (``paths[k]`` = old rank k's file; None for a file this rank does not
     need, never for rank 0); returns the saved step."""
+    for name, x in zip(("master", "exp_avg", "exp_avg_sq"), (master, exp_avg, exp_avg_sq)):
+        _need(x, plan.S * 4, "zs_checkpoint_load", name)
     arr = (ctypes.c_char_p * max(len(paths), 1))(
         *[None if p is None else os.fsencode(p) for p in paths])
     step = ctypes.c_int64()

@@ -199,3 +199,22 @@ def test_strided_buffers_refused():
     with pytest.raises(ValueError):
         _step(plan, master=t)
     plan.free()
+
+
+def test_short_buffers_refused():
+    """A tensor or array shorter than the bytes a call touches is refused by
+    the binding (raw addresses go to the library, which checks device
+    allocations where the driver can tell)."""
+    import numpy as np
+    import torch
+    plan = zs.zs_flatten_plan([1000], world=4)
+    short = np.zeros(plan.S - 1, np.float32)
+    with pytest.raises(ValueError, match="master holds"):
+        zs.zs_checkpoint_save(plan, 0, short, short, short, 1, "/nonexistent/never-written",
+                              stream=0)
+    with pytest.raises(ValueError, match="grad_slices\\[2\\]"):
+        _step(plan, grad_slices=[16, 32, torch.zeros(plan.S - 1, dtype=torch.int16), 48])
+    with pytest.raises(ValueError, match="output"):
+        _step(plan, full_flat=torch.zeros(plan.P_pad - 1, dtype=torch.int16))
+    _step(plan, lo=3, hi=3, master=np.zeros(1, np.float32))   # empty range: nothing checked
+    plan.free()
