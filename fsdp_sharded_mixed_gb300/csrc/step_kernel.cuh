@@ -344,9 +344,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 // by bulk asynchronous copies (cp.async.bulk, completion counted on an
 // mbarrier): one producer thread keeps the next tiles' copies in flight while
 // 16 consumer warps compute the current one from shared memory, so loads and
-// arithmetic overlap instead of alternating per thread. A tile is 2048
-// elements, each consumer thread 4 of them; stages are reused once every
-// consumer warp has released them. On GB300 this wins where the register-
+// arithmetic overlap instead of alternating per thread. A tile is 512 × E
+// elements, each consumer thread E of them: E = 4 (2048 elements) where two
+// stages of that fit in shared memory, else E = 2 (1024), which stages up to
+// 50 bf16 or 25 fp32 slices; stages are reused once every consumer warp has
+// released them. (E = 1 was measured and left out: its 1 KB and 2 KB copies
+// per slice ran at 0.46 and 0.83 of the copy bandwidth.) On GB300 this wins where the register-
 // streaming kernel above cannot keep enough bytes in flight: short ranges,
 // many slices (32 bytes or more per element) and N <= 2 with 3-byte
 // parameters; elsewhere the kernel above is faster (the choice is in
@@ -355,15 +358,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 // waits, bounded, for its own copies before the block exits.
 constexpr int kStagedWarps = 16;                     // consumer warps
 constexpr int kStagedThreads = (kStagedWarps + 1) * 32;
-constexpr int kStagedE = 4;                          // elements per consumer thread per tile
-constexpr int kTile = kStagedWarps * 32 * kStagedE;  // 2048
-constexpr int kStagedMaxN = 16;
+constexpr int kStagedMaxN = 64;
+// Elements of a tile with E elements per consumer thread: 2048 or 1024.
+__host__ __device__ constexpr int staged_tile(int E) { return kStagedWarps * 32 * E; }
 constexpr int kStagedMaxStages = 4;
 constexpr uint32_t kWaitPolls = 1u << 21;
 
 struct StagedArgs {
   StepArgs<kStagedMaxN> a;
-  int64_t t0, t1;      // whole tiles [t0, t1): elements [t0*kTile, t1*kTile)
+  int64_t t0, t1;      // whole tiles [t0, t1): elements [t0*T, t1*T), T the tile
   int64_t rag_lo[2], rag_hi[2];  // the ragged head and tail, element by element
   int stages;
   uint32_t stage_bytes;
@@ -416,14 +419,92 @@ __device__ __forceinline__ void st_u32(void* p, uint32_t w) {
 }
 
 // Bytes of one tile of one slice.
-template <bool BF16G>
+template <bool BF16G, int E>
 __host__ __device__ constexpr uint32_t tile_grad_bytes() {
-  return kTile * (BF16G ? 2 : 4);
+  return staged_tile(E) * (BF16G ? 2 : 4);
 }
 
-template <bool BF16G, int PD, bool ACC>
+// E consecutive fp32 values from shared memory (aligned to 4E bytes).
+template <int E>
+__device__ __forceinline__ void lds_f(const float* p, float* x) {
+  static_assert(E == 4 || E == 2, "tile widths of 4 or 2 elements per thread");
+  if constexpr (E == 4) {
+    const float4 q = *reinterpret_cast<const float4*>(p);
+    x[0] = q.x;
+    x[1] = q.y;
+    x[2] = q.z;
+    x[3] = q.w;
+  } else {
+    const float2 q = *reinterpret_cast<const float2*>(p);
+    x[0] = q.x;
+    x[1] = q.y;
+  }
+}
+// Consumer c's E values of one staged slice tile, added into acc.
+template <int E, bool BF16G>
+__device__ __forceinline__ void add_slice(const unsigned char* gp, int c, float* acc) {
+  if constexpr (BF16G) {
+    if constexpr (E == 4) {
+      const uint2 w = *reinterpret_cast<const uint2*>(gp + c * 8);
+      acc[0] = __fadd_rn(acc[0], bf16_lo(w.x));
+      acc[1] = __fadd_rn(acc[1], bf16_hi(w.x));
+      acc[2] = __fadd_rn(acc[2], bf16_lo(w.y));
+      acc[3] = __fadd_rn(acc[3], bf16_hi(w.y));
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(gp + c * 4);
+      acc[0] = __fadd_rn(acc[0], bf16_lo(w));
+      acc[1] = __fadd_rn(acc[1], bf16_hi(w));
+    }
+  } else {
+    float x[E];
+    lds_f<E>(reinterpret_cast<const float*>(gp) + c * E, x);
+#pragma unroll
+    for (int k = 0; k < E; ++k) acc[k] = __fadd_rn(acc[k], x[k]);
+  }
+}
+// E fp32 values to global memory (aligned to 4E bytes).
+template <int E>
+__device__ __forceinline__ void stg_f(float* p, const float* x) {
+  if constexpr (E == 4) {
+    st16_f(p, x);
+  } else {
+    *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
+  }
+}
+// The E cast parameters of elements e0 .. e0 + E - 1 into the slot.
+template <int E, int PD>
+__device__ __forceinline__ void stg_params(unsigned char* slot, int64_t e0, const float* p) {
+  if constexpr (PD == kParamBf16) {
+    if constexpr (E == 4) {
+      const uint32_t w[2] = {pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3])};
+      st8_u(slot + 2 * e0, w);
+    } else {
+      *reinterpret_cast<uint32_t*>(slot + 2 * e0) = pack_bf16x2(p[0], p[1]);
+    }
+  } else if constexpr (PD == kParamFp32) {
+    stg_f<E>(reinterpret_cast<float*>(slot) + e0, p);
+  } else {
+    unsigned char* d = slot + 3 * e0;
+    if constexpr (E == 4) {  // 12 bytes = three little-endian words
+      const uint32_t q0 = to_fp24(p[0]), q1 = to_fp24(p[1]), q2 = to_fp24(p[2]),
+                     q3 = to_fp24(p[3]);
+      st_u32(d, q0 | (q1 << 24));
+      st_u32(d + 4, (q1 >> 8) | (q2 << 16));
+      st_u32(d + 8, (q2 >> 16) | (q3 << 8));
+    } else {  // 6 bytes = three little-endian half-words
+      const uint32_t q0 = to_fp24(p[0]), q1 = to_fp24(p[1]);
+      uint16_t* h = reinterpret_cast<uint16_t*>(d);
+      h[0] = (uint16_t)(q0 & 0xFFFFu);
+      h[1] = (uint16_t)((q0 >> 16) | ((q1 & 0xFFu) << 8));
+      h[2] = (uint16_t)(q1 >> 8);
+    }
+  }
+}
+
+template <bool BF16G, int PD, bool ACC, int E>
 __global__ void __launch_bounds__(kStagedThreads, 2)
     staged_step_kernel(const __grid_constant__ StagedArgs sa) {
+  constexpr int T = staged_tile(E);
   const StepArgs<kStagedMaxN>& a = sa.a;
   if (a.skip && *a.skip) return;  // the ranks' shared non-finite decision
   const bool clip = a.coef != nullptr;
@@ -434,8 +515,8 @@ __global__ void __launch_bounds__(kStagedThreads, 2)
   uint64_t* empty = full + NS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = a.world;
-  constexpr uint32_t gtile = tile_grad_bytes<BF16G>();
-  constexpr uint32_t stile = kTile * 4;
+  constexpr uint32_t gtile = tile_grad_bytes<BF16G, E>();
+  constexpr uint32_t stile = T * 4;
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
@@ -455,7 +536,7 @@ __global__ void __launch_bounds__(kStagedThreads, 2)
       const uint32_t use = (uint32_t)(i / NS);
       if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, sa.err)) break;
       unsigned char* st = smem + (size_t)s * sa.stage_bytes;
-      if (!within(t * kTile, (t + 1) * kTile, a.win_lo, a.win_hi, sa.err)) {
+      if (!within(t * T, (t + 1) * T, a.win_lo, a.win_hi, sa.err)) {
         mbar_expect_tx(&full[s], 0);  // checked build: the stage completes empty
         continue;
       }
@@ -464,10 +545,10 @@ __global__ void __launch_bounds__(kStagedThreads, 2)
         bulk_to_smem(st + j * gtile, static_cast<const unsigned char*>(a.grads[j]) + t * gtile,
                      gtile, &full[s]);
       unsigned char* sp = st + n * gtile;
-      bulk_to_smem(sp, a.master + t * kTile, stile, &full[s]);
-      bulk_to_smem(sp + stile, a.m + t * kTile, stile, &full[s]);
-      bulk_to_smem(sp + 2 * stile, a.v + t * kTile, stile, &full[s]);
-      if constexpr (ACC) bulk_to_smem(sp + 3 * stile, a.accum + t * kTile, stile, &full[s]);
+      bulk_to_smem(sp, a.master + t * T, stile, &full[s]);
+      bulk_to_smem(sp + stile, a.m + t * T, stile, &full[s]);
+      bulk_to_smem(sp + 2 * stile, a.v + t * T, stile, &full[s]);
+      if constexpr (ACC) bulk_to_smem(sp + 3 * stile, a.accum + t * T, stile, &full[s]);
     }
     // Every copy issued has landed before the block may exit.
     for (int64_t k = i > NS ? i - NS : 0; k < i; ++k)
@@ -489,67 +570,42 @@ __global__ void __launch_bounds__(kStagedThreads, 2)
     const int s = (int)(i % NS);
     const uint32_t use = (uint32_t)(i / NS);
     if (!mbar_wait(&full[s], use & 1u, sa.err)) return;
-    if (!within(t * kTile, (t + 1) * kTile, a.win_lo, a.win_hi, sa.err)) {
+    if (!within(t * T, (t + 1) * T, a.win_lo, a.win_hi, sa.err)) {
       __syncwarp();  // checked build: an empty stage, released untouched
       if (lane == 0) mbar_arrive(&empty[s]);
       continue;
     }
     const unsigned char* st = smem + (size_t)s * sa.stage_bytes;
-    float acc[kStagedE];
+    float acc[E];
 #pragma unroll
-    for (int k = 0; k < kStagedE; ++k) acc[k] = 0.0f;
+    for (int k = 0; k < E; ++k) acc[k] = 0.0f;
 #pragma unroll 1
-    for (int j = 0; j < n; ++j) {
-      const unsigned char* gp = st + j * gtile;
-      if constexpr (BF16G) {
-        const uint2 w = *reinterpret_cast<const uint2*>(gp + c * 8);
-        acc[0] = __fadd_rn(acc[0], bf16_lo(w.x));
-        acc[1] = __fadd_rn(acc[1], bf16_hi(w.x));
-        acc[2] = __fadd_rn(acc[2], bf16_lo(w.y));
-        acc[3] = __fadd_rn(acc[3], bf16_hi(w.y));
-      } else {
-        const float4 x = *reinterpret_cast<const float4*>(gp + c * 16);
-        acc[0] = __fadd_rn(acc[0], x.x);
-        acc[1] = __fadd_rn(acc[1], x.y);
-        acc[2] = __fadd_rn(acc[2], x.z);
-        acc[3] = __fadd_rn(acc[3], x.w);
-      }
+    for (int j = 0; j < n; ++j) add_slice<E, BF16G>(st + j * gtile, c, acc);
+    const float* sp = reinterpret_cast<const float*>(st + n * gtile) + c * E;
+    float p[E], m[E], v[E], prev[E];
+    lds_f<E>(sp, p);
+    lds_f<E>(sp + T, m);
+    lds_f<E>(sp + 2 * T, v);
+    if constexpr (ACC) {
+      lds_f<E>(sp + 3 * T, prev);
+    } else {
+#pragma unroll
+      for (int k = 0; k < E; ++k) prev[k] = 0.0f;
     }
-    const float* sp = reinterpret_cast<const float*>(st + n * gtile) + c * kStagedE;
-    const float4 p4 = *reinterpret_cast<const float4*>(sp);
-    const float4 m4 = *reinterpret_cast<const float4*>(sp + kTile);
-    const float4 v4 = *reinterpret_cast<const float4*>(sp + 2 * kTile);
-    float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if constexpr (ACC) a4 = *reinterpret_cast<const float4*>(sp + 3 * kTile);
     // The stage's next fill is written by the async proxy: order this
     // thread's reads of it before the warp releases the stage.
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    float p[4] = {p4.x, p4.y, p4.z, p4.w}, m[4] = {m4.x, m4.y, m4.z, m4.w},
-          v[4] = {v4.x, v4.y, v4.z, v4.w};
-    const float prev[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < E; ++k)
       adamw(a.s, step_grad<ACC>(acc[k], prev[k], a.s.invN, a.invG, clip, coef), p[k], m[k],
             v[k]);
-    const int64_t e0 = t * kTile + (int64_t)c * kStagedE;
-    st16_f(a.master + e0, p);
-    st16_f(a.m + e0, m);
-    st16_f(a.v + e0, v);
-    if constexpr (PD == kParamBf16) {
-      const uint32_t w[2] = {pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3])};
-      st8_u(a.slot + 2 * e0, w);
-    } else if constexpr (PD == kParamFp32) {
-      st16_f(reinterpret_cast<float*>(a.slot) + e0, p);
-    } else {
-      const uint32_t q0 = to_fp24(p[0]), q1 = to_fp24(p[1]), q2 = to_fp24(p[2]),
-                     q3 = to_fp24(p[3]);
-      unsigned char* d = a.slot + 3 * e0;  // 12 bytes = three little-endian words
-      st_u32(d, q0 | (q1 << 24));
-      st_u32(d + 4, (q1 >> 8) | (q2 << 16));
-      st_u32(d + 8, (q2 >> 16) | (q3 << 8));
-    }
+    const int64_t e0 = t * T + (int64_t)c * E;
+    stg_f<E>(a.master + e0, p);
+    stg_f<E>(a.m + e0, m);
+    stg_f<E>(a.v + e0, v);
+    stg_params<E, PD>(a.slot, e0, p);
   }
 }
 
@@ -566,10 +622,11 @@ inline void staged_shape(uint32_t stage_bytes, int smem_per_sm, int smem_per_blo
   *stages = ns >= 2 ? (int)ns : 0;
 }
 
-template <bool BF16G, int PD, bool ACC>
+template <bool BF16G, int PD, bool ACC, int E>
 cudaError_t launch_staged(const ShardStepLaunch& in, uint32_t stage_bytes, int stages,
                           int blocks_per_sm, int sms, cudaStream_t stream) {
-  auto kernel = staged_step_kernel<BF16G, PD, ACC>;
+  constexpr int T = staged_tile(E);
+  auto kernel = staged_step_kernel<BF16G, PD, ACC, E>;
   const size_t smem = (size_t)stages * stage_bytes + 16 * (size_t)stages;
   // This instantiation's shared-memory opt-in so far, per device; raised
   // under a lock so that concurrent first calls cannot leave it recorded
@@ -604,11 +661,11 @@ cudaError_t launch_staged(const ShardStepLaunch& in, uint32_t stage_bytes, int s
   sa.a.s = in.s;
   sa.a.win_lo = in.win.lo;
   sa.a.win_hi = in.win.hi;
-  sa.t0 = (in.lo + kTile - 1) / kTile;
-  sa.t1 = in.hi / kTile;
+  sa.t0 = (in.lo + T - 1) / T;
+  sa.t1 = in.hi / T;
   sa.rag_lo[0] = in.lo;
-  sa.rag_hi[0] = sa.t0 * kTile;
-  sa.rag_lo[1] = sa.t1 * kTile;
+  sa.rag_hi[0] = sa.t0 * T;
+  sa.rag_lo[1] = sa.t1 * T;
   sa.rag_hi[1] = in.hi;
   sa.stages = stages;
   sa.stage_bytes = stage_bytes;
@@ -667,19 +724,17 @@ cudaError_t launch_one(const ShardStepLaunch& in, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// The staged path where it is eligible and (path 0) measured faster: N <= 16,
-// 16-byte aligned state and slices, a slot aligned for its stores, at least 8
-// whole tiles, two stages that fit in shared memory.
+// The staged path where it is eligible and (path 0) measured faster: N <= 50,
+// 16-byte aligned state and slices, a slot aligned for its stores, two stages
+// of some tile width that fit in shared memory (the widest is taken), at least
+// 8 whole tiles of it.
 template <bool BF16G, int PD, bool ACC>
 bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* result) {
   const int path = step_path();
   if (path == 1 || a.world > kStagedMaxN) return false;
-  const int64_t tiles = a.hi / kTile - (a.lo + kTile - 1) / kTile;
-  if (tiles < 8) return false;
   uintptr_t ptrs = (uintptr_t)a.master | (uintptr_t)a.m | (uintptr_t)a.v | (uintptr_t)a.accum;
   for (int j = 0; j < a.world; ++j) ptrs |= (uintptr_t)a.grads[j];
-  const uintptr_t slot_align = PD == kParamBf16 ? 8 : PD == kParamFp32 ? 16 : 4;
-  if (ptrs % 16 != 0 || (uintptr_t)a.slot % slot_align != 0) return false;
+  if (ptrs % 16 != 0) return false;
   // Per device: shared memory per SM (0 = not looked up yet), the opt-in
   // shared memory per block, the SM count.
   struct Shape {
@@ -703,24 +758,48 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
     sh.sms.store(sms, std::memory_order_relaxed);
     sh.per_sm.store(per_sm, std::memory_order_release);
   }
-  const uint32_t stage_bytes =
-      (uint32_t)a.world * tile_grad_bytes<BF16G>() + (ACC ? 4u : 3u) * kTile * 4u;
+  // The widest tile (E = 4 or 2 elements per consumer thread) of which two
+  // stages fit.
+  int E = 0, stages = 0, per_sm_blocks = 0;
+  uint32_t stage_bytes = 0;
+  for (int e = 4; e >= 2 && E == 0; e /= 2) {
+    const uint32_t t = (uint32_t)staged_tile(e);
+    const uint32_t sb = (uint32_t)a.world * t * (BF16G ? 2u : 4u) + (ACC ? 4u : 3u) * t * 4u;
+    int st = 0, bps = 0;
+    staged_shape(sb, sh.per_sm.load(std::memory_order_relaxed),
+                 sh.per_block.load(std::memory_order_relaxed), &st, &bps);
+    if (st >= 2) {
+      E = e;
+      stages = st;
+      per_sm_blocks = bps;
+      stage_bytes = sb;
+    }
+  }
+  if (E == 0) return false;
+  const int64_t T = staged_tile(E);
+  if (a.hi / T - (a.lo + T - 1) / T < 8) return false;
+  // Each consumer thread stores its E parameters in one access.
+  const uintptr_t slot_align = PD == kParamBf16 ? 2 * E : PD == kParamFp32 ? 4 * E : E;
+  if ((uintptr_t)a.slot % slot_align != 0) return false;
   // The per-call choice, from the GB300 sweep (S x N x dtypes, both kernels)
   // and the accumulated step: the staged kernel is faster for ranges under
   // 2^24 elements, where the slices bring 32 bytes or more per element (N >= 16
   // bf16, N >= 8 fp32), and at N <= 2 with 3-byte parameters; the register-
   // streaming kernel elsewhere (including N = 8 bf16 with the accumulator:
-  // 1.026 vs 0.956 on Llama-7B).
+  // 1.026 vs 0.956 on Llama-7B). 1024-element tiles pay with fp32 slices
+  // (4 KB copies per slice: N = 16 at 2^22..2^28 elements 0.92 / 1.03 / 1.04 /
+  // 1.05 against 0.78 / 0.97 / 1.01 / 1.02; N = 12 at 2^24 1.005 vs 0.983) but
+  // not with bf16 slices (2 KB copies: N = 24..48 at 2^24 0.89-0.91 against
+  // 0.95-0.97), where they run only when forced.
   const int slice_bytes = a.world * (BF16G ? 2 : 4);
-  if (path == 0 && !(a.hi - a.lo < (int64_t(1) << 24) || slice_bytes >= 32 ||
-                     (a.world <= 2 && PD == kParamFp24)))
-    return false;
-  int stages = 0, per_sm_blocks = 0;
-  staged_shape(stage_bytes, sh.per_sm.load(std::memory_order_relaxed),
-               sh.per_block.load(std::memory_order_relaxed), &stages, &per_sm_blocks);
-  if (stages == 0) return false;
-  *result = launch_staged<BF16G, PD, ACC>(a, stage_bytes, stages, per_sm_blocks,
-                                          sh.sms.load(std::memory_order_relaxed), stream);
+  const bool wide_rule = a.hi - a.lo < (int64_t(1) << 24) || slice_bytes >= 32 ||
+                         (a.world <= 2 && PD == kParamFp24);
+  if (path == 0 && !(E == 4 ? wide_rule : !BF16G)) return false;
+  const int sms = sh.sms.load(std::memory_order_relaxed);
+  if (E == 4)
+    *result = launch_staged<BF16G, PD, ACC, 4>(a, stage_bytes, stages, per_sm_blocks, sms, stream);
+  else
+    *result = launch_staged<BF16G, PD, ACC, 2>(a, stage_bytes, stages, per_sm_blocks, sms, stream);
   return true;
 }
 

@@ -481,9 +481,10 @@ zs_status zs_selftest_bounds_window(int64_t shrink);
  * operations in the same order (results are identical): the register-
  * streaming kernel (each thread loads its 16-element group of every slice and
  * state array straight into registers) and the staged kernel (one thread per
- * block streams 2048-element tiles of the slices and state into shared memory
- * with bulk asynchronous copies while 16 warps compute; N <= 16 only). path 0
- * (default): chosen per call by N and the range's length; 1: always the
+ * block streams 2048- or 1024-element tiles of the slices and state into
+ * shared memory with bulk asynchronous copies while 16 warps compute; where
+ * two stages fit: N <= 50 bf16 or 25 fp32 slices). path 0 (default): chosen
+ * per call by N, the slice dtype and the range's length; 1: always the
  * register-streaming kernel; 2: the staged kernel wherever it applies.
  * Returns the previous path, or -1 for an unknown path (nothing changed).
  * The pages have no counterpart: this is a choice between two GB300 kernels. */

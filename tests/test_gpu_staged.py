@@ -1,7 +1,7 @@
 """Both step kernels against the oracle: the register-streaming kernel and the
-staged kernel (bulk asynchronous copies of 2048-element tiles into shared
-memory), each forced with zs_set_step_path, on ranges long enough for the
-staged kernel (whole tiles plus ragged ends), every dtype pair, N up to 16,
+staged kernel (bulk asynchronous copies of 2048- or 1024-element tiles into
+shared memory), each forced with zs_set_step_path, on ranges long enough for
+the staged kernel (whole tiles plus ragged ends), every dtype pair, N up to 64,
 with clipping, a skipped step and gradient accumulation; guard bands around
 every buffer. The two kernels must give the oracle's bits."""
 import numpy as np
@@ -278,4 +278,68 @@ def test_step_to_shard_matches_oracle(orc, path, pdt):
     got = to_host(shard, np.uint8)
     assert np.array_equal(got, o_full[rank * S * eb:(rank + 1) * S * eb])
     assert guards_intact(shard_whole)
+    plan.free()
+
+
+@pytest.mark.parametrize("path", [2], indirect=True, ids=["staged"])
+@pytest.mark.parametrize("N,bf16", [(20, True), (32, True), (48, True), (16, False), (24, False),
+                                    (64, True), (32, False)],
+                         ids=["bf16x20-tile2048", "bf16x32-tile1024", "bf16x48-tile1024",
+                              "fp32x16-tile1024", "fp32x24-tile1024", "bf16x64-unstaged",
+                              "fp32x32-unstaged"])
+@pytest.mark.parametrize("pdt", [oracle.BF16, oracle.FP24, oracle.FP32], ids=["bf16", "fp24", "fp32"])
+def test_narrow_tiles_match_oracle(orc, path, N, bf16, pdt):
+    """Many slices, the staged kernel forced: 2048-element tiles while two
+    stages of them fit in shared memory, else 1024-element tiles, else (no
+    tile fits) the register-streaming kernel; over a ragged range, the plain
+    step then a clipped accumulated step, against the oracle bit for bit with
+    guard bands."""
+    S0 = 23_000
+    plan = zs.zs_flatten_plan([N * S0], world=N, align_elems=128)
+    S, P = plan.S, plan.P
+    rank, lo, hi = N // 2, 301, S - 77
+    eb = oracle.ELEM_BYTES[pdt]
+    master0 = synth.fill(S, index0=rank * S, seed=N, stream=synth.STREAM_MASTER, sigma=0.02,
+                         p_limit=P)
+    o_st = [master0.copy(), np.zeros(S, np.float32), np.zeros(S, np.float32)]
+    o_full = np.zeros(plan.P_pad * eb, np.uint8)
+    bufs = [guarded(S * 4, x) for x in o_st]
+    full_whole, full = guarded(plan.P_pad * eb, o_full)
+    gdt = zs.ZS_BF16 if bf16 else zs.ZS_FP32
+    acc = (np.random.default_rng(N).standard_normal(S) * 1e-3).astype(np.float32)
+    acc_whole, d_acc = guarded(S * 4, acc)
+    coef = torch.tensor([0.625], dtype=torch.float32, device=DEV)
+    skip = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for t in (1, 2):
+        g_host = [synth.fill(S, index0=rank * S, seed=N, rank=j, step=t, p_limit=P, bf16=bf16)
+                  for j in range(N)]
+        g_dev = [guarded(g.nbytes, g) for g in g_host]
+        dev_slices = [g[1] for g in g_dev]
+        if t == 1:
+            zs.zs_shard_step(plan, rank, lo, hi, dev_slices, gdt, *[b[1] for b in bufs], full,
+                             ZS_OF[pdt], HP, t)
+            orc.shard_step(world=N, rank=rank, S=S, lo=lo, hi=hi, grads=g_host, master=o_st[0],
+                           m=o_st[1], v=o_st[2], full_flat=o_full, param_dtype=pdt, t=t,
+                           **oracle_hp(HP))
+        else:
+            zs.zs_shard_step_accumulated_clipped(plan, rank, lo, hi, dev_slices, gdt, d_acc, 3,
+                                                 *[b[1] for b in bufs], full, ZS_OF[pdt], HP, t,
+                                                 coef=coef, skip=skip)
+            orc.shard_step_accumulated_clipped(world=N, rank=rank, S=S, lo=lo, hi=hi,
+                                               grads=g_host, accum=acc, micro_steps=3,
+                                               master=o_st[0], m=o_st[1], v=o_st[2],
+                                               full_flat=o_full, coef=np.float32(0.625), skip=0,
+                                               param_dtype=pdt, t=t, **oracle_hp(HP))
+        zs.zs_check_device_error()
+        for name, (whole, inner), ref in zip(("master", "m", "v"), bufs, o_st):
+            got = to_host(inner, np.float32)
+            assert assert_state_close(got, ref, name) == 0, name
+            assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), name
+            assert guards_intact(whole), name
+        got = to_host(full, np.uint8)
+        assert assert_params_close(got, o_full, pdt) == 0
+        assert np.array_equal(got, o_full)
+        assert guards_intact(full_whole) and guards_intact(acc_whole)
+        for whole, _ in g_dev:
+            assert guards_intact(whole)
     plan.free()
