@@ -726,8 +726,10 @@ def run_ours(args, w):
 def run_sweep(args):
     """--pipeline sweep: the shard step over a grid of shard sizes S x emulated
     ranks N x incoming-gradient dtype x parameter dtype (one tensor of N*S
-    elements, rank 0's step), 20 timed steps per point with state carried
-    forward, per-step CUDA events; points whose buffers do not fit in free
+    elements, rank 0's step), 20 steps per point with state carried forward,
+    captured in a CUDA graph and timed over 5 replays (CUDA events around each
+    replay; the per-step time is a replay's over 20); points whose buffers do
+    not fit in free
     device memory are reported as skipped, points whose working set fits in
     L2 are marked cache-resident (not roofline points)."""
     import torch
@@ -746,7 +748,7 @@ def run_sweep(args):
     peak, peak_kind = measured_peak()
     hp = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
     pdt_of = {2: zs.ZS_BF16, 3: zs.ZS_FP24, 4: zs.ZS_FP32}
-    warm, reps = max(3, min(args.warmup, 5)), 20
+    warm, reps, replays = max(3, min(args.warmup, 5)), 20, 5
     sizes = [S for S in SWEEP_SHARD_SIZES if S <= (1 << args.sweep_max_log2)]
     only = None
     if args.sweep_only:
@@ -783,22 +785,41 @@ def run_sweep(args):
                     v = torch.zeros(S, dtype=torch.float32, device=dev)
                     full = torch.zeros(N * S * pb, dtype=torch.uint8, device=dev)
                     gdt = zs.ZS_BF16 if gb == 2 else zs.ZS_FP32
-                    ev = [(torch.cuda.Event(enable_timing=True),
-                           torch.cuda.Event(enable_timing=True)) for _ in range(warm + reps)]
+                    # Warm-up launches (they also make the first-call set-up),
+                    # then `reps` steps captured in a CUDA graph, replayed
+                    # `replays` times: the per-step time is a replay's time /
+                    # reps, free of host launch overhead (at 2^22 elements a
+                    # step is ~25 us, less than a launch from Python costs).
+                    side = torch.cuda.Stream()
+                    side.wait_stream(torch.cuda.current_stream())
+                    with torch.cuda.stream(side):
+                        for t in range(1, warm + 1):
+                            zs.zs_shard_step(plan, 0, 0, S, grads, gdt, master, m, v, full,
+                                             pdt_of[pb], hp, t, stream=side.cuda_stream)
                     torch.cuda.synchronize()
-                    for t, (a, b) in enumerate(ev, start=1):
+                    graph = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(graph, stream=side):
+                        for t in range(warm + 1, warm + reps + 1):
+                            zs.zs_shard_step(plan, 0, 0, S, grads, gdt, master, m, v, full,
+                                             pdt_of[pb], hp, t, stream=side.cuda_stream)
+                    graph.replay()
+                    torch.cuda.synchronize()
+                    ts = []
+                    for _ in range(replays):
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+                            enable_timing=True)
                         a.record()
-                        zs.zs_shard_step(plan, 0, 0, S, grads, gdt, master, m, v, full,
-                                         pdt_of[pb], hp, t, stream=sptr)
+                        graph.replay()
                         b.record()
-                    torch.cuda.synchronize()
-                    launches += reps
-                    ts = sorted(a.elapsed_time(b) for a, b in ev[warm:])
+                        torch.cuda.synchronize()
+                        ts.append(a.elapsed_time(b) / reps)
+                    del graph
+                    launches += reps * (replays + 1)
+                    ts.sort()
                     med = statistics.median(ts)
                     gbs = pt["bytes_per_elem"] * S / med / 1e6
-                    pt.update({"ms_median": med, "ms_p10": ts[len(ts) // 10],
-                               "ms_p90": ts[(9 * len(ts)) // 10], "gbs": gbs,
-                               "frac": gbs / peak})
+                    pt.update({"ms_median": med, "ms_min": ts[0], "ms_max": ts[-1],
+                               "gbs": gbs, "frac": gbs / peak})
                     if need < 129e6:
                         pt["cache_resident"] = True
                     points.append(pt)
@@ -816,6 +837,7 @@ def run_sweep(args):
         "config": {"workload": "sweep: one tensor of N*S elements, rank 0's step",
                    "pipeline": "sweep", "step_path": args.step_path, "shard_sizes": sizes, "worlds": SWEEP_WORLDS,
                    "grad_bytes": SWEEP_GRAD_BYTES, "param_bytes": SWEEP_PARAM_BYTES,
+                   "timing": "20 steps in a CUDA graph, 5 timed replays per point",
                    "l2": "points under 129 MB of buffers are cache-resident, not roofline points"},
         "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s",
                      "frac": None if value is None else value / peak, "peak_source": peak_kind,

@@ -208,22 +208,16 @@ def _ptr(x):
     return x.ctypes.data
 
 
-def _nbytes(x):
-    """Byte size of a tensor or array argument; None for a raw address."""
-    if x is None or isinstance(x, int):
-        return None
-    if hasattr(x, "data_ptr"):
-        return x.numel() * x.element_size()
-    return x.nbytes
-
-
-def _need(x, nbytes, fn, name):
+def _need(x, nbytes, fn, name, index=None):
     """A tensor or array argument must hold the bytes the call touches (raw
     addresses are the caller's responsibility; the library checks device
     allocations where the driver can tell)."""
-    have = _nbytes(x)
-    if have is not None and have < nbytes:
-        raise ValueError(f"{fn}: {name} holds {have} bytes, the call needs {nbytes}")
+    if x is None or isinstance(x, int):
+        return
+    have = x.nbytes  # torch.Tensor and numpy.ndarray alike
+    if have < nbytes:
+        label = name if index is None else f"{name}[{index}]"
+        raise ValueError(f"{fn}: {label} holds {have} bytes, the call needs {nbytes}")
 
 
 def _step_sizes(fn, plan, lo, hi, grad_slices, grad_dtype, states, out, param_dtype,
@@ -233,8 +227,9 @@ def _step_sizes(fn, plan, lo, hi, grad_slices, grad_dtype, states, out, param_dt
     if hi <= lo:
         return
     S = plan.S
+    gbytes = S * ELEM_BYTES[grad_dtype]
     for j, g in enumerate(grad_slices):
-        _need(g, S * ELEM_BYTES[grad_dtype], fn, f"grad_slices[{j}]")
+        _need(g, gbytes, fn, "grad_slices", j)
     for name, x in zip(("master", "exp_avg", "exp_avg_sq"), states):
         _need(x, S * 4, fn, name)
     if out is not None:
@@ -474,7 +469,7 @@ def zs_gather_assemble(plan, rank, shard_srcs, full_flat, param_dtype, stream=No
     return the per-parameter device addresses (the unflattened views)."""
     eb = ELEM_BYTES.get(param_dtype, 0)
     for j, x in enumerate(shard_srcs):
-        _need(x, plan.S * eb, "zs_gather_assemble", f"shard_srcs[{j}]")
+        _need(x, plan.S * eb, "zs_gather_assemble", "shard_srcs", j)
     _need(full_flat, plan.P_pad * eb, "zs_gather_assemble", "full_flat")
     srcs = (ctypes.c_void_p * max(len(shard_srcs), 1))(*[_ptr(s) for s in shard_srcs])
     views = None if plan.rows else (ctypes.c_void_p * max(plan.n_params, 1))()
