@@ -65,9 +65,10 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def emulated_rank(global_rank, n_ranks):
-    """The data-parallel rank whose shard step GPU `global_rank` runs."""
-    return global_rank % n_ranks
+def emulated_rank(global_rank, n_ranks, first=0):
+    """The data-parallel rank whose shard step GPU `global_rank` runs (GPU 0
+    runs rank `first`)."""
+    return (global_rank + first) % n_ranks
 
 
 def max_over_ranks(value, device=None):
@@ -299,9 +300,17 @@ def run_ours(args, w):
     sptr = stream.cuda_stream
     Ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
-    plan = zs.zs_flatten_plan(w.numels, w.tied_to, world=w.world, align_elems=w.align)
+    bucketed = args.buckets and w.bucket_elems > 0 and args.pipeline == "step"
+    plan = zs.zs_flatten_plan(w.numels, w.tied_to, world=w.world, align_elems=w.align,
+                              bucket_elems=w.bucket_elems if bucketed else 0)
     N, S, P = plan.world, plan.S, plan.P
-    r = emulated_rank(grank, N)
+    r = emulated_rank(grank, N, args.rank)
+    # --buckets: the step as the configuration's ZeRO-2 job runs it, one call
+    # per gradient bucket over this rank's part of it, in bucket order.
+    ranges = [(0, S)]
+    if bucketed:
+        ranges = [b for b in (zs.zs_plan_bucket(plan, k, r) for k in range(plan.n_buckets))
+                  if b[1] > b[0]]
     hp = w.hparams
     bpe = bytes_per_elem(N)
     norm_bpe = 2 * N  # the norm pass reads the N bf16 slices once
@@ -366,8 +375,9 @@ def run_ours(args, w):
 
     # The parts of one optimizer step: (name, enqueue(stream), algorithmic bytes/elem).
     def part_step(sp):
-        zs.zs_shard_step(plan, r, 0, S, grads, zs.ZS_BF16, master, m, v, full, zs.ZS_BF16, hp,
-                         step_no[0], stream=sp)
+        for lo, hi in ranges:
+            zs.zs_shard_step(plan, r, lo, hi, grads, zs.ZS_BF16, master, m, v, full, zs.ZS_BF16,
+                             hp, step_no[0], stream=sp)
 
     def part_norm(sp):
         zs.zs_grad_sqnorm(plan, r, 0, S, grads, zs.ZS_BF16, ws, parts.narrow(0, r, 1), stream=sp)
@@ -464,7 +474,7 @@ def run_ours(args, w):
         launches_per_step = G
     else:
         pipeline = [("shard_step_kernel", part_step, bpe)]
-        launches_per_step = 1
+        launches_per_step = len(ranges)
     pipe_bpe = sum(b for _, _, b in pipeline)
 
     def step(sp=sptr, marks=None):
@@ -697,7 +707,8 @@ def run_ours(args, w):
             "data": "synthetic", "config": dict(workload_config(w, plan),
                                                 parallelism=f"replicas{gworld}",
                                                 emulated_rank_gpu0=r, pipeline=args.pipeline,
-                                                step_path=args.step_path),
+                                                step_path=args.step_path,
+                                                bucket_calls=len(ranges)),
             "hbm_gbs": pipe_bpe * value / gworld / 1e9,
             "step_ms": {"median": statistics.median(per_step),
                         "p10": per_step[len(per_step) // 10],
@@ -1027,6 +1038,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--graph", action="store_true",
                     help="time one replay of a CUDA graph holding the K launches")
+    ap.add_argument("--rank", type=int, default=0,
+                    help="the emulated rank GPU 0 runs (GPU g runs rank + g mod N)")
+    ap.add_argument("--buckets", action="store_true",
+                    help="step pipeline: one call per gradient bucket of the workload "
+                         "(GPT-2-small: 25M-element buckets), as its ZeRO-2 job runs it")
     ap.add_argument("--pipeline",
                     choices=["step", "clip", "accum", "accum_clip", "unshard", "gather",
                              "checkpoint", "sweep"],

@@ -57,6 +57,7 @@ def test_two_rank_aggregation_gloo():
 
 def test_emulated_rank_wraps():
     assert [bench.emulated_rank(g, 4) for g in range(9)] == [0, 1, 2, 3, 0, 1, 2, 3, 0]
+    assert [bench.emulated_rank(g, 4, 3) for g in range(5)] == [3, 0, 1, 2, 3]
 
 
 def test_reference_arm_under_torchrun_two_ranks():
