@@ -28,7 +28,9 @@ Other measurements (--pipeline; the default is the step above):
     unshard     FSDP2 copy-out of every wrap unit's gathered parameters
     checkpoint  save, restore, and restore into world N/2 of one rank's state
     sweep       the step over shard sizes x N x gradient and parameter dtypes
---step-path forces either step kernel (register-streaming or staged).
+--step-path forces either step kernel (register-streaming or staged); --buckets runs the
+step as one call per gradient bucket (GPT-2-small's 25M-element buckets) and --rank picks
+the emulated rank GPU 0 runs; --graph times one CUDA-graph replay of the K steps.
 """
 from __future__ import annotations
 
