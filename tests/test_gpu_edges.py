@@ -3,7 +3,7 @@ with guard bands around every output: the largest world the ABI takes
 (N = 1024 slices, the kernels' largest parameter blocks) through the step, the
 norm pass, the accumulation and the gather; N = 1 (the mean is the slice
 itself); one-element shards, one of them all padding; an empty range; and the
-staged kernel's largest N on 2048-element tiles (16) at exactly the smallest range it takes (8 whole
+staged kernel with N = 16 bf16 slices on 2048-element tiles at exactly the smallest range it takes (8 whole
 2048-element tiles) and one element or one tile short of it."""
 import numpy as np
 import pytest
@@ -155,7 +155,7 @@ def test_empty_range_touches_nothing():
 @pytest.mark.parametrize("lo,hi", [(0, 8 * 2048), (0, 8 * 2048 - 1), (1, 8 * 2048 + 3),
                                    (2048, 10 * 2048), (5, 9 * 2048 + 7)])
 def test_staged_boundary_ranges(orc, lo, hi):
-    """N = 16 (the largest N the 2048-element tiles take) with the step path forced to
+    """N = 16 bf16 slices (2048-element tiles) with the step path forced to
     staged: exactly 8 whole tiles runs the staged kernel, one element or one
     tile fewer falls back to the register-streaming kernel; both equal the
     oracle."""
