@@ -3,8 +3,8 @@ with guard bands around every output: the largest world the ABI takes
 (N = 1024 slices, the kernels' largest parameter blocks) through the step, the
 norm pass, the accumulation and the gather; N = 1 (the mean is the slice
 itself); one-element shards, one of them all padding; an empty range; and the
-staged kernel with N = 16 bf16 slices on 2048-element tiles at exactly the smallest range it takes (8 whole
-2048-element tiles) and one element or one tile short of it."""
+staged kernel with N = 16 bf16 slices at exactly the smallest range it takes
+(8 whole 2048-element tiles) and one element or one tile short of it."""
 import numpy as np
 import pytest
 import torch
