@@ -16,6 +16,9 @@
 namespace {
 
 thread_local char g_err[512];
+// Counts this thread's calls (clear_error opens a call): allocations checked
+// once in a call are trusted for the rest of it.
+thread_local uint64_t g_call = 0;
 int32_t g_validation = 1;
 
 typedef CUresult (*PFN_addressRange)(CUdeviceptr*, size_t*, CUdeviceptr);
@@ -46,9 +49,22 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Device-resident, on the current device, and (where the driver can tell)
 // [p, p+bytes) inside one allocation.
+// Allocations already checked in this call (device memory on the current
+// device, extent known): the N slices of a ReduceScatter output usually share
+// one, so a call with many slices makes a few driver queries instead of 2N.
+struct CheckedAllocation {
+  uint64_t call;
+  uintptr_t base, end;
+};
+thread_local CheckedAllocation g_checked[4];
+thread_local int g_checked_next = 0;
+
 zs_status check_device_buffer(const void* p, int64_t bytes, const char* fn, const char* name,
                               int index) {
   if (g_validation < 1 || bytes == 0) return ZS_OK;
+  const uintptr_t lo = (uintptr_t)p, hi = lo + (uint64_t)bytes;
+  for (const CheckedAllocation& c : g_checked)
+    if (c.call == g_call && c.base <= lo && hi <= c.end) return ZS_OK;
   cudaPointerAttributes attr;
   if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
     cudaGetLastError();
@@ -73,6 +89,8 @@ zs_status check_device_buffer(const void* p, int64_t bytes, const char* fn, cons
                         "%s: %s[%d] needs %lld bytes but its allocation ends %lld bytes after it",
                         fn, name, index, (long long)bytes,
                         (long long)((uintptr_t)base + size - (uintptr_t)p));
+      g_checked[g_checked_next] = {g_call, (uintptr_t)base, (uintptr_t)base + size};
+      g_checked_next = (g_checked_next + 1) % 4;
     }
   }
   return ZS_OK;
@@ -118,7 +136,10 @@ zs_status fail(zs_status st, const char* fmt, ...) {
   return st;
 }
 
-void clear_error() { g_err[0] = '\0'; }
+void clear_error() {
+  g_err[0] = '\0';
+  ++g_call;
+}
 
 int elem_bytes(zs_dtype dt) {
   switch (dt) {

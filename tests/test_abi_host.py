@@ -218,3 +218,24 @@ def test_short_buffers_refused():
         _step(plan, full_flat=torch.zeros(plan.P_pad - 1, dtype=torch.int16))
     _step(plan, lo=3, hi=3, master=np.zeros(1, np.float32))   # empty range: nothing checked
     plan.free()
+
+
+def test_buffers_marshalled_once():
+    """zs.Buffers holds a slice list's addresses in a C array, checked once:
+    accepted wherever a list of slices is, and a short one is still refused."""
+    import torch
+    plan = zs.zs_flatten_plan([1000], world=4)
+    addrs = [16 * (j + 1) * 4096 for j in range(4)]
+    b = zs.Buffers(addrs)
+    assert len(b) == 4 and b.min_nbytes is None and list(b.array) == addrs
+    with pytest.raises(zs.ZsError) as e:
+        _step(plan, grad_slices=b, rank=4)          # reaches the library: rank out of range
+    assert e.value.status == zs.ZS_ERR_RANGE
+    short = zs.Buffers([torch.zeros(plan.S, dtype=torch.int16) for _ in range(3)] +
+                       [torch.zeros(plan.S - 1, dtype=torch.int16)])
+    assert short.min_nbytes == (plan.S - 1) * 2
+    with pytest.raises(ValueError, match="gradient slice holds"):
+        _step(plan, grad_slices=short)
+    with pytest.raises(ValueError):
+        zs.Buffers([torch.zeros(2 * plan.S, dtype=torch.int16)[::2]])
+    plan.free()

@@ -164,3 +164,25 @@ def test_staged_boundary_ranges(orc, lo, hi):
     assert plan.S == 10 * 2048
     _step_case(orc, plan, 9, lo, hi, seed=31, path=zs.STEP_PATH_STAGED)
     plan.free()
+
+
+def test_buffers_same_as_list():
+    """Slices passed as a zs.Buffers (marshalled once) give the same bits as
+    the same slices passed as a list, for the step and the gather."""
+    N = 64
+    plan = zs.zs_flatten_plan([N * 5000], world=N, align_elems=16)
+    S = plan.S
+    g = [to_dev(synth.fill(S, seed=33, rank=j, step=1, bf16=True)) for j in range(N)]
+    outs = []
+    for slices in (g, zs.Buffers(g)):
+        st = [to_dev(synth.fill(S, seed=33, stream=synth.STREAM_MASTER, sigma=0.02)),
+              torch.zeros(S, device=DEV), torch.zeros(S, device=DEV)]
+        full = torch.zeros(plan.P_pad, dtype=torch.int16, device=DEV)
+        for t in (1, 2):
+            zs.zs_shard_step(plan, 3, 0, S, slices, zs.ZS_BF16, *st, full, zs.ZS_BF16, HP, t)
+        gathered = torch.zeros(plan.P_pad, dtype=torch.int16, device=DEV)
+        zs.zs_gather_assemble(plan, 0, slices, gathered, zs.ZS_BF16)
+        torch.cuda.synchronize()
+        outs.append([x.cpu().numpy().tobytes() for x in st + [full, gathered]])
+    assert outs[0] == outs[1]
+    plan.free()
