@@ -342,14 +342,17 @@ __global__ void __launch_bounds__(kThreads, 2)
 // ---- the staged path ------------------------------------------------------------
 // The same step with the N slices and the state tile staged in shared memory
 // by bulk asynchronous copies (cp.async.bulk, completion counted on an
-// mbarrier): one producer thread keeps the next tiles' copies in flight while
+// mbarrier): one producer warp keeps the next tiles' copies in flight (its
+// lanes issue them in parallel: one thread issuing 35 copies of 2 KB per stage
+// held N = 32 bf16 slices to 0.89 of the copy bandwidth, 32 lanes 0.98) while
 // 16 consumer warps compute the current one from shared memory, so loads and
 // arithmetic overlap instead of alternating per thread. A tile is 512 × E
 // elements, each consumer thread E of them: E = 4 (2048 elements) where two
 // stages of that fit in shared memory, else E = 2 (1024), which stages up to
 // 50 bf16 or 25 fp32 slices; stages are reused once every consumer warp has
-// released them. (E = 1 was measured and left out: its 1 KB and 2 KB copies
-// per slice ran at 0.46 and 0.83 of the copy bandwidth.) On GB300 this wins where the register-
+// released them. (E = 1 was measured and left out: with 1 KB and 2 KB copies
+// per slice it ran at 0.59 and 0.94-0.96 of the copy bandwidth for N = 64 bf16
+// and N = 32 fp32 slices, where the register-streaming kernel runs at 0.98-1.03.) On GB300 this wins where the register-
 // streaming kernel above cannot keep enough bytes in flight: short ranges,
 // many slices (32 bytes or more per element) and N <= 2 with 3-byte
 // parameters; elsewhere the kernel above is faster (the choice is in
@@ -527,32 +530,40 @@ __global__ void __launch_bounds__(kStagedThreads, 2)
   __syncthreads();
 
   if (warp == kStagedWarps) {
-    // The producer: one thread arms each stage with the tile's byte count and
-    // issues the N + 3 (+1) bulk copies into it.
-    if (lane != 0) return;
+    // The producer warp: lane 0 waits for a stage to be free and arms it with
+    // the tile's byte count; then the warp's lanes issue its N + 3 (+1) bulk
+    // copies, copy k by lane k % 32.
+    const int ncopies = n + (ACC ? 4 : 3);
     int64_t i = 0;
     for (int64_t t = sa.t0 + blockIdx.x; t < sa.t1; t += gridDim.x, ++i) {
       const int s = (int)(i % NS);
       const uint32_t use = (uint32_t)(i / NS);
-      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, sa.err)) break;
+      int ok = 1;
+      if (lane == 0 && use > 0) ok = mbar_wait(&empty[s], (use - 1) & 1u, sa.err) ? 1 : 0;
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
       unsigned char* st = smem + (size_t)s * sa.stage_bytes;
       if (!within(t * T, (t + 1) * T, a.win_lo, a.win_hi, sa.err)) {
-        mbar_expect_tx(&full[s], 0);  // checked build: the stage completes empty
+        if (lane == 0) mbar_expect_tx(&full[s], 0);  // checked build: the stage completes empty
+        __syncwarp();
         continue;
       }
-      mbar_expect_tx(&full[s], sa.stage_bytes);
-      for (int j = 0; j < n; ++j)
-        bulk_to_smem(st + j * gtile, static_cast<const unsigned char*>(a.grads[j]) + t * gtile,
-                     gtile, &full[s]);
-      unsigned char* sp = st + n * gtile;
-      bulk_to_smem(sp, a.master + t * T, stile, &full[s]);
-      bulk_to_smem(sp + stile, a.m + t * T, stile, &full[s]);
-      bulk_to_smem(sp + 2 * stile, a.v + t * T, stile, &full[s]);
-      if constexpr (ACC) bulk_to_smem(sp + 3 * stile, a.accum + t * T, stile, &full[s]);
+      if (lane == 0) mbar_expect_tx(&full[s], sa.stage_bytes);
+      __syncwarp();  // the stage is armed before any of its copies is issued
+      for (int k = lane; k < ncopies; k += 32) {
+        if (k < n) {
+          bulk_to_smem(st + k * gtile, static_cast<const unsigned char*>(a.grads[k]) + t * gtile,
+                       gtile, &full[s]);
+        } else {
+          const int q = k - n;
+          const float* src = q == 0 ? a.master : q == 1 ? a.m : q == 2 ? a.v : a.accum;
+          bulk_to_smem(st + n * gtile + q * stile, src + t * T, stile, &full[s]);
+        }
+      }
     }
     // Every copy issued has landed before the block may exit.
-    for (int64_t k = i > NS ? i - NS : 0; k < i; ++k)
-      mbar_wait(&full[k % NS], (uint32_t)(k / NS) & 1u, sa.err);
+    if (lane == 0)
+      for (int64_t k = i > NS ? i - NS : 0; k < i; ++k)
+        mbar_wait(&full[k % NS], (uint32_t)(k / NS) & 1u, sa.err);
     return;
   }
 
@@ -786,15 +797,17 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
   // 2^24 elements, where the slices bring 32 bytes or more per element (N >= 16
   // bf16, N >= 8 fp32), and at N <= 2 with 3-byte parameters; the register-
   // streaming kernel elsewhere (including N = 8 bf16 with the accumulator:
-  // 1.026 vs 0.956 on Llama-7B). 1024-element tiles pay with fp32 slices
-  // (4 KB copies per slice: N = 16 at 2^22..2^28 elements 0.92 / 1.03 / 1.04 /
-  // 1.05 against 0.78 / 0.97 / 1.01 / 1.02; N = 12 at 2^24 1.005 vs 0.983) but
-  // not with bf16 slices (2 KB copies: N = 24..48 at 2^24 0.89-0.91 against
-  // 0.95-0.97), where they run only when forced.
+  // 1.026 vs 0.956 on Llama-7B). 1024-element tiles: with fp32 slices (4 KB
+  // copies) at every size (N = 16 at 2^22..2^28 elements 0.92 / 1.04 / 1.04 /
+  // 1.05 against 0.78 / 0.97 / 1.01 / 1.02; N = 20 at 2^26 1.048 vs 1.021);
+  // with bf16 slices (2 KB copies) for ranges under 2^25 (N = 24 / 32 / 48 at
+  // 2^24: 1.01 / 0.98 / 1.01 against 0.94 / 0.96 / 0.97), not above (N = 32 at
+  // 2^26 and 2^28: 1.00 against 1.02 and 1.03).
   const int slice_bytes = a.world * (BF16G ? 2 : 4);
   const bool wide_rule = a.hi - a.lo < (int64_t(1) << 24) || slice_bytes >= 32 ||
                          (a.world <= 2 && PD == kParamFp24);
-  if (path == 0 && !(E == 4 ? wide_rule : !BF16G)) return false;
+  const bool narrow_rule = !BF16G || a.hi - a.lo < (int64_t(1) << 25);
+  if (path == 0 && !(E == 4 ? wide_rule : narrow_rule)) return false;
   const int sms = sh.sms.load(std::memory_order_relaxed);
   if (E == 4)
     *result = launch_staged<BF16G, PD, ACC, 4>(a, stage_bytes, stages, per_sm_blocks, sms, stream);
