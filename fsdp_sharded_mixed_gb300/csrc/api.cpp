@@ -109,6 +109,42 @@ zs_status check_overlaps(const std::vector<Range>& rs, const char* fn) {
   return ZS_OK;
 }
 
+// The plan, rank and shard-local range [lo, hi) of a call on a rank's shard.
+zs_status check_call(const char* fn, const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi) {
+  if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
+  if (rank < 0 || rank >= plan->world)
+    return zs::fail(ZS_ERR_RANGE, "%s: rank %d not in [0, %d)", fn, rank, plan->world);
+  if (lo < 0 || hi < lo || hi > plan->S)
+    return zs::fail(ZS_ERR_RANGE, "%s: [lo, hi) = [%lld, %lld) not inside [0, %lld)", fn,
+                    (long long)lo, (long long)hi, (long long)plan->S);
+  return ZS_OK;
+}
+
+// The N incoming slices of S elements of gb bytes: non-NULL and 16-byte
+// aligned; their byte ranges go to `ranges` for the overlap check, and
+// *all32 is cleared unless every one is 32-byte aligned.
+zs_status check_slices(const char* fn, int32_t N, int64_t S, const void* const* grad_slices,
+                       int gb, std::vector<Range>* ranges, bool* all32) {
+  for (int32_t j = 0; j < N; ++j) {
+    const void* g = grad_slices[j];
+    if (!g) return zs::fail(ZS_ERR_INVAL, "%s: grad_slices[%d] is NULL", fn, j);
+    if (!aligned16(g))
+      return zs::fail(ZS_ERR_ALIGN, "%s: grad_slices[%d] is not 16-byte aligned", fn, j);
+    *all32 = *all32 && (uintptr_t)g % 32 == 0;
+    ranges->push_back({(uintptr_t)g, (uintptr_t)g + (uint64_t)S * gb, "grad_slices", j, false});
+  }
+  return ZS_OK;
+}
+
+// After the overlap check: each slice is device memory covering its bytes.
+zs_status check_slices_resident(const char* fn, int32_t N, int64_t S,
+                                const void* const* grad_slices, int gb) {
+  for (int32_t j = 0; j < N; ++j)
+    if (zs_status st = check_device_buffer(grad_slices[j], S * gb, fn, "grad_slices", j))
+      return st;
+  return ZS_OK;
+}
+
 // beta^t by right-to-left binary powering in IEEE double.
 double pow_binary(double base, int64_t e) {
   double r = 1.0;
@@ -161,13 +197,9 @@ zs_status shard_step_impl(const char* fn, const zs_plan* plan, int32_t rank, int
                           const float* coef, const int32_t* skip, const float* accum,
                           int32_t micro_steps, void* cuda_stream, bool shard_only = false) {
   zs::clear_error();
-  if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
+  if (zs_status st = check_call(fn, plan, rank, lo, hi)) return st;
   const int32_t N = plan->world;
   const int64_t S = plan->S;
-  if (rank < 0 || rank >= N) return zs::fail(ZS_ERR_RANGE, "%s: rank %d not in [0, %d)", fn, rank, N);
-  if (lo < 0 || hi < lo || hi > S)
-    return zs::fail(ZS_ERR_RANGE, "%s: [lo, hi) = [%lld, %lld) not inside [0, %lld)", fn,
-                    (long long)lo, (long long)hi, (long long)S);
   if (step < 1) return zs::fail(ZS_ERR_RANGE, "%s: step %lld < 1", fn, (long long)step);
   if (grad_dtype != ZS_BF16 && grad_dtype != ZS_FP32)
     return zs::fail(ZS_ERR_INVAL, "%s: gradient dtype %d is not bf16 or fp32", fn, (int)grad_dtype);
@@ -186,12 +218,8 @@ zs_status shard_step_impl(const char* fn, const zs_plan* plan, int32_t rank, int
   const int gb = grad_dtype == ZS_BF16 ? 2 : 4;
   std::vector<Range> ranges;
   ranges.reserve(N + 4);
-  for (int32_t j = 0; j < N; ++j) {
-    const void* g = grad_slices[j];
-    if (!g) return zs::fail(ZS_ERR_INVAL, "%s: grad_slices[%d] is NULL", fn, j);
-    if (!aligned16(g)) return zs::fail(ZS_ERR_ALIGN, "%s: grad_slices[%d] is not 16-byte aligned", fn, j);
-    ranges.push_back({(uintptr_t)g, (uintptr_t)g + (uint64_t)S * gb, "grad_slices", j, false});
-  }
+  bool slices32 = true;
+  if (zs_status st = check_slices(fn, N, S, grad_slices, gb, &ranges, &slices32)) return st;
   const void* outs[4] = {master, exp_avg, exp_avg_sq, full_flat};
   // full_flat: the flat buffer of all N slots, or (shard_only) the rank's own
   // parameter shard of S elements.
@@ -207,8 +235,7 @@ zs_status shard_step_impl(const char* fn, const zs_plan* plan, int32_t rank, int
     ranges.push_back({(uintptr_t)accum, (uintptr_t)accum + (uint64_t)S * 4, "accum", 0, false});
   }
   if (zs_status st = check_overlaps(ranges, fn)) return st;
-  for (int32_t j = 0; j < N; ++j)
-    if (zs_status st = check_device_buffer(grad_slices[j], S * gb, fn, "grad_slices", j)) return st;
+  if (zs_status st = check_slices_resident(fn, N, S, grad_slices, gb)) return st;
   for (int k = 0; k < 4; ++k)
     if (zs_status st = check_device_buffer(outs[k], out_bytes[k], fn, names[k], 0)) return st;
   if (accum)
@@ -229,9 +256,8 @@ zs_status shard_step_impl(const char* fn, const zs_plan* plan, int32_t rank, int
   // The widest vector path every pointer allows: 32-byte accesses need all
   // bases (and the slot's 16-element groups) 32-byte aligned; 16-byte
   // accesses need the slot's 8-element groups aligned; else element by element.
-  bool all32 = ((uintptr_t)master | (uintptr_t)exp_avg | (uintptr_t)exp_avg_sq |
-                (uintptr_t)accum) % 32 == 0;
-  for (int32_t j = 0; j < N && all32; ++j) all32 = (uintptr_t)grad_slices[j] % 32 == 0;
+  const bool all32 = slices32 && ((uintptr_t)master | (uintptr_t)exp_avg |
+                                   (uintptr_t)exp_avg_sq | (uintptr_t)accum) % 32 == 0;
   const uintptr_t slot_addr = (uintptr_t)a.slot;
   if (all32 && slot_addr % (pb == 3 ? 16u : 32u) == 0)
     a.vec_width = 16;
@@ -334,13 +360,9 @@ static zs_status zs_grad_accumulate_untraced(const zs_plan* plan, int32_t rank, 
                                         void* cuda_stream) {
   static const char* fn = "zs_grad_accumulate";
   zs::clear_error();
-  if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
+  if (zs_status st = check_call(fn, plan, rank, lo, hi)) return st;
   const int32_t N = plan->world;
   const int64_t S = plan->S;
-  if (rank < 0 || rank >= N) return zs::fail(ZS_ERR_RANGE, "%s: rank %d not in [0, %d)", fn, rank, N);
-  if (lo < 0 || hi < lo || hi > S)
-    return zs::fail(ZS_ERR_RANGE, "%s: [lo, hi) = [%lld, %lld) not inside [0, %lld)", fn,
-                    (long long)lo, (long long)hi, (long long)S);
   if (grad_dtype != ZS_BF16 && grad_dtype != ZS_FP32)
     return zs::fail(ZS_ERR_INVAL, "%s: gradient dtype %d is not bf16 or fp32", fn, (int)grad_dtype);
   if (lo == hi) return ZS_OK;
@@ -349,17 +371,10 @@ static zs_status zs_grad_accumulate_untraced(const zs_plan* plan, int32_t rank, 
   const int gb = grad_dtype == ZS_BF16 ? 2 : 4;
   std::vector<Range> ranges;
   bool all32 = (uintptr_t)accum % 32 == 0;
-  for (int32_t j = 0; j < N; ++j) {
-    const void* g = grad_slices[j];
-    if (!g) return zs::fail(ZS_ERR_INVAL, "%s: grad_slices[%d] is NULL", fn, j);
-    if (!aligned16(g)) return zs::fail(ZS_ERR_ALIGN, "%s: grad_slices[%d] is not 16-byte aligned", fn, j);
-    all32 = all32 && (uintptr_t)g % 32 == 0;
-    ranges.push_back({(uintptr_t)g, (uintptr_t)g + (uint64_t)S * gb, "grad_slices", j, false});
-  }
+  if (zs_status st = check_slices(fn, N, S, grad_slices, gb, &ranges, &all32)) return st;
   ranges.push_back({(uintptr_t)accum, (uintptr_t)accum + (uint64_t)S * 4, "accum", 0, true});
   if (zs_status st = check_overlaps(ranges, fn)) return st;
-  for (int32_t j = 0; j < N; ++j)
-    if (zs_status st = check_device_buffer(grad_slices[j], S * gb, fn, "grad_slices", j)) return st;
+  if (zs_status st = check_slices_resident(fn, N, S, grad_slices, gb)) return st;
   if (zs_status st = check_device_buffer(accum, S * 4, fn, "accum", 0)) return st;
   zs::ShardStepLaunch a = {};
   a.grads = grad_slices;
@@ -391,13 +406,9 @@ zs_status sqnorm_impl(const char* fn, const zs_plan* plan, int32_t rank, int64_t
                       int32_t micro_steps, bool noalloc, void* workspace,
                       int64_t workspace_bytes, double* sqnorm_out, void* cuda_stream) {
   zs::clear_error();
-  if (!zs::plan_is_live(plan)) return zs::fail(ZS_ERR_INVAL, "%s: not a live plan", fn);
+  if (zs_status st = check_call(fn, plan, rank, lo, hi)) return st;
   const int32_t N = plan->world;
   const int64_t S = plan->S;
-  if (rank < 0 || rank >= N) return zs::fail(ZS_ERR_RANGE, "%s: rank %d not in [0, %d)", fn, rank, N);
-  if (lo < 0 || hi < lo || hi > S)
-    return zs::fail(ZS_ERR_RANGE, "%s: [lo, hi) = [%lld, %lld) not inside [0, %lld)", fn,
-                    (long long)lo, (long long)hi, (long long)S);
   if (grad_dtype != ZS_BF16 && grad_dtype != ZS_FP32)
     return zs::fail(ZS_ERR_INVAL, "%s: gradient dtype %d is not bf16 or fp32", fn, (int)grad_dtype);
   if (noalloc) {
@@ -417,13 +428,8 @@ zs_status sqnorm_impl(const char* fn, const zs_plan* plan, int32_t rank, int64_t
   const int gb = grad_dtype == ZS_BF16 ? 2 : 4;
   std::vector<Range> ranges;
   bool all32 = true;
-  for (int32_t j = 0; j < N && hi > lo; ++j) {
-    const void* g = grad_slices[j];
-    if (!g) return zs::fail(ZS_ERR_INVAL, "%s: grad_slices[%d] is NULL", fn, j);
-    if (!aligned16(g)) return zs::fail(ZS_ERR_ALIGN, "%s: grad_slices[%d] is not 16-byte aligned", fn, j);
-    all32 = all32 && (uintptr_t)g % 32 == 0;
-    ranges.push_back({(uintptr_t)g, (uintptr_t)g + (uint64_t)S * gb, "grad_slices", j, false});
-  }
+  if (hi > lo)
+    if (zs_status st = check_slices(fn, N, S, grad_slices, gb, &ranges, &all32)) return st;
   if (accum && hi > lo) {
     if (!aligned16(accum)) return zs::fail(ZS_ERR_ALIGN, "%s: accum is not 16-byte aligned", fn);
     all32 = all32 && (uintptr_t)accum % 32 == 0;
@@ -438,8 +444,8 @@ zs_status sqnorm_impl(const char* fn, const zs_plan* plan, int32_t rank, int64_t
   if (!noalloc)
     if (zs_status st = check_device_buffer(workspace, zs::kNormWorkspaceBytes, fn, "workspace", 0))
       return st;
-  for (int32_t j = 0; j < N && hi > lo; ++j)
-    if (zs_status st = check_device_buffer(grad_slices[j], S * gb, fn, "grad_slices", j)) return st;
+  if (hi > lo)
+    if (zs_status st = check_slices_resident(fn, N, S, grad_slices, gb)) return st;
   if (accum && hi > lo)
     if (zs_status st = check_device_buffer(accum, S * 4, fn, "accum", 0)) return st;
   zs::NormLaunch a = {};
