@@ -24,6 +24,7 @@ PDT = {2: (zs.ZS_BF16, oracle.BF16), 3: (zs.ZS_FP24, oracle.FP24), 4: (zs.ZS_FP3
     (1 << 24, 64, 2, 4),     # the widest world, fp32 parameters
     (1 << 28, 2, 2, 3),
     (1 << 22, 8, 4, 2),
+    (1 << 24, 16, 4, 3),     # fp32 slices on 1024-element tiles (the per-call choice)
     (1 << 10, 4, 2, 2),      # the smallest point
 ])
 def test_sweep_point_sampled(orc, S, N, gb, pb):
