@@ -155,6 +155,7 @@ EXPORTS = {
     "zs_check_device_error": ([_P], ctypes.c_int),
     "zs_set_validation": ([_I32], _I32),
     "zs_set_step_path": ([_I32], _I32),
+    "zs_last_step_kernel": ([_P, _P], ctypes.c_int),
     "zs_selftest_wait_timeout": ([ctypes.c_uint32, _P], ctypes.c_int),
     "zs_bounds_checked": ([], _I32),
     "zs_selftest_bounds_window": ([_I64], ctypes.c_int),
@@ -614,6 +615,15 @@ def zs_set_step_path(path):
     if old < 0:
         raise ValueError(f"unknown step path {path}")
     return old
+
+
+def zs_last_step_kernel():
+    """(kernel, elems) of the calling thread's last step-family launch: (1, 16 /
+    8 / 0) register-streaming with that vector group, (2, 2048 / 1024) staged
+    with that tile; (0, 0) before the first."""
+    k, e = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib().zs_last_step_kernel(ctypes.byref(k), ctypes.byref(e)))
+    return k.value, e.value
 
 
 def zs_version():

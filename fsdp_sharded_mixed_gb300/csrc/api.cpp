@@ -411,12 +411,11 @@ zs_status sqnorm_impl(const char* fn, const zs_plan* plan, int32_t rank, int64_t
   const int64_t S = plan->S;
   if (grad_dtype != ZS_BF16 && grad_dtype != ZS_FP32)
     return zs::fail(ZS_ERR_INVAL, "%s: gradient dtype %d is not bf16 or fp32", fn, (int)grad_dtype);
-  if (noalloc) {
-    // The scratch this call needs must fit the library's static array.
-    if (zs::kNormWorkspaceBytes > zs::kNoAllocScratchBytes)
-      return zs::fail(ZS_ERR_RANGE, "%s: needs %lld bytes of scratch, the static array holds %lld",
-                      fn, (long long)zs::kNormWorkspaceBytes, (long long)zs::kNoAllocScratchBytes);
-  } else {
+  // The scratch one norm pass needs does not depend on the input's size, and
+  // the library's static array holds it.
+  static_assert(zs::kNormWorkspaceBytes <= zs::kNoAllocScratchBytes,
+                "the no-alloc norm pass's scratch must fit its static array");
+  if (!noalloc) {
     if (!workspace || workspace_bytes < zs::kNormWorkspaceBytes)
       return zs::fail(ZS_ERR_RANGE, "%s: workspace must hold %lld bytes", fn,
                       (long long)zs::kNormWorkspaceBytes);
@@ -792,6 +791,25 @@ extern "C" zs_status zs_selftest_wait_timeout(uint32_t polls, void* cuda_stream)
 extern "C" int32_t zs_set_step_path(int32_t path) {
   if (path < 0 || path > 2) return -1;
   return g_step_path.exchange(path);
+}
+
+namespace {
+thread_local int32_t t_last_kernel = 0, t_last_elems = 0;
+}  // namespace
+
+namespace zs {
+void note_step_kernel(int kernel, int elems) {
+  t_last_kernel = kernel;
+  t_last_elems = elems;
+}
+}  // namespace zs
+
+extern "C" zs_status zs_last_step_kernel(int32_t* kernel, int32_t* elems) {
+  zs::clear_error();
+  if (!kernel || !elems) return zs::fail(ZS_ERR_INVAL, "zs_last_step_kernel: NULL output");
+  *kernel = t_last_kernel;
+  *elems = t_last_elems;
+  return ZS_OK;
 }
 
 extern "C" int32_t zs_set_validation(int32_t level) {

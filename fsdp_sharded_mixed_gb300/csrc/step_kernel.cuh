@@ -809,6 +809,7 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
   const bool narrow_rule = !BF16G || a.hi - a.lo < (int64_t(1) << 25);
   if (path == 0 && !(E == 4 ? wide_rule : narrow_rule)) return false;
   const int sms = sh.sms.load(std::memory_order_relaxed);
+  note_step_kernel(2, (int)T);
   if (E == 4)
     *result = launch_staged<BF16G, PD, ACC, 4>(a, stage_bytes, stages, per_sm_blocks, sms, stream);
   else
@@ -820,6 +821,7 @@ template <bool BF16G, int PD, bool ACC>
 cudaError_t dispatch(const ShardStepLaunch& a, cudaStream_t stream) {
   cudaError_t staged_result = cudaSuccess;
   if (try_staged<BF16G, PD, ACC>(a, stream, &staged_result)) return staged_result;
+  note_step_kernel(1, a.vec_width);
   if (a.vec_width == 16) {
     if (a.world <= 16) return launch_one<16, BF16G, PD, 16, ACC>(a, stream);
     return launch_one<16, BF16G, PD, ZS_MAX_WORLD, ACC>(a, stream);

@@ -164,6 +164,10 @@ class CallRange {
 // Which kernel runs the step: 0 = chosen per call, 1 = the register-streaming
 // kernel, 2 = the staged kernel wherever it is eligible (zs_set_step_path).
 int step_path();
+// Records, for zs_last_step_kernel, the kernel the calling thread's step-family
+// launch used: 1 = register-streaming (elems = vector group: 16, 8, 0),
+// 2 = staged (elems = tile elements).
+void note_step_kernel(int kernel, int elems);
 // This device's error word (device address), for kernels that report into it.
 unsigned int* device_error_word();
 // One block waiting, bounded by `polls`, on an mbarrier nothing arrives on.

@@ -230,16 +230,18 @@ zs_status zs_grad_sqnorm(const zs_plan* plan, int32_t rank, int64_t lo, int64_t 
  * after the device has run out of memory, to decide whether to skip the step
  * or to record why a rank is failing, when a cudaMalloc would itself fail.
  * This variant keeps the norm pass's scratch (1216 fp64 partials and a ticket
- * word, 9984 bytes, the most one call needs whatever the input size) in a
- * static device array of the library, held on every GPU that loads it until
- * the process exits; a call whose scratch would not fit is refused with
- * ZS_ERR_RANGE. It calls no allocator. The caller still passes the inputs and
- * the output, as for zs_grad_sqnorm, and gets the same value. The first call on
- * a device looks the array up (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture. All calls share the one
- * array: calls that overlap on the GPU (on different streams, or from several
- * threads) race and must not be issued; calls in order on one stream are
- * safe, each clearing what must start at zero. */
+ * word, 9984 bytes: what one call needs whatever the input size, so every
+ * call fits; the library is built only if the array holds it) in a static
+ * device array of the library, held on every GPU that loads it until the
+ * process exits. It calls no allocator. The caller still passes the inputs and
+ * the output, as for zs_grad_sqnorm, and gets the same value, bit for bit. The
+ * first call on a device looks the array up (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture. The address
+ * is kept for the life of the process: do not use the library across a
+ * cudaDeviceReset. All calls share the one array: calls that overlap on the
+ * GPU (on different streams, or from several threads) race and must not be
+ * issued; calls in order on one stream are safe, each clearing what must
+ * start at zero. */
 zs_status zs_grad_sqnorm_noalloc(const zs_plan* plan, int32_t rank, int64_t lo, int64_t hi,
                                  const void* const* grad_slices, zs_dtype grad_dtype,
                                  double* sqnorm_out, void* cuda_stream);
@@ -458,7 +460,10 @@ const char* zs_last_error(void);
 /* Synchronises `cuda_stream`, then reads and clears this device's error word
  * (set by the bounds-checked build's checks and by bounded waits);
  * ZS_ERR_TIMEOUT or ZS_ERR_RANGE if it was set, ZS_ERR_CUDA if the stream
- * reports an error. */
+ * reports an error. The library looks the addresses of its device arrays
+ * (this error word, the no-alloc norm scratch) up once per device and keeps
+ * them for the life of the process: it is not to be used across a
+ * cudaDeviceReset of a device it has used. */
 zs_status zs_check_device_error(void* cuda_stream);
 /* The bounds-checked build. The library also exists as libzs_checked.so: the
  * same host code, and kernels that check, before each global access or bulk
@@ -489,6 +494,16 @@ zs_status zs_selftest_bounds_window(int64_t shrink);
  * Returns the previous path, or -1 for an unknown path (nothing changed).
  * The pages have no counterpart: this is a choice between two GB300 kernels. */
 int32_t zs_set_step_path(int32_t path);
+/* Which kernel ran the calling thread's last step-family launch (zs_shard_step
+ * and its clipped, accumulated and to-shard forms): *kernel = 1 for the
+ * register-streaming kernel, with *elems = the elements of one thread's vector
+ * group (16: 32-byte accesses, 8: 16-byte accesses, 0: element by element);
+ * *kernel = 2 for the staged kernel, with *elems = the elements of one tile
+ * (2048 or 1024). *kernel = 0 and *elems = 0 before the thread's first launch.
+ * A call that launches nothing (an empty range, an error) leaves the record as
+ * it was. For tests that must know which code path a call took; the pages
+ * have no counterpart. ZS_ERR_INVAL for NULL outputs. */
+zs_status zs_last_step_kernel(int32_t* kernel, int32_t* elems);
 /* Failure detection without a fault: enqueues one block that waits, through
  * the same bounded mbarrier wait the staged step kernel uses, on a barrier
  * nothing arrives on, giving up after `polls` polls (1..2^20). The wait then

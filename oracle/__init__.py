@@ -110,6 +110,8 @@ def load(path=LIB_PATH):
     L.oracle_bf16_rne_array.restype = None
     L.oracle_bf16_rne_bits_range.argtypes = [ctypes.c_uint32, _I64, _P]
     L.oracle_bf16_rne_bits_range.restype = None
+    L.oracle_fp24_rne_bits_range.argtypes = [ctypes.c_uint32, _I64, _P]
+    L.oracle_fp24_rne_bits_range.restype = None
     return L
 
 
@@ -348,6 +350,13 @@ class Oracle:
     def bf16_bits_range(self, first, n):
         out = np.empty(n, dtype=np.uint16)
         self.L.oracle_bf16_rne_bits_range(first, n, out.ctypes.data)
+        return out
+
+    def fp24_bits_range(self, first, n):
+        """3 bytes per value (little-endian) of the patterns first .. first+n-1
+        (mod 2^32) cast to the 3-byte parameter type."""
+        out = np.empty(3 * n, dtype=np.uint8)
+        self.L.oracle_fp24_rne_bits_range(first & 0xFFFFFFFF, n, out.ctypes.data)
         return out
 
     def fp24(self, x):

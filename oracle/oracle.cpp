@@ -663,5 +663,15 @@ void oracle_bf16_rne_bits_range(uint32_t first, int64_t n, uint16_t* out) {
   for (int64_t i = 0; i < n; ++i)
     out[i] = (uint16_t)round_keep_high(bits_float(first + (uint32_t)i), 16);
 }
+/* The 3-byte cast of the fp32 patterns first, first + 1, ... (mod 2^32),
+ * stored as the parameter slot stores it: 3 bytes per value, little-endian. */
+void oracle_fp24_rne_bits_range(uint32_t first, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) {
+    uint32_t q = round_keep_high(bits_float(first + (uint32_t)i), 8);
+    out[3 * i] = (uint8_t)(q & 0xFFu);
+    out[3 * i + 1] = (uint8_t)((q >> 8) & 0xFFu);
+    out[3 * i + 2] = (uint8_t)((q >> 16) & 0xFFu);
+  }
+}
 
 }  // extern "C"

@@ -3,6 +3,15 @@
  * the definition). Fills are split over POSIX threads; every element depends
  * only on its own counter key, so the result does not depend on the split.
  * Compiled with -O2 -ffp-contract=off.
+ *
+ * Contiguous fills run SYN_LANES elements in lockstep: the first attempt of
+ * the polar method, its logarithm and square root for all lanes at once
+ * (independent chains the compiler can interleave and vectorise, and no
+ * data-dependent branch), then the rare lanes whose first pair was rejected
+ * continue one by one with attempt 1 of the scalar definition. Every lane
+ * performs exactly the IEEE operations of synth.h in the same order, so the
+ * values are the definition's bits; gathers at arbitrary indices use the
+ * scalar definition directly, and the tests compare the two.
  */
 #include <pthread.h>
 #include <stdint.h>
@@ -19,9 +28,96 @@ typedef struct {
   int64_t begin, end;
 } syn_job;
 
+#define SYN_LANES 16
+
+/* The key prefix shared by every index of one (seed, stream, step, rank):
+ * syn_key(seed, stream, step, rank, index) = mix64(prefix + G + index). */
+static uint64_t syn_prefix(uint64_t seed, uint64_t stream, uint64_t step, uint64_t rank) {
+  uint64_t h = syn_mix64(seed + SYN_GOLDEN * (stream + 1u));
+  h = syn_mix64(h + SYN_GOLDEN + step);
+  return syn_mix64(h + SYN_GOLDEN + rank);
+}
+
+/* The polar method from attempt a0 on (synth.h's syn_normal, resumed). */
+static double syn_normal_from(uint64_t key, uint64_t a0) {
+  for (uint64_t a = a0; a < SYN_MAX_ATTEMPTS; ++a) {
+    double u = syn_unit(syn_mix64(key + (2u * a + 1u) * SYN_GOLDEN));
+    double v = syn_unit(syn_mix64(key + (2u * a + 2u) * SYN_GOLDEN));
+    double s = u * u + v * v;
+    if (s > 0.0 && s < 1.0) return u * sqrt((-2.0 * syn_log(s)) / s);
+  }
+  return 0.0;
+}
+
+/* SYN_LANES values at global indices first .. first + SYN_LANES - 1. */
+static void syn_lanes(const syn_params* q, uint64_t pre, uint64_t pre_out, int64_t first,
+                      void* out, int bf16) {
+  double u[SYN_LANES], s[SYN_LANES], m[SYN_LANES], e[SYN_LANES], t[SYN_LANES],
+      t2[SYN_LANES], h[SYN_LANES], x[SYN_LANES];
+  uint64_t key[SYN_LANES];
+  int ok[SYN_LANES];
+  for (int k = 0; k < SYN_LANES; ++k) {
+    key[k] = syn_mix64(pre + SYN_GOLDEN + (uint64_t)(first + k));
+    u[k] = syn_unit(syn_mix64(key[k] + SYN_GOLDEN));
+    double v = syn_unit(syn_mix64(key[k] + 2u * SYN_GOLDEN));
+    s[k] = u[k] * u[k] + v * v;
+    ok[k] = s[k] > 0.0 && s[k] < 1.0;
+    if (!ok[k]) s[k] = 0.5; /* any value in range; the lane is redone below */
+  }
+  /* syn_log on every lane: the same operations, the branch as a select. */
+  for (int k = 0; k < SYN_LANES; ++k) {
+    uint64_t b;
+    memcpy(&b, &s[k], sizeof b);
+    int64_t ex = (int64_t)((b >> 52) & 0x7FFu) - 1023;
+    b = (b & 0x000FFFFFFFFFFFFFull) | 0x3FF0000000000000ull;
+    double mm;
+    memcpy(&mm, &b, sizeof mm);
+    int big = mm > 1.4142135623730951;
+    m[k] = big ? mm * 0.5 : mm;
+    e[k] = (double)(big ? ex + 1 : ex);
+  }
+  for (int k = 0; k < SYN_LANES; ++k) {
+    t[k] = (m[k] - 1.0) / (m[k] + 1.0);
+    t2[k] = t[k] * t[k];
+    h[k] = 1.0 / 25.0;
+  }
+  for (int c = 11; c >= 0; --c) {
+    const double inv = 1.0 / (double)(2 * c + 1);
+    for (int k = 0; k < SYN_LANES; ++k) h[k] = h[k] * t2[k] + inv;
+  }
+  for (int k = 0; k < SYN_LANES; ++k) {
+    double lg = (2.0 * t[k]) * h[k] + e[k] * 0.69314718055994530942;
+    x[k] = u[k] * sqrt((-2.0 * lg) / s[k]);
+  }
+  for (int k = 0; k < SYN_LANES; ++k) {
+    const int64_t index = first + k;
+    float val = 0.0f;
+    if (index < q->p_limit && index >= 0) {
+      double r = q->sigma * (ok[k] ? x[k] : syn_normal_from(key[k], 1u));
+      if (q->outlier_thr != 0u &&
+          syn_mix64(pre_out + SYN_GOLDEN + (uint64_t)index) < q->outlier_thr)
+        r = r * q->outlier_scale;
+      val = (float)r;
+    }
+    if (bf16)
+      ((uint16_t*)out)[k] = syn_to_bf16(val);
+    else
+      ((float*)out)[k] = val;
+  }
+}
+
 static void* syn_worker(void* arg) {
   syn_job* j = (syn_job*)arg;
-  for (int64_t i = j->begin; i < j->end; ++i) {
+  int64_t i = j->begin;
+  if (!j->idx) {
+    const uint64_t pre = syn_prefix(j->q.seed, j->q.stream, j->q.step, j->q.rank);
+    const uint64_t pre_out = syn_prefix(j->q.seed, SYN_STREAM_OUTLIER, j->q.step, j->q.rank);
+    const size_t eb = j->bf16 ? 2 : 4;
+    for (; i + SYN_LANES <= j->end; i += SYN_LANES)
+      syn_lanes(&j->q, pre, pre_out, j->index0 + i, (unsigned char*)j->out + eb * (size_t)i,
+                j->bf16);
+  }
+  for (; i < j->end; ++i) {
     int64_t index = j->idx ? j->idx[i] : j->index0 + i;
     float x = syn_value(&j->q, index);
     if (j->bf16)

@@ -26,6 +26,26 @@ def test_streams_steps_ranks_differ():
         assert not np.array_equal(a, synth.fill(1000, **kw))
 
 
+def test_lockstep_fill_equals_scalar_definition():
+    """Contiguous fills run 16 elements in lockstep; gathers at arbitrary
+    indices run the definition one element at a time. Both give the same bits,
+    for both streams, with outliers, across the tail pad and a ragged end."""
+    rng = np.random.default_rng(11)
+    for trial in range(12):
+        n = int(rng.integers(1, 40_000))
+        index0 = int(rng.integers(0, 1 << 40))
+        p_limit = index0 + int(rng.integers(0, n + 40))
+        kw = dict(seed=int(rng.integers(0, 1 << 32)), rank=int(rng.integers(0, 64)),
+                  step=int(rng.integers(1, 20)), p_limit=p_limit, bf16=bool(trial % 2),
+                  stream=synth.STREAM_GRAD if trial % 3 else synth.STREAM_MASTER,
+                  sigma=float(rng.choice([1e-3, 0.02, 1.0])))
+        if trial % 4 == 0:
+            kw.update(outlier_frac=0.01, outlier_scale=100.0)
+        a = synth.fill(n, index0=index0, threads=3, **kw)
+        b = synth.at(np.arange(index0, index0 + n), threads=2, **kw)
+        assert np.array_equal(a, b), trial
+
+
 def test_threads_do_not_change_values():
     a = synth.fill(50_000, seed=4, threads=1)
     b = synth.fill(50_000, seed=4, threads=7)
