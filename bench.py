@@ -208,23 +208,27 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ CPU oracle ----
-def oracle_sample_rate(w, plan_S, P, rank, n_elems, steps, warmup=0):
-    """Time the single-threaded oracle on the first n_elems of rank's shard.
-    Returns (elements/s, seconds, cores used)."""
+def oracle_time(w, S, P, rank, n_elems, steps, warmup=0):
+    """Time the single-threaded oracle on the first n_elems elements of rank's
+    shard (n_elems <= 0 or >= S: the whole shard), `steps` steps after `warmup`
+    untimed ones. The inputs (the N bf16 slices, the master) are made first by
+    the seeded host generator on every core, untimed; the oracle's steps run
+    on one pinned core. Returns (elements/s, timed seconds, cores used,
+    elements per step)."""
     import numpy as np
 
     import oracle
     import synth
     o = oracle.default()
     N = w.world
-    n = max(8, min(plan_S, n_elems))
+    n = S if n_elems <= 0 else max(8, min(S, n_elems))
     kw = dict(seed=w.seed, sigma=w.grad_sigma, p_limit=P, outlier_frac=w.outlier_frac,
               outlier_scale=w.outlier_scale, bf16=True)
-    grads = [synth.fill(n, index0=rank * plan_S, rank=j, step=1, **kw) for j in range(N)]
-    master = synth.fill(n, index0=rank * plan_S, seed=w.seed, stream=synth.STREAM_MASTER,
+    grads = [synth.fill(n, index0=rank * S, rank=j, step=1, **kw) for j in range(N)]
+    master = synth.fill(n, index0=rank * S, seed=w.seed, stream=synth.STREAM_MASTER,
                         sigma=w.master_sigma, p_limit=P)
     m, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
-    full = np.zeros(n * N, np.uint16)
+    slot = np.zeros(n, np.uint16)   # rank 0 of an n-element shard: the slot is [0, n)
     hp = w.hparams
     old_aff = None
     if hasattr(os, "sched_setaffinity"):
@@ -235,7 +239,7 @@ def oracle_sample_rate(w, plan_S, P, rank, n_elems, steps, warmup=0):
         for t in range(1, warmup + steps + 1):
             t0 = time.perf_counter()
             o.shard_step(world=N, rank=0, S=n, lo=0, hi=n, grads=grads, master=master, m=m,
-                         v=v, full_flat=full, lr=hp["lr"], beta1=hp["beta1"],
+                         v=v, full_flat=slot, lr=hp["lr"], beta1=hp["beta1"],
                          beta2=hp["beta2"], eps=hp["eps"], wd=hp["weight_decay"], t=t)
             if t > warmup:
                 total += time.perf_counter() - t0
@@ -250,40 +254,59 @@ def bytes_per_elem(world, grad_bytes=2, param_bytes=2):
     return grad_bytes * world + 24 + param_bytes
 
 
+def run_config(args, w, S, P, P_pad, gworld, r, n_calls):
+    """The `config` of both arms' JSON lines (the same dict for the same run)."""
+    cfg = {"workload": f"{w.key}: {w.title}", "emulated_ranks": w.world,
+           "shard_elems": S, "flat_params": P, "flat_padded": P_pad,
+           "grad_dtype": "bf16", "param_dtype": "bf16", "state_dtype": "fp32",
+           "bytes_per_elem": bytes_per_elem(w.world),
+           "l2": "no flush: each step streams >> 129 MB L2 (inputs larger than L2)",
+           "parallelism": f"replicas{gworld}", "emulated_rank_gpu0": r,
+           "pipeline": args.pipeline, "step_path": args.step_path, "bucket_calls": n_calls}
+    if args.pipeline in ("clip", "accum_clip"):
+        cfg["clip"] = True
+    if args.pipeline in ("accum", "accum_clip"):
+        cfg["micro_steps"] = max(1, args.micro_steps)
+    return cfg
+
+
 def run_reference(args, w):
-    """The reference arm: the CPU oracle, as it stands, one thread."""
+    """The reference arm: the CPU oracle, as it stands, one thread, on a
+    bounded sample of each step (the first elements of the rank's shard),
+    sized so that the warm-up and timed steps take about a minute. Only the
+    oracle and the input generator are loaded (the plan is the oracle's)."""
     rank, world_size, _ = dist_env()
     if rank != 0:
         return
-    import fsdp_sharded_mixed_gb300 as zs
-    plan = zs.zs_flatten_plan(w.numels, w.tied_to, world=w.world, align_elems=w.align)
+    import oracle
+    o = oracle.default()
+    bucketed = args.buckets and w.bucket_elems > 0 and args.pipeline == "step"
+    op = o.plan(w.numels, w.tied_to, world=w.world, align=w.align,
+                bucket_elems=w.bucket_elems if bucketed else 0)
+    S, P, P_pad = op["S"], op["P"], op["P_pad"]
+    r = emulated_rank(0, w.world, args.rank)
+    n_calls = 1
+    if bucketed:
+        n_calls = sum(1 for lo, hi in (o.shard_range(a, b, r, S) for a, b in op["buckets"])
+                      if hi > lo)
     budget_s, est_rate = 60.0, 20e6
     sample = int(budget_s * est_rate / max(1, args.steps + args.warmup))
-    sample = max(4096, min(plan.S, sample)) // 8 * 8
-    r = emulated_rank(0, w.world)
-    rate, secs, cores, n = oracle_sample_rate(w, plan.S, plan.P, r, sample, args.steps,
-                                              warmup=args.warmup)
+    sample = max(4096, min(S, sample)) // 8 * 8
+    rate, secs, cores, n = oracle_time(w, S, P, r, sample, args.steps, warmup=args.warmup)
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * secs / args.steps * plan.S / n,
+        "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": workload_config(w, plan),
+        "data": "synthetic", "config": run_config(args, w, S, P, P_pad, world_size, r, n_calls),
+        "sample_elems_per_step": n,
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"first {n:,} elements of rank {r}'s shard per step "
-                                   f"(of {plan.S:,}); ms_per_step scaled to the full shard"},
+                         "sample": f"each step: the first {n:,} elements of rank {r}'s "
+                                   f"{S:,}-element shard; ms_per_step and value are of that "
+                                   f"measured sample (not scaled to the shard)"},
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
-    plan.free()
-
-
-def workload_config(w, plan):
-    return {"workload": f"{w.key}: {w.title}", "emulated_ranks": w.world,
-            "shard_elems": plan.S, "flat_params": plan.P, "flat_padded": plan.P_pad,
-            "grad_dtype": "bf16", "param_dtype": "bf16", "state_dtype": "fp32",
-            "bytes_per_elem": bytes_per_elem(w.world),
-            "l2": "no flush: each step streams >> 129 MB L2 (inputs larger than L2)"}
 
 
 def run_ours(args, w):
@@ -639,6 +662,32 @@ def run_ours(args, w):
         torch.cuda.synchronize()
         e2e_t = max_over_ranks(a.elapsed_time(b) / 1e3, dev)
         e2e_elems = sum_over_ranks(float(S) * args.e2e_steps, dev)
+        # The host link during the leg: after the timed steps, e2e steps and
+        # plain host->device copies of the same bytes alternate, each timed
+        # alone, so that each step's host bandwidth is compared with the link
+        # as it was a moment later (the link is shared and dips periodically).
+        pair_frac, pair_e2e, pair_link = [], [], []
+        for _ in range(args.e2e_steps):
+            a, b = Ev(), Ev()
+            a.record(stream)
+            for s_ in (s_in, s_cmp, s_out):
+                s_.wait_stream(stream)
+            e2e_step()
+            for s_ in (s_in, s_cmp, s_out):
+                stream.wait_stream(s_)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ge = 2 * N * S / (a.elapsed_time(b) / 1e3) / 1e9
+            a, b = Ev(), Ev()
+            a.record(stream)
+            for hg, g in zip(h_grads, grads):
+                g.copy_(hg, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            gl = 2 * N * S / (a.elapsed_time(b) / 1e3) / 1e9
+            pair_e2e.append(ge)
+            pair_link.append(gl)
+            pair_frac.append(ge / gl)
         e2e = {"value": e2e_elems / e2e_t, "unit": UNIT, "h2d_bytes_per_step": 2 * N * S,
                "d2h_bytes_per_step": 2 * S, "steps": args.e2e_steps,
                "ms_per_step": 1e3 * e2e_t / args.e2e_steps, "chunks": nch,
@@ -646,7 +695,15 @@ def run_ours(args, w):
                "link_h2d_gbs": {"median": statistics.median(link), "min": min(link),
                                 "max": max(link),
                                 "note": "plain host->device copies of the same bytes, "
-                                        "timed just before; the host link is shared"}}
+                                        "timed just before; the host link is shared"},
+               "frac_of_link": statistics.median(pair_frac),
+               "link_during": {"pairs": len(pair_frac),
+                               "e2e_h2d_gbs_median": statistics.median(pair_e2e),
+                               "link_h2d_gbs_median": statistics.median(pair_link),
+                               "frac_min": min(pair_frac), "frac_max": max(pair_frac),
+                               "note": "one e2e step then one plain copy of its host->device "
+                                       "bytes, alternating, each timed alone; frac_of_link "
+                                       "is the median of the pairs' ratios"}}
         del h_grads, h_out
 
     # A practical ceiling beside the measured peak: a device-to-device copy
@@ -691,11 +748,15 @@ def run_ours(args, w):
                              "bytes_per_elem": b}
         cpu = None
         if not args.no_cpu_baseline and gworld == 1:
-            rate, secs, cores, n = oracle_sample_rate(w, S, P, r, args.cpu_sample_elems,
-                                                      args.cpu_steps)
+            rate, secs, cores, n = oracle_time(w, S, P, r, args.cpu_sample_elems,
+                                               args.cpu_steps)
+            what = (f"the full shard ({n:,} elements)" if n == S else
+                    f"the first {n:,} elements of the {S:,}-element shard")
             cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                   "sample": f"first {n:,} elements of rank {r}'s shard x {args.cpu_steps} "
-                             f"steps ({secs:.1f} s, 1 pinned thread)",
+                   "sample": f"rank {r}'s step on {what} x {args.cpu_steps} step(s), "
+                             f"{secs:.1f} s on 1 pinned thread; inputs made beforehand, "
+                             f"untimed",
+                   "full_step": n == S,
                    "ns_per_elem": 1e9 / rate, "algorithmic_gbs": rate * bpe / 1e9,
                    "host": host_cpu(), "nproc": os.cpu_count()}
         if copy_gbs is not None:
@@ -706,11 +767,8 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": gworld,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": dict(workload_config(w, plan),
-                                                parallelism=f"replicas{gworld}",
-                                                emulated_rank_gpu0=r, pipeline=args.pipeline,
-                                                step_path=args.step_path,
-                                                bucket_calls=len(ranges)),
+            "data": "synthetic",
+            "config": run_config(args, w, S, P, plan.P_pad, gworld, r, len(ranges)),
             "hbm_gbs": pipe_bpe * value / gworld / 1e9,
             "step_ms": {"median": statistics.median(per_step),
                         "p10": per_step[len(per_step) // 10],
@@ -722,12 +780,10 @@ def run_ours(args, w):
             "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
         }
         if clip:
-            line["config"]["clip_max_norm"] = max_norm
-        if accum_mode:
-            line["config"]["micro_steps"] = G
+            line["clip_max_norm"] = max_norm
         if args.pipeline == "unshard":
-            line["config"]["wrap_units"] = len(units)
-            line["config"]["unit_param_bytes"] = unit_bytes // 2
+            line["wrap_units"] = len(units)
+            line["unit_param_bytes"] = unit_bytes // 2
         print(json.dumps(line), flush=True)
     del grads, master, m, v, full
     plan.free()
@@ -1080,8 +1136,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-copy-ceiling", action="store_true",
                     help="skip the device-to-device copy measured beside the roofline")
-    ap.add_argument("--cpu-sample-elems", type=int, default=32 * 1024 * 1024)
-    ap.add_argument("--cpu-steps", type=int, default=8)
+    ap.add_argument("--cpu-sample-elems", type=int, default=0,
+                    help="cpu_baseline: the oracle on the first K elements of the shard "
+                         "(0 = the full shard)")
+    ap.add_argument("--cpu-steps", type=int, default=1)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -36,6 +36,16 @@ def dev_fill(n, *, bf16, **kw):
     return t
 
 
+def all_zero(t, chunk=1 << 28):
+    """True when every element of the device tensor is zero; checked a chunk at
+    a time so that no temporary the size of a large buffer is allocated."""
+    flat = t.reshape(-1)
+    for i in range(0, flat.numel(), chunk):
+        if bool(flat[i:i + chunk].any()):
+            return False
+    return True
+
+
 def assert_state_close(got, ref, name):
     """fp32 gate: max |a-b|/max(|a|,|b|) <= 1e-6 (0/0 = 0), NaN only with NaN."""
     got = np.asarray(got, np.float32)

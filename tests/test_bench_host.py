@@ -77,6 +77,37 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert line["e2e"]["h2d_bytes_per_step"] == 0
 
 
+def test_reference_arm_loads_only_the_oracle_and_generator():
+    """The reference arm sizes its sample with the oracle's own plan: the CUDA
+    path's library is never loaded, and its config is the dict the GPU arm
+    prints for the same run; ms_per_step is the measured sample's."""
+    code = ("import json, sys; sys.argv = ['bench.py', '--impl', 'reference', '--steps', '3', "
+            "'--warmup', '3', '--workload', 'gpt2-small', '--buckets']; import bench; "
+            "bench.main(sys.argv[1:]); "
+            "maps = open('/proc/self/maps').read(); "
+            "print('LIBS', json.dumps(sorted({l.split()[-1].rsplit('/', 1)[-1] for l in "
+            "maps.splitlines() if l.endswith('.so') and '/repo' in l or 'libzs' in l "
+            "or 'liboracle' in l})))")
+    p = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                       timeout=600, cwd=ROOT)
+    assert p.returncode == 0, p.stderr[-2000:]
+    line = json.loads(next(x for x in p.stdout.splitlines() if x.startswith("{")))
+    libs = json.loads(next(x for x in p.stdout.splitlines() if x.startswith("LIBS"))[5:])
+    assert "liboracle.so" in libs and not any(x.startswith("libzs.") or
+                                               x.startswith("libzs_checked") for x in libs), libs
+    from synth.workloads import WORKLOADS
+    import oracle
+    w = WORKLOADS["gpt2-small"]
+    op = oracle.default().plan(w.numels, w.tied_to, world=w.world, align=w.align,
+                               bucket_elems=w.bucket_elems)
+    args = bench.argparse.Namespace(pipeline="step", step_path="auto", micro_steps=4)
+    # rank 0's shard lies inside one bucket (the one holding wte): one call
+    want = bench.run_config(args, w, op["S"], op["P"], op["P_pad"], 1, 0, 1)
+    assert line["config"] == want
+    n = line["sample_elems_per_step"]
+    assert abs(line["value"] * line["ms_per_step"] / 1e3 - n) <= 1e-6 * n
+
+
 def test_traffic_summary_matches_kernel_sha(tmp_path, monkeypatch):
     f = tmp_path / "traffic.txt"
     sha = bench.kernel_sha()

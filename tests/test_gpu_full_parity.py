@@ -29,7 +29,8 @@ import fsdp_sharded_mixed_gb300 as zs
 import oracle
 import synth
 from full_parity import bitwise_check, oracle_chunks
-from gpu_util import DEV, assert_params_close, assert_state_close, dev_fill, oracle_hp
+from gpu_util import (DEV, all_zero, assert_params_close, assert_state_close, dev_fill,
+                      oracle_hp)
 from synth.workloads import GPT2_SMALL, LLAMA_7B, QWEN25_3B, SWEEP_WORLDS
 
 pytestmark = [
@@ -72,8 +73,8 @@ def _flat_workload(orc, w, rank, steps):
     g_master, g_m, g_v = _host(d_master, np.float32), _host(d_m, np.float32), _host(d_v, np.float32)
     g_slot = _host(d_full.narrow(0, rank * S, S), np.uint8)
     # The other ranks' slots are untouched.
-    assert int(d_full.narrow(0, 0, rank * S).count_nonzero()) == 0
-    assert int(d_full.narrow(0, (rank + 1) * S, P_pad - (rank + 1) * S).count_nonzero()) == 0
+    assert all_zero(d_full.narrow(0, 0, rank * S))
+    assert all_zero(d_full.narrow(0, (rank + 1) * S, P_pad - (rank + 1) * S))
     del d_master, d_m, d_v, d_full
     torch.cuda.empty_cache()
     check = bitwise_check(g_master, g_m, g_v, {oracle.BF16: g_slot})
@@ -194,7 +195,7 @@ def _sweep_point(N, S, gb, steps, together=True):
         for (zdt, odt), st, full in zip(pdts, states, fulls):
             host_states.append(tuple(_host(x, np.float32) for x in st))
             eb = oracle.ELEM_BYTES[odt]
-            assert int(full[S * eb:].count_nonzero()) == 0, "another rank's slot was written"
+            assert all_zero(full[S * eb:]), "another rank's slot was written"
             slots[odt] = _host(full[:S * eb], np.uint8)
         del states, fulls
         torch.cuda.empty_cache()
