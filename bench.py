@@ -666,7 +666,7 @@ def run_ours(args, w):
         # plain host->device copies of the same bytes alternate, each timed
         # alone, so that each step's host bandwidth is compared with the link
         # as it was a moment later (the link is shared and dips periodically).
-        pair_frac, pair_e2e, pair_link = [], [], []
+        pair_frac, pair_e2e, pair_link, t_e2e, t_link = [], [], [], 0.0, 0.0
         for _ in range(args.e2e_steps):
             a, b = Ev(), Ev()
             a.record(stream)
@@ -677,6 +677,7 @@ def run_ours(args, w):
                 stream.wait_stream(s_)
             b.record(stream)
             torch.cuda.synchronize()
+            t_e2e += a.elapsed_time(b) / 1e3
             ge = 2 * N * S / (a.elapsed_time(b) / 1e3) / 1e9
             a, b = Ev(), Ev()
             a.record(stream)
@@ -684,6 +685,7 @@ def run_ours(args, w):
                 g.copy_(hg, non_blocking=True)
             b.record(stream)
             torch.cuda.synchronize()
+            t_link += a.elapsed_time(b) / 1e3
             gl = 2 * N * S / (a.elapsed_time(b) / 1e3) / 1e9
             pair_e2e.append(ge)
             pair_link.append(gl)
@@ -696,14 +698,16 @@ def run_ours(args, w):
                                 "max": max(link),
                                 "note": "plain host->device copies of the same bytes, "
                                         "timed just before; the host link is shared"},
-               "frac_of_link": statistics.median(pair_frac),
+               "frac_of_link": t_link / t_e2e,
                "link_during": {"pairs": len(pair_frac),
-                               "e2e_h2d_gbs_median": statistics.median(pair_e2e),
-                               "link_h2d_gbs_median": statistics.median(pair_link),
-                               "frac_min": min(pair_frac), "frac_max": max(pair_frac),
+                               "e2e_h2d_gbs": 2 * N * S * len(pair_frac) / t_e2e / 1e9,
+                               "link_h2d_gbs": 2 * N * S * len(pair_frac) / t_link / 1e9,
+                               "pair_frac_median": statistics.median(pair_frac),
+                               "pair_frac_min": min(pair_frac), "pair_frac_max": max(pair_frac),
                                "note": "one e2e step then one plain copy of its host->device "
-                                       "bytes, alternating, each timed alone; frac_of_link "
-                                       "is the median of the pairs' ratios"}}
+                                       "bytes, alternating, each timed alone; frac_of_link = "
+                                       "the e2e steps' host->device GB/s over the plain "
+                                       "copies' GB/s across all pairs"}}
         del h_grads, h_out
 
     # A practical ceiling beside the measured peak: a device-to-device copy
