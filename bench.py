@@ -262,7 +262,8 @@ def run_config(args, w, S, P, P_pad, gworld, r, n_calls):
            "bytes_per_elem": bytes_per_elem(w.world),
            "l2": "no flush: each step streams >> 129 MB L2 (inputs larger than L2)",
            "parallelism": f"replicas{gworld}", "emulated_rank_gpu0": r,
-           "pipeline": args.pipeline, "step_path": args.step_path, "bucket_calls": n_calls}
+           "pipeline": args.pipeline, "step_path": args.step_path, "bucket_calls": n_calls,
+           "launch_overlap": not args.no_overlap}
     if args.pipeline in ("clip", "accum_clip"):
         cfg["clip"] = True
     if args.pipeline in ("accum", "accum_clip"):
@@ -562,14 +563,36 @@ def run_ours(args, w):
         dist.barrier()
     clocks = sampler.stop()
     elapsed = t0.elapsed_time(t1) / 1e3
-    if multi and marks is None:
-        # A graph replay gives no per-part split: time each part in a separate
-        # pass of direct launches.
-        marks = [[Ev() for _ in range(nmk)] for _ in range(min(args.steps, 50))]
-        for mk in marks:
-            step(marks=mk)
-        torch.cuda.synchronize()
-    if multi:
+    split = "events around each part of direct launches"
+    if multi and graph is not None:
+        # Each part in place: CUDA graphs of the K steps' pipeline suffixes
+        # (parts k.., k = 1, 2, ...), each replayed and timed; part k's time is
+        # the difference between the suffixes from k and from k + 1, so it
+        # includes its own launches' gaps and whatever the part before it
+        # leaves in flight.
+        suffix_s = [elapsed]
+        for k in range(1, len(pipeline)):
+            g_k = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.graph(g_k, stream=side, capture_error_mode="relaxed"):
+                for _ in range(args.steps):
+                    for _, fn, _ in pipeline[k:]:
+                        fn(side.cuda_stream)
+            stream.wait_stream(side)
+            g_k.replay()
+            torch.cuda.synchronize()
+            a_ev, b_ev = Ev(), Ev()
+            a_ev.record(stream)
+            g_k.replay()
+            b_ev.record(stream)
+            torch.cuda.synchronize()
+            suffix_s.append(a_ev.elapsed_time(b_ev) / 1e3)
+            del g_k
+        suffix_s.append(0.0)
+        part_s = [(suffix_s[k] - suffix_s[k + 1]) / args.steps for k in range(len(pipeline))]
+        split = "in place: differences of CUDA-graph replays of the pipeline's suffixes"
+    elif multi:  # direct launches: the events recorded around each part
         part_s = [sum(mk[k].elapsed_time(mk[k + 1]) for mk in marks) / 1e3 / len(marks)
                   for k in range(len(pipeline))]
     else:
@@ -780,7 +803,8 @@ def run_ours(args, w):
                         "note": f"{n_spread} steps with events around each, after the timed region"},
             "timing": "cuda graph replay of the K steps" if graph is not None
                       else "K direct launches between two events",
-            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "kernels": kernels, "kernels_split": split,
+            "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
         }
         if clip:
@@ -823,6 +847,8 @@ def run_sweep(args):
     pdt_of = {2: zs.ZS_BF16, 3: zs.ZS_FP24, 4: zs.ZS_FP32}
     warm, reps, replays = max(3, min(args.warmup, 5)), 20, 5
     sizes = [S for S in SWEEP_SHARD_SIZES if S <= (1 << args.sweep_max_log2)]
+    worlds = [int(x) for x in args.sweep_worlds.split(",")] if args.sweep_worlds \
+        else SWEEP_WORLDS
     only = None
     if args.sweep_only:
         # "log2S:N:grad_bytes:param_bytes,..." selects points of the grid
@@ -833,7 +859,7 @@ def run_sweep(args):
     for S in sizes:
         torch.cuda.empty_cache()
         free = torch.cuda.mem_get_info()[0]
-        for N in SWEEP_WORLDS:
+        for N in worlds:
             for gb in SWEEP_GRAD_BYTES:
                 for pb in SWEEP_PARAM_BYTES:
                     if only is not None and (S.bit_length() - 1, N, gb, pb) not in only:
@@ -908,7 +934,9 @@ def run_sweep(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": "sweep: one tensor of N*S elements, rank 0's step",
-                   "pipeline": "sweep", "step_path": args.step_path, "shard_sizes": sizes, "worlds": SWEEP_WORLDS,
+                   "pipeline": "sweep", "step_path": args.step_path,
+                   "launch_overlap": not args.no_overlap, "shard_sizes": sizes,
+                   "worlds": worlds,
                    "grad_bytes": SWEEP_GRAD_BYTES, "param_bytes": SWEEP_PARAM_BYTES,
                    "timing": "20 steps in a CUDA graph, 5 timed replays per point",
                    "l2": "points under 129 MB of buffers are cache-resident, not roofline points"},
@@ -1127,6 +1155,9 @@ def main(argv=None):
                          "kernel (direct) or the bulk-async staged kernel where it applies")
     ap.add_argument("--sweep-max-log2", type=int, default=30,
                     help="--pipeline sweep: largest shard size 2^k")
+    ap.add_argument("--sweep-worlds", default=None,
+                    help="--pipeline sweep: emulated world sizes N (comma list; default "
+                         "2,4,8,16,64)")
     ap.add_argument("--sweep-only", default=None,
                     help="--pipeline sweep: only these points, 'log2S:N:gbytes:pbytes,...'")
     ap.add_argument("--ckpt-dir", default=None,
@@ -1134,6 +1165,8 @@ def main(argv=None):
     ap.add_argument("--ckpt-reps", type=int, default=3)
     ap.add_argument("--ckpt-cold", action="store_true",
                     help="drop the files from the page cache before each timed load")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="ordinary kernel launches (no programmatic dependent launch)")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--e2e-chunks", type=int, default=32)
     ap.add_argument("--no-e2e", action="store_true")
@@ -1152,6 +1185,9 @@ def main(argv=None):
     if args.impl != "reference" and args.step_path != "auto":
         import fsdp_sharded_mixed_gb300 as zs
         zs.zs_set_step_path({"direct": 1, "staged": 2}[args.step_path])
+    if args.impl != "reference" and args.no_overlap:
+        import fsdp_sharded_mixed_gb300 as zs
+        zs.zs_set_launch_overlap(0)
     if args.impl == "reference":
         run_reference(args, w)
     elif args.pipeline == "checkpoint":

@@ -156,6 +156,7 @@ EXPORTS = {
     "zs_set_validation": ([_I32], _I32),
     "zs_set_step_path": ([_I32], _I32),
     "zs_last_step_kernel": ([_P, _P], ctypes.c_int),
+    "zs_set_launch_overlap": ([_I32], _I32),
     "zs_selftest_wait_timeout": ([ctypes.c_uint32, _P], ctypes.c_int),
     "zs_bounds_checked": ([], _I32),
     "zs_selftest_bounds_window": ([_I64], ctypes.c_int),
@@ -614,6 +615,16 @@ def zs_set_step_path(path):
     old = lib().zs_set_step_path(path)
     if old < 0:
         raise ValueError(f"unknown step path {path}")
+    return old
+
+
+def zs_set_launch_overlap(on):
+    """1: launches may overlap the previous kernel's drain (programmatic
+    dependent launch; results unchanged), 0: ordinary launches. Returns the
+    previous setting."""
+    old = lib().zs_set_launch_overlap(int(on))
+    if old < 0:
+        raise ValueError(f"launch overlap must be 0 or 1, got {on}")
     return old
 
 

@@ -27,6 +27,7 @@ namespace {
 template <int GW, bool BF16G, int MAXN>
 __global__ void __launch_bounds__(kThreads, 2)
     accumulate_kernel(const __grid_constant__ StepArgs<MAXN> a, int first) {
+  overlap_wait();
   float* accum = const_cast<float*>(a.accum);  // the output of this kernel
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
@@ -106,8 +107,7 @@ cudaError_t launch_acc(const ShardStepLaunch& in, int first, cudaStream_t stream
   int64_t blocks = (units + kThreads - 1) / kThreads;
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
-  kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(a, first);
-  return cudaGetLastError();
+  return launch_kernel(kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a, first);
 }
 
 template <bool BF16G>

@@ -795,7 +795,17 @@ extern "C" int32_t zs_set_step_path(int32_t path) {
 
 namespace {
 thread_local int32_t t_last_kernel = 0, t_last_elems = 0;
+std::atomic<int32_t> g_launch_overlap{1};
 }  // namespace
+
+namespace zs {
+bool launch_overlap() { return g_launch_overlap.load(std::memory_order_relaxed) != 0; }
+}  // namespace zs
+
+extern "C" int32_t zs_set_launch_overlap(int32_t on) {
+  if (on != 0 && on != 1) return -1;
+  return g_launch_overlap.exchange(on);
+}
 
 namespace zs {
 void note_step_kernel(int kernel, int elems) {

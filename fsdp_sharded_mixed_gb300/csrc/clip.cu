@@ -30,6 +30,7 @@
 #include <mutex>
 
 #include "bounds.cuh"
+#include "overlap.cuh"
 #include "zs_internal.h"
 
 namespace zs {
@@ -94,6 +95,7 @@ __device__ __forceinline__ float mean_grad(const NormArgs<MAXN>& a, int64_t i) {
 // of the accumulated step's gradient (accum + mean) * (1/G).
 template <bool BF16G, bool VEC, int MAXN, bool ACC>
 __global__ void __launch_bounds__(kThreads, 2) grad_sqnorm_kernel(const __grid_constant__ NormArgs<MAXN> a) {
+  overlap_wait();
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   double sum = 0.0;
@@ -181,21 +183,35 @@ __global__ void __launch_bounds__(kThreads, 2) grad_sqnorm_kernel(const __grid_c
     last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
   }
   __syncthreads();
-  if (!last || threadIdx.x >= 32) return;
-  // The last block: lane l adds partials l, l+32, ... in order, then a tree.
+  if (!last) return;
+  // The last block adds the partials in a fixed order: thread k the partials
+  // k, k + 256, ... (all its loads in flight at once, read at L2 where the
+  // other blocks' fenced stores are), then the same shuffle tree and warp
+  // order as the block sums above.
   __threadfence();
-  const volatile double* parts = a.partials;
   double t = 0.0;
-  for (unsigned int b = threadIdx.x; b < gridDim.x; b += 32) t += parts[b];
+  double p[(kNormPartials + kThreads - 1) / kThreads];
+#pragma unroll
+  for (int k = 0; k < (kNormPartials + kThreads - 1) / kThreads; ++k) {
+    const unsigned int b = threadIdx.x + k * kThreads;
+    p[k] = b < gridDim.x ? __ldcg(a.partials + b) : 0.0;
+  }
+#pragma unroll
+  for (int k = 0; k < (kNormPartials + kThreads - 1) / kThreads; ++k) t += p[k];
   for (int off = 16; off > 0; off >>= 1) t += __shfl_down_sync(0xFFFFFFFFu, t, off);
+  if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = t;
+  __syncthreads();
   if (threadIdx.x == 0) {
-    *a.out = t;
+    double total = 0.0;
+    for (int w = 0; w < kThreads / 32; ++w) total += warp_sums[w];
+    *a.out = total;
     *a.ticket = 0u;
   }
 }
 
 __global__ void clip_coef_kernel(const double* rank_sqnorms, int n, double max_norm, float* coef,
                                  int32_t* nonfinite) {
+  overlap_wait();
   if (blockIdx.x != 0 || threadIdx.x != 0) return;
   double total = 0.0;
   for (int r = 0; r < n; ++r) total = total + rank_sqnorms[r];
@@ -205,6 +221,7 @@ __global__ void clip_coef_kernel(const double* rank_sqnorms, int n, double max_n
   *nonfinite = bad ? 1 : 0;
   *coef = bad ? 1.0f : (float)(c < 1.0 ? c : 1.0);
 }
+
 
 template <bool BF16G, bool VEC, int MAXN, bool ACC>
 cudaError_t launch_norm(const NormLaunch& in, cudaStream_t stream) {
@@ -225,8 +242,8 @@ cudaError_t launch_norm(const NormLaunch& in, cudaStream_t stream) {
   a.invG = in.invG;
   cudaError_t e = cudaMemsetAsync(in.ticket, 0, sizeof(unsigned int), stream);
   if (e != cudaSuccess) return e;
-  grad_sqnorm_kernel<BF16G, VEC, MAXN, ACC><<<kNormPartials, kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(grad_sqnorm_kernel<BF16G, VEC, MAXN, ACC>, dim3(kNormPartials),
+                       dim3(kThreads), 0, stream, a);
 }
 
 }  // namespace
@@ -254,8 +271,8 @@ cudaError_t launch_grad_sqnorm(const NormLaunch& a, cudaStream_t stream) {
 
 cudaError_t launch_clip_coef(const double* rank_sqnorms, int n, double max_norm, float* coef,
                              int32_t* nonfinite, cudaStream_t stream) {
-  clip_coef_kernel<<<1, 32, 0, stream>>>(rank_sqnorms, n, max_norm, coef, nonfinite);
-  return cudaGetLastError();
+  return launch_kernel(clip_coef_kernel, dim3(1), dim3(32), 0, stream, rank_sqnorms, n, max_norm,
+                       coef, nonfinite);
 }
 
 }  // namespace zs

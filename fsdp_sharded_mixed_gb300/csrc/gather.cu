@@ -11,6 +11,7 @@
 #include <stdint.h>
 
 #include "bounds.cuh"
+#include "overlap.cuh"
 #include "zs_internal.h"
 
 namespace zs {
@@ -45,6 +46,7 @@ __device__ __forceinline__ uint4 ld_once(const void* p) {
 
 // blockIdx.y = active slot; 16-byte units, kUnroll loads in flight per thread.
 __global__ void __launch_bounds__(kThreads) gather16_kernel(const __grid_constant__ GatherArgs a) {
+  overlap_wait();
   const uint4* src = reinterpret_cast<const uint4*>(a.src[blockIdx.y]);
   uint4* dst = reinterpret_cast<uint4*>(a.dst + (int64_t)a.slot[blockIdx.y] * a.slot_bytes);
   const int64_t n = a.slot_bytes / 16;
@@ -78,6 +80,7 @@ __device__ __forceinline__ void st32(void* p, const uint32_t* w) {
 }
 // blockIdx.y = active slot; 32-byte units, kUnroll loads in flight per thread.
 __global__ void __launch_bounds__(kThreads) gather32_kernel(const __grid_constant__ GatherArgs a) {
+  overlap_wait();
   const unsigned char* src = a.src[blockIdx.y];
   unsigned char* dst = a.dst + (int64_t)a.slot[blockIdx.y] * a.slot_bytes;
   const int64_t n = a.slot_bytes / 32;
@@ -100,6 +103,7 @@ __global__ void __launch_bounds__(kThreads) gather32_kernel(const __grid_constan
 
 // Any alignment: byte copy (slots whose byte size is not a multiple of 16).
 __global__ void __launch_bounds__(kThreads) gather1_kernel(const __grid_constant__ GatherArgs a) {
+  overlap_wait();
   const unsigned char* src = a.src[blockIdx.y];
   unsigned char* dst = a.dst + (int64_t)a.slot[blockIdx.y] * a.slot_bytes;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
@@ -142,12 +146,11 @@ cudaError_t launch_gather(const GatherLaunch& in, cudaStream_t stream) {
     int64_t w32 = (in.slot_bytes / 32 / kUnroll + kThreads - 1) / kThreads;
     if (w32 > cap) w32 = cap;
     if (w32 < 1) w32 = 1;
-    gather32_kernel<<<dim3((unsigned)w32, (unsigned)active), kThreads, 0, stream>>>(a);
-  } else if (vec)
-    gather16_kernel<<<grid, kThreads, 0, stream>>>(a);
-  else
-    gather1_kernel<<<grid, kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+    return launch_kernel(gather32_kernel, dim3((unsigned)w32, (unsigned)active), dim3(kThreads), 0,
+                         stream, a);
+  }
+  if (vec) return launch_kernel(gather16_kernel, grid, dim3(kThreads), 0, stream, a);
+  return launch_kernel(gather1_kernel, grid, dim3(kThreads), 0, stream, a);
 }
 
 }  // namespace zs

@@ -23,6 +23,7 @@
 #include <stdint.h>
 
 #include "bounds.cuh"
+#include "overlap.cuh"
 #include "zs_internal.h"
 
 namespace zs {
@@ -134,6 +135,7 @@ __device__ __forceinline__ int unit_of(uintptr_t a) {
 }
 
 __global__ void __launch_bounds__(kThreads) segment_copy_kernel(const __grid_constant__ SegArgs a) {
+  overlap_wait();
   const int64_t total = a.first[a.count];
   for (int64_t c = blockIdx.x; c < total; c += gridDim.x) {
     int lo = 0, hi = a.count - 1;  // the segment holding chunk c
@@ -211,8 +213,7 @@ cudaError_t launch_segment_copy(const RowSegment* segs, int n, cudaStream_t stre
     // 8 resident blocks per SM; blocks stride over the launch's chunks.
     const int64_t cap = (int64_t)sms * 8;
     const int64_t blocks = total < cap ? total : cap;
-    segment_copy_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(a);
-    e = cudaGetLastError();
+    e = launch_kernel(segment_copy_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

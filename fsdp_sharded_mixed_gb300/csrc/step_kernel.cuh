@@ -12,6 +12,8 @@
 #include <mutex>
 
 #include "bounds.cuh"
+#include "bulk.cuh"
+#include "overlap.cuh"
 #include "zs_internal.h"
 
 namespace zs {
@@ -314,6 +316,7 @@ __device__ __forceinline__ void process_element(const StepArgs<MAXN>& a, int64_t
 template <int GW, bool BF16G, int PD, int MAXN, bool ACC>
 __global__ void __launch_bounds__(kThreads, 2)
     shard_step_kernel(const __grid_constant__ StepArgs<MAXN> a) {
+  overlap_wait();
   if (a.skip && *a.skip) return;  // the ranks' shared non-finite decision
   const bool clip = a.coef != nullptr;
   const float coef = clip ? *a.coef : 1.0f;
@@ -342,30 +345,29 @@ __global__ void __launch_bounds__(kThreads, 2)
 // ---- the staged path ------------------------------------------------------------
 // The same step with the N slices and the state tile staged in shared memory
 // by bulk asynchronous copies (cp.async.bulk, completion counted on an
-// mbarrier): one producer warp keeps the next tiles' copies in flight (its
+// mbarrier): one producer warp keeps the next tile's copies in flight (its
 // lanes issue them in parallel: one thread issuing 35 copies of 2 KB per stage
 // held N = 32 bf16 slices to 0.89 of the copy bandwidth, 32 lanes 0.98) while
 // 16 consumer warps compute the current one from shared memory, so loads and
 // arithmetic overlap instead of alternating per thread. A tile is 512 × E
 // elements, each consumer thread E of them: E = 4 (2048 elements) where two
-// stages of that fit in shared memory, else E = 2 (1024), which stages up to
-// 50 bf16 or 25 fp32 slices; stages are reused once every consumer warp has
-// released them. (E = 1 was measured and left out: with 1 KB and 2 KB copies
-// per slice it ran at 0.59 and 0.94-0.96 of the copy bandwidth for N = 64 bf16
-// and N = 32 fp32 slices, where the register-streaming kernel runs at 0.98-1.03.) On GB300 this wins where the register-
-// streaming kernel above cannot keep enough bytes in flight: short ranges,
-// many slices (32 bytes or more per element) and N <= 2 with 3-byte
-// parameters; elsewhere the kernel above is faster (the choice is in
-// try_staged). Every wait is bounded: a wait that gives up sets the device
-// error word's timeout bit (value 2) and the thread stops; the producer
-// waits, bounded, for its own copies before the block exits.
+// stages of that fit in a block's shared memory, else E = 2 (1024), which
+// stages up to 50 bf16 or 25 fp32 slices; a stage is reused once every consumer
+// warp has released it. One block per SM, two stages (staged_shape): on GB300
+// that streams faster than deeper pipelines or two blocks per SM, and faster
+// than the register-streaming kernel above nearly everywhere (the choice is in
+// try_staged). (E = 1 was measured and left out: with 1 KB and 2 KB copies per
+// slice it ran at 0.59 and 0.94-0.96 of the copy bandwidth for N = 64 bf16 and
+// N = 32 fp32 slices, where the register-streaming kernel runs at 0.98-1.03.)
+// Every wait is bounded: a wait that gives up sets the device error word's
+// timeout bit (value 2) and the thread stops; the producer waits, bounded,
+// for its own copies before the block exits.
 constexpr int kStagedWarps = 16;                     // consumer warps
 constexpr int kStagedThreads = (kStagedWarps + 1) * 32;
 constexpr int kStagedMaxN = 64;
 // Elements of a tile with E elements per consumer thread: 2048 or 1024.
 __host__ __device__ constexpr int staged_tile(int E) { return kStagedWarps * 32 * E; }
-constexpr int kStagedMaxStages = 4;
-constexpr uint32_t kWaitPolls = 1u << 21;
+constexpr int kStagedMaxStages = 2;
 
 struct StagedArgs {
   StepArgs<kStagedMaxN> a;
@@ -376,47 +378,6 @@ struct StagedArgs {
   unsigned int* err;   // the device error word
 };
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
-}
-// Bounded wait for the phase of parity `parity` to complete: at most `polls`
-// polls, then the error word's timeout bit (value 2) is set and the caller
-// stops.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, unsigned int* err,
-                                          uint32_t polls = kWaitPolls) {
-  for (uint32_t it = 0; it < polls; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(done)
-        : "r"(smem_addr(b)), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  atomicOr(err, 2u);
-  return false;
-}
-__device__ __forceinline__ void bulk_to_smem(void* dst, const void* src, uint32_t bytes,
-                                             uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
 __device__ __forceinline__ void st_u32(void* p, uint32_t w) {
   asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(w) : "memory");
 }
@@ -509,6 +470,7 @@ __global__ void __launch_bounds__(kStagedThreads, 2)
     staged_step_kernel(const __grid_constant__ StagedArgs sa) {
   constexpr int T = staged_tile(E);
   const StepArgs<kStagedMaxN>& a = sa.a;
+  overlap_wait();
   if (a.skip && *a.skip) return;  // the ranks' shared non-finite decision
   const bool clip = a.coef != nullptr;
   const float coef = clip ? *a.coef : 1.0f;
@@ -620,25 +582,33 @@ __global__ void __launch_bounds__(kStagedThreads, 2)
   }
 }
 
-// Shared memory of the staged path: the stages a block holds and the blocks
-// an SM holds, from the tile's byte count; 0 stages = the path does not fit.
-inline void staged_shape(uint32_t stage_bytes, int smem_per_sm, int smem_per_block, int* stages,
+// The staged path's launch shape: one block per SM holding two stages (the
+// tile being computed and the next one being filled); 0 stages = two stages of
+// this tile do not fit in a block's shared memory. Measured on GB300 against
+// deeper pipelines and two blocks per SM (same tiles): the GPT-2-small step
+// (N = 8, 15.5M elements) ran at 1.004 of the copy bandwidth with one block of
+// two stages, 0.857 / 0.840 with three / four stages, 0.893 with two blocks of
+// two; the Llama-7B shard at 1.042 against 0.962 / 0.927 / 0.950. More bytes in
+// flight per SM were slower, not faster.
+inline void staged_shape(uint32_t stage_bytes, int smem_per_block, int* stages,
                          int* blocks_per_sm) {
-  const int reserve = 1024 + 16 * kStagedMaxStages;  // per-block system use and barriers
-  *blocks_per_sm = 2 * (2 * (int64_t)stage_bytes + reserve) <= smem_per_sm ? 2 : 1;
-  int64_t budget = smem_per_sm / *blocks_per_sm - reserve;
-  if (budget > smem_per_block - 16 * kStagedMaxStages) budget = smem_per_block - 16 * kStagedMaxStages;
-  int64_t ns = budget / stage_bytes;
-  if (ns > kStagedMaxStages) ns = kStagedMaxStages;
-  *stages = ns >= 2 ? (int)ns : 0;
+  *blocks_per_sm = 1;
+  *stages = kStagedMaxStages * ((int64_t)stage_bytes + 16) <= smem_per_block ? kStagedMaxStages
+                                                                            : 0;
 }
 
 template <bool BF16G, int PD, bool ACC, int E>
 cudaError_t launch_staged(const ShardStepLaunch& in, uint32_t stage_bytes, int stages,
-                          int blocks_per_sm, int sms, cudaStream_t stream) {
+                          int blocks_per_sm, int sms, int smem_per_sm, cudaStream_t stream) {
   constexpr int T = staged_tile(E);
   auto kernel = staged_step_kernel<BF16G, PD, ACC, E>;
-  const size_t smem = (size_t)stages * stage_bytes + 16 * (size_t)stages;
+  // One block per SM whatever else is resident when the blocks are placed:
+  // with launch overlap they are dispatched while the previous kernel's
+  // blocks drain, and two blocks of a small stage would fit on one SM while
+  // another SM got none (measured: the Qwen2.5-3B clip pipeline took 6.08 ms
+  // instead of 4.81). A block asks for more than half an SM's shared memory.
+  size_t smem = (size_t)stages * stage_bytes + 16 * (size_t)stages;
+  if (blocks_per_sm == 1 && smem < (size_t)smem_per_sm / 2) smem = (size_t)smem_per_sm / 2;
   // This instantiation's shared-memory opt-in so far, per device; raised
   // under a lock so that concurrent first calls cannot leave it recorded
   // above what the attribute holds.
@@ -685,8 +655,7 @@ cudaError_t launch_staged(const ShardStepLaunch& in, uint32_t stage_bytes, int s
   sa.a.err = sa.err;
   int64_t blocks = sa.t1 - sa.t0;
   if (blocks > (int64_t)sms * blocks_per_sm) blocks = (int64_t)sms * blocks_per_sm;
-  kernel<<<(unsigned)blocks, kStagedThreads, smem, stream>>>(sa);
-  return cudaGetLastError();
+  return launch_kernel(kernel, dim3((unsigned)blocks), dim3(kStagedThreads), smem, stream, sa);
 }
 
 template <int GW, bool BF16G, int PD, int MAXN, bool ACC>
@@ -731,8 +700,7 @@ cudaError_t launch_one(const ShardStepLaunch& in, cudaStream_t stream) {
   int64_t blocks = (units + kThreads - 1) / kThreads;
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
-  kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a);
 }
 
 // The staged path where it is eligible and (path 0) measured faster: N <= 50,
@@ -777,8 +745,7 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
     const uint32_t t = (uint32_t)staged_tile(e);
     const uint32_t sb = (uint32_t)a.world * t * (BF16G ? 2u : 4u) + (ACC ? 4u : 3u) * t * 4u;
     int st = 0, bps = 0;
-    staged_shape(sb, sh.per_sm.load(std::memory_order_relaxed),
-                 sh.per_block.load(std::memory_order_relaxed), &st, &bps);
+    staged_shape(sb, sh.per_block.load(std::memory_order_relaxed), &st, &bps);
     if (st >= 2) {
       E = e;
       stages = st;
@@ -792,28 +759,34 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
   // Each consumer thread stores its E parameters in one access.
   const uintptr_t slot_align = PD == kParamBf16 ? 2 * E : PD == kParamFp32 ? 4 * E : E;
   if ((uintptr_t)a.slot % slot_align != 0) return false;
-  // The per-call choice, from the GB300 sweep (S x N x dtypes, both kernels)
-  // and the accumulated step: the staged kernel is faster for ranges under
-  // 2^24 elements, where the slices bring 32 bytes or more per element (N >= 16
-  // bf16, N >= 8 fp32), and at N <= 2 with 3-byte parameters; the register-
-  // streaming kernel elsewhere (including N = 8 bf16 with the accumulator:
-  // 1.026 vs 0.956 on Llama-7B). 1024-element tiles: with fp32 slices (4 KB
-  // copies) at every size (N = 16 at 2^22..2^28 elements 0.92 / 1.04 / 1.04 /
-  // 1.05 against 0.78 / 0.97 / 1.01 / 1.02; N = 20 at 2^26 1.048 vs 1.021);
-  // with bf16 slices (2 KB copies) for ranges under 2^25 (N = 24 / 32 / 48 at
-  // 2^24: 1.01 / 0.98 / 1.01 against 0.94 / 0.96 / 0.97), not above (N = 32 at
-  // 2^26 and 2^28: 1.00 against 1.02 and 1.03).
-  const int slice_bytes = a.world * (BF16G ? 2 : 4);
-  const bool wide_rule = a.hi - a.lo < (int64_t(1) << 24) || slice_bytes >= 32 ||
-                         (a.world <= 2 && PD == kParamFp24);
-  const bool narrow_rule = !BF16G || a.hi - a.lo < (int64_t(1) << 25);
-  if (path == 0 && !(E == 4 ? wide_rule : narrow_rule)) return false;
+  // The per-call choice, from GB300 sweeps of both kernels (shard sizes 2^20 ..
+  // 2^30 x N in 2..64 x slice and parameter dtypes, CUDA graphs of 20 steps)
+  // and the named workloads' step, accumulated and clipped pipelines. The
+  // staged kernel (one block per SM) is faster nearly everywhere with
+  // 2048-element tiles (2^24 elements, N = 8 bf16: 1.002 against 0.897 of the
+  // copy bandwidth; the GPT-2-small step 1.00 against 0.87; Llama-7B 1.041
+  // against 1.014); the register-streaming kernel keeps fp32 parameters with
+  // N <= 8 from 2^24 elements (2^30, N = 4: 1.036 against 0.987) and fp32 slices
+  // with N <= 4 from 2^25 (2^26, N = 4: 1.006 against 0.977). With 1024-element
+  // tiles (more slices than two 2048-element stages hold) the staged kernel wins
+  // under 2^25 elements with bf16 slices (N = 48 at 2^24: 1.018 against 0.970)
+  // and loses above (N = 32 at 2^26: 0.997 against 1.017); with fp32 slices it
+  // wins or ties.
+  const int64_t len = a.hi - a.lo;
+  const bool direct_wins =
+      E == 4 ? (PD == kParamFp32 && a.world <= 8 && len >= (int64_t(1) << 24)) ||
+                   (!BF16G && a.world <= 4 && len >= (int64_t(1) << 25))
+             : BF16G && len >= (int64_t(1) << 25);
+  if (path == 0 && direct_wins) return false;
   const int sms = sh.sms.load(std::memory_order_relaxed);
   note_step_kernel(2, (int)T);
+  const int smem_sm = sh.per_sm.load(std::memory_order_relaxed);
   if (E == 4)
-    *result = launch_staged<BF16G, PD, ACC, 4>(a, stage_bytes, stages, per_sm_blocks, sms, stream);
+    *result = launch_staged<BF16G, PD, ACC, 4>(a, stage_bytes, stages, per_sm_blocks, sms, smem_sm,
+                                               stream);
   else
-    *result = launch_staged<BF16G, PD, ACC, 2>(a, stage_bytes, stages, per_sm_blocks, sms, stream);
+    *result = launch_staged<BF16G, PD, ACC, 2>(a, stage_bytes, stages, per_sm_blocks, sms, smem_sm,
+                                               stream);
   return true;
 }
 

@@ -485,15 +485,27 @@ zs_status zs_selftest_bounds_window(int64_t shrink);
 /* The step's kernel. Two kernels compute the same step with the same fp32
  * operations in the same order (results are identical): the register-
  * streaming kernel (each thread loads its 16-element group of every slice and
- * state array straight into registers) and the staged kernel (one thread per
- * block streams 2048- or 1024-element tiles of the slices and state into
- * shared memory with bulk asynchronous copies while 16 warps compute; where
- * two stages fit: N <= 50 bf16 or 25 fp32 slices). path 0 (default): chosen
- * per call by N, the slice dtype and the range's length; 1: always the
- * register-streaming kernel; 2: the staged kernel wherever it applies.
+ * state array straight into registers) and the staged kernel (one block per
+ * SM; one warp streams 2048- or 1024-element tiles of the slices and state
+ * into shared memory with bulk asynchronous copies while 16 warps compute;
+ * where two stages fit: N <= 50 bf16 or 25 fp32 slices). path 0 (default):
+ * chosen per call by N, the slice and parameter dtypes and the range's
+ * length (mostly the staged kernel); 1: always the register-streaming
+ * kernel; 2: the staged kernel wherever it applies.
  * Returns the previous path, or -1 for an unknown path (nothing changed).
  * The pages have no counterpart: this is a choice between two GB300 kernels. */
 int32_t zs_set_step_path(int32_t path);
+/* 1 (default): the library's kernels are launched so that each may be
+ * scheduled while the previous kernel in its stream finishes (programmatic
+ * dependent launch); every kernel waits, before its first access to global
+ * memory, until the kernels before it have completed and their writes are
+ * visible, so stream order and results are those of ordinary launches. This
+ * hides most of a launch's ramp between back-to-back calls (a bucket's step
+ * after another's, the norm pass, coefficient and clipped step). 0: ordinary
+ * launches. Process-wide; returns the previous setting, or -1 for a value
+ * other than 0 or 1 (nothing changed). The pages have no counterpart: this is
+ * how the GPU schedules this library's launches. */
+int32_t zs_set_launch_overlap(int32_t on);
 /* Which kernel ran the calling thread's last step-family launch (zs_shard_step
  * and its clipped, accumulated and to-shard forms): *kernel = 1 for the
  * register-streaming kernel, with *elems = the elements of one thread's vector

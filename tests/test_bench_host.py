@@ -100,7 +100,8 @@ def test_reference_arm_loads_only_the_oracle_and_generator():
     w = WORKLOADS["gpt2-small"]
     op = oracle.default().plan(w.numels, w.tied_to, world=w.world, align=w.align,
                                bucket_elems=w.bucket_elems)
-    args = bench.argparse.Namespace(pipeline="step", step_path="auto", micro_steps=4)
+    args = bench.argparse.Namespace(pipeline="step", step_path="auto", micro_steps=4,
+                                    no_overlap=False)
     # rank 0's shard lies inside one bucket (the one holding wte): one call
     want = bench.run_config(args, w, op["S"], op["P"], op["P_pad"], 1, 0, 1)
     assert line["config"] == want

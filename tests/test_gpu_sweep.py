@@ -19,15 +19,22 @@ HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
 PDT = {2: (zs.ZS_BF16, oracle.BF16), 3: (zs.ZS_FP24, oracle.FP24), 4: (zs.ZS_FP32, oracle.FP32)}
 
 
-@pytest.mark.parametrize("S,N,gb,pb", [
-    (1 << 26, 16, 4, 3),     # fp32 slices, 3-byte parameters
-    (1 << 24, 64, 2, 4),     # the widest world, fp32 parameters
-    (1 << 28, 2, 2, 3),
-    (1 << 22, 8, 4, 2),
-    (1 << 24, 16, 4, 3),     # fp32 slices on 1024-element tiles (the per-call choice)
-    (1 << 10, 4, 2, 2),      # the smallest point
+# (S, N, slice bytes, parameter bytes, the kernel the per-call choice takes:
+# (1, vector group) register-streaming, (2, tile elements) staged, None = any)
+@pytest.mark.parametrize("S,N,gb,pb,kernel", [
+    (1 << 26, 16, 4, 3, None),       # fp32 slices, 3-byte parameters
+    (1 << 24, 64, 2, 4, (1, 16)),    # the widest world (no two staged tiles fit)
+    (1 << 28, 2, 2, 3, (2, 2048)),   # N <= 2 with 3-byte parameters: staged
+    (1 << 22, 8, 4, 2, None),
+    (1 << 24, 16, 4, 3, (2, 1024)),  # fp32 slices on 1024-element tiles
+    (1 << 24, 32, 2, 2, (2, 1024)),  # bf16 slices, N in 24..48, under 2^25: 1024-element tiles
+    (1 << 26, 32, 2, 2, (1, 16)),    # the same above 2^25: register-streaming
+    (1 << 28, 8, 2, 2, (2, 2048)),   # bf16, N = 8, large: staged
+    (1 << 26, 4, 4, 2, (1, 16)),     # fp32 slices, N <= 4, from 2^25: register-streaming
+    (1 << 24, 8, 2, 4, (1, 16)),     # fp32 parameters, N <= 8, from 2^24: register-streaming
+    (1 << 10, 4, 2, 2, None),        # the smallest point
 ])
-def test_sweep_point_sampled(orc, S, N, gb, pb):
+def test_sweep_point_sampled(orc, S, N, gb, pb, kernel):
     plan = zs.zs_flatten_plan([N * S], world=N, align_elems=128)
     assert plan.S == S
     stream = torch.cuda.current_stream().cuda_stream
@@ -52,6 +59,8 @@ def test_sweep_point_sampled(orc, S, N, gb, pb):
                               cuda_stream=stream)
         zs.zs_shard_step(plan, 0, 0, S, grads, zs.ZS_BF16 if bf16 else zs.ZS_FP32, master, m, v,
                          full, PDT[pb][0], HP, t)
+        if kernel is not None:
+            assert zs.zs_last_step_kernel() == kernel
         g_host = [synth.at(idx, seed=1, rank=j, step=t, sigma=1e-3, bf16=bf16, p_limit=S)
                   for j in range(N)]
         orc.shard_step(world=N, rank=0, S=K, lo=0, hi=K, grads=g_host, master=o_master, m=o_m,
