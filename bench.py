@@ -52,7 +52,7 @@ METRIC = "shard-step elements/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "elements/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = [os.path.join(ROOT, "fsdp_sharded_mixed_gb300", "csrc", f)
-                  for f in ("shard_step.cu", "step_kernel.cuh")]
+                  for f in ("shard_step.cu", "step_kernel.cuh", "bulk.cuh", "overlap.cuh")]
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "shard_step_traffic.txt")
 
 
@@ -470,7 +470,7 @@ def run_ours(args, w):
 
     if args.pipeline == "gather":
         # every other rank's shard read once and written once into its slot
-        pipeline = [("gather16_kernel", part_gather, 4 * (N - 1))]
+        pipeline = [("gather_kernel", part_gather, 4 * (N - 1))]
         launches_per_step = 1
     elif args.pipeline == "unshard":
         # bytes per shard element of the workload's plan: every parameter
@@ -762,6 +762,11 @@ def run_ours(args, w):
         step_bpe = pipeline[-1][2]
         achieved = step_bpe * S / step_s / 1e9
         kname = pipeline[-1][0]
+        if kname == "shard_step_kernel":
+            # the step kernel the last call took (the per-call choice)
+            kk, ke = zs.zs_last_step_kernel()
+            kname = (f"staged_step_kernel ({ke}-element tiles)" if kk == 2 else
+                     f"shard_step_kernel ({ke}-element groups)" if kk == 1 else kname)
         traffic_pe = committed_traffic(w.key)
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "peak_source": peak_kind,
