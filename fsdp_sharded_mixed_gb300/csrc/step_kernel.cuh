@@ -353,10 +353,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 // elements, each consumer thread E of them: E = 4 (2048 elements) where two
 // stages of that fit in a block's shared memory, else E = 2 (1024), which
 // stages up to 50 bf16 or 25 fp32 slices; a stage is reused once every consumer
-// warp has released it. One block per SM, two stages (staged_shape): on GB300
-// that streams faster than deeper pipelines or two blocks per SM, and faster
-// than the register-streaming kernel above nearly everywhere (the choice is in
-// try_staged). (E = 1 was measured and left out: with 1 KB and 2 KB copies per
+// warp has released it. One block per SM and two stages for calls larger than
+// twice the L2, two blocks per SM and up to four stages below (staged_shape):
+// on GB300 that streams faster than the register-streaming kernel above
+// nearly everywhere (the choice is in try_staged). (E = 1 was measured and left out: with 1 KB and 2 KB copies per
 // slice it ran at 0.59 and 0.94-0.96 of the copy bandwidth for N = 64 bf16 and
 // N = 32 fp32 slices, where the register-streaming kernel runs at 0.98-1.03.)
 // Every wait is bounded: a wait that gives up sets the device error word's
@@ -367,7 +367,7 @@ constexpr int kStagedThreads = (kStagedWarps + 1) * 32;
 constexpr int kStagedMaxN = 64;
 // Elements of a tile with E elements per consumer thread: 2048 or 1024.
 __host__ __device__ constexpr int staged_tile(int E) { return kStagedWarps * 32 * E; }
-constexpr int kStagedMaxStages = 2;
+constexpr int kStagedMaxStages = 4;
 
 struct StagedArgs {
   StepArgs<kStagedMaxN> a;
@@ -582,19 +582,32 @@ __global__ void __launch_bounds__(kStagedThreads, 2)
   }
 }
 
-// The staged path's launch shape: one block per SM holding two stages (the
-// tile being computed and the next one being filled); 0 stages = two stages of
-// this tile do not fit in a block's shared memory. Measured on GB300 against
-// deeper pipelines and two blocks per SM (same tiles): the GPT-2-small step
-// (N = 8, 15.5M elements) ran at 1.004 of the copy bandwidth with one block of
-// two stages, 0.857 / 0.840 with three / four stages, 0.893 with two blocks of
-// two; the Llama-7B shard at 1.042 against 0.962 / 0.927 / 0.950. More bytes in
-// flight per SM were slower, not faster.
-inline void staged_shape(uint32_t stage_bytes, int smem_per_block, int* stages,
-                         int* blocks_per_sm) {
-  *blocks_per_sm = 1;
-  *stages = kStagedMaxStages * ((int64_t)stage_bytes + 16) <= smem_per_block ? kStagedMaxStages
-                                                                            : 0;
+// The staged path's launch shape. A call whose algorithmic bytes exceed twice
+// the L2 (the steps of every named workload and bucket): one block per SM
+// holding two stages (the tile being computed and the next one being filled).
+// Measured on GB300 against deeper pipelines and two blocks per SM (same
+// tiles): the GPT-2-small step (N = 8, 15.5M elements) ran at 1.004 of the
+// copy bandwidth with one block of two stages, 0.857 / 0.840 with three / four
+// stages, 0.893 with two blocks of two; the Llama-7B shard at 1.042 against
+// 0.962 / 0.927 / 0.950; the GPT-2-small bucket calls (1.2M to 14.4M elements)
+// at 0.96 against 0.87. Smaller calls, whose data a step back to back with the
+// previous one partly finds in L2: two blocks per SM where two stages of each
+// fit, with up to four stages (2^22 elements, N = 4 bf16: 1.12 against 0.94;
+// 2^20: 0.76 against 0.66). 0 stages = two stages of this tile do not fit.
+inline void staged_shape(uint32_t stage_bytes, int smem_per_sm, int smem_per_block, bool small,
+                         int* stages, int* blocks_per_sm) {
+  if (!small) {
+    *blocks_per_sm = 1;
+    *stages = 2 * ((int64_t)stage_bytes + 16) <= smem_per_block ? 2 : 0;
+    return;
+  }
+  const int reserve = 1024 + 16 * kStagedMaxStages;  // per-block system use and barriers
+  *blocks_per_sm = 2 * (2 * (int64_t)stage_bytes + reserve) <= smem_per_sm ? 2 : 1;
+  int64_t budget = smem_per_sm / *blocks_per_sm - reserve;
+  if (budget > smem_per_block - 16 * kStagedMaxStages) budget = smem_per_block - 16 * kStagedMaxStages;
+  int64_t ns = budget / stage_bytes;
+  if (ns > kStagedMaxStages) ns = kStagedMaxStages;
+  *stages = ns >= 2 ? (int)ns : 0;
 }
 
 template <bool BF16G, int PD, bool ACC, int E>
@@ -741,11 +754,17 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
   // stages fit.
   int E = 0, stages = 0, per_sm_blocks = 0;
   uint32_t stage_bytes = 0;
+  // The call's algorithmic bytes against twice the L2 (the launch shape).
+  const int64_t call_bytes =
+      (a.hi - a.lo) * ((int64_t)a.world * (BF16G ? 2 : 4) + (ACC ? 28 : 24) +
+                       (PD == kParamBf16 ? 2 : PD == kParamFp32 ? 4 : 3));
+  const bool small = call_bytes < (int64_t(256) << 20);
   for (int e = 4; e >= 2 && E == 0; e /= 2) {
     const uint32_t t = (uint32_t)staged_tile(e);
     const uint32_t sb = (uint32_t)a.world * t * (BF16G ? 2u : 4u) + (ACC ? 4u : 3u) * t * 4u;
     int st = 0, bps = 0;
-    staged_shape(sb, sh.per_block.load(std::memory_order_relaxed), &st, &bps);
+    staged_shape(sb, sh.per_sm.load(std::memory_order_relaxed),
+                 sh.per_block.load(std::memory_order_relaxed), small, &st, &bps);
     if (st >= 2) {
       E = e;
       stages = st;
@@ -762,7 +781,7 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
   // The per-call choice, from GB300 sweeps of both kernels (shard sizes 2^20 ..
   // 2^30 x N in 2..64 x slice and parameter dtypes, CUDA graphs of 20 steps)
   // and the named workloads' step, accumulated and clipped pipelines. The
-  // staged kernel (one block per SM) is faster nearly everywhere with
+  // staged kernel is faster nearly everywhere with
   // 2048-element tiles (2^24 elements, N = 8 bf16: 1.002 against 0.897 of the
   // copy bandwidth; the GPT-2-small step 1.00 against 0.87; Llama-7B 1.041
   // against 1.014); the register-streaming kernel keeps fp32 parameters with

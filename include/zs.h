@@ -485,9 +485,10 @@ zs_status zs_selftest_bounds_window(int64_t shrink);
 /* The step's kernel. Two kernels compute the same step with the same fp32
  * operations in the same order (results are identical): the register-
  * streaming kernel (each thread loads its 16-element group of every slice and
- * state array straight into registers) and the staged kernel (one block per
- * SM; one warp streams 2048- or 1024-element tiles of the slices and state
- * into shared memory with bulk asynchronous copies while 16 warps compute;
+ * state array straight into registers) and the staged kernel (one or two
+ * blocks per SM; one warp streams 2048- or 1024-element tiles of the slices
+ * and state into shared memory with bulk asynchronous copies while 16 warps
+ * compute;
  * where two stages fit: N <= 50 bf16 or 25 fp32 slices). path 0 (default):
  * chosen per call by N, the slice and parameter dtypes and the range's
  * length (mostly the staged kernel); 1: always the register-streaming
