@@ -68,6 +68,12 @@ def oracle_chunks(orc, *, world, rank, S, P, steps, hp, grad_kw, master_kw, pdts
                 params[pdt] = out
         return check(c0, c1, master, m, v, params)
 
+    return run_chunks(work, lo, hi, chunk=chunk, threads=threads)
+
+
+def run_chunks(work, lo, hi, chunk=CHUNK, threads=None):
+    """work(c0, c1) over [lo, hi) in chunks on a thread pool; returns the sum
+    of the results (the first exception raised by a worker propagates)."""
     total = 0
     ex = cf.ThreadPoolExecutor(max_workers=threads or host_threads())
     try:

@@ -28,7 +28,7 @@ import torch
 import fsdp_sharded_mixed_gb300 as zs
 import oracle
 import synth
-from full_parity import bitwise_check, oracle_chunks
+from full_parity import CHUNK, bitwise_check, oracle_chunks, run_chunks
 from gpu_util import (DEV, all_zero, assert_params_close, assert_state_close, dev_fill,
                       oracle_hp)
 from synth.workloads import GPT2_SMALL, LLAMA_7B, QWEN25_3B, SWEEP_WORLDS
@@ -216,11 +216,12 @@ def _sweep_point(N, S, gb, steps, together=True):
 
 @pytest.mark.parametrize("gb", [2, 4], ids=["bf16_slices", "fp32_slices"])
 @pytest.mark.parametrize("N", SWEEP_WORLDS)
-def test_sweep_every_element_2p24(orc, N, gb):
-    """Sweep grid at S = 2^24 (the mid size where the per-call kernel choice
-    changes with N and the slice dtype), 3 steps, bf16 / 3-byte / fp32
-    parameters: every element bit for bit."""
-    S, steps = 1 << 24, 3
+@pytest.mark.parametrize("log2S", [22, 24])
+def test_sweep_every_element(orc, log2S, N, gb):
+    """Sweep grid at S = 2^22 and 2^24 (the sizes where the per-call kernel
+    choice and the staged kernel's launch shape change with N and the dtypes),
+    3 steps, bf16 / 3-byte / fp32 parameters: every element bit for bit."""
+    S, steps = 1 << log2S, 3
     (g_master, g_m, g_v), slots = _sweep_point(N, S, gb, steps)
     check = bitwise_check(g_master, g_m, g_v, slots)
     diff = oracle_chunks(orc, world=N, rank=0, S=S, P=S, steps=steps, hp=HP,
@@ -269,3 +270,94 @@ def test_sweep_sampled_2p28(orc, N, gb):
     for name, got, ref in (("master", g_master, o_master), ("m", g_m, o_m), ("v", g_v, o_v)):
         assert assert_state_close(got[idx], ref, name) == 0
         assert np.array_equal(got[idx].view(np.uint32), ref.view(np.uint32)), name
+
+
+def test_qwen25_3b_accumulated_clipped_every_element(orc):
+    """Gradient accumulation with clipping at full size (Qwen2.5-3B, N = 4,
+    rank 1, 771,484,672 elements): G = 2 micro-batches per optimizer step, two
+    optimizer steps; each step accumulates the first micro-batch's mean, takes
+    the norm of the accumulated step's gradient, forms the clip coefficient
+    from the N ranks' partial sums (every rank's taken equal to this one's, the
+    emulated AllReduce) with max_norm at half the norm so that the step clips,
+    and runs the clipped accumulated step. The oracle, chunk by chunk over the
+    whole shard, runs the same micro-steps with the coefficient the device
+    formed (the coefficient from given partials is compared bit for bit in
+    test_gpu_clip.py); master, m, v and the slot bit for bit; each step's norm
+    against the oracle's sequential sum within that sum's rounding bound."""
+    w, rank, G, T = QWEN25_3B, 1, 2, 2
+    plan = zs.zs_flatten_plan(w.numels, w.tied_to, world=w.world, align_elems=w.align)
+    N, S, P = plan.world, plan.S, plan.P
+    grad_kw = dict(seed=w.seed, sigma=w.grad_sigma, bf16=True)
+    master_kw = dict(seed=w.seed, stream=synth.STREAM_MASTER, sigma=w.master_sigma)
+    stream = torch.cuda.current_stream().cuda_stream
+    d_master = dev_fill(S, bf16=False, index0=rank * S, p_limit=P, **master_kw)
+    d_m = torch.zeros(S, dtype=torch.float32, device=DEV)
+    d_v = torch.zeros(S, dtype=torch.float32, device=DEV)
+    d_full = torch.zeros(plan.P_pad, dtype=torch.int16, device=DEV)
+    d_acc = torch.empty(S, dtype=torch.float32, device=DEV)
+    d_grads = [torch.empty(S, dtype=torch.int16, device=DEV) for _ in range(N)]
+    ws = torch.empty(zs.zs_grad_norm_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    parts = torch.zeros(N, dtype=torch.float64, device=DEV)
+    coef = torch.zeros(1, dtype=torch.float32, device=DEV)
+    bad = torch.zeros(1, dtype=torch.int32, device=DEV)
+    coefs, norms = [], []
+    for t in range(1, T + 1):
+        for mstep in range(1, G + 1):
+            for j in range(N):
+                synth.fill_device(d_grads[j].data_ptr(), S, index0=rank * S, rank=j,
+                                  step=(t - 1) * G + mstep, p_limit=P, cuda_stream=stream,
+                                  **grad_kw)
+            if mstep < G:
+                zs.zs_grad_accumulate(plan, rank, 0, S, d_grads, zs.ZS_BF16, d_acc, mstep == 1)
+                continue
+            zs.zs_grad_sqnorm_accumulated(plan, rank, 0, S, d_grads, zs.ZS_BF16, d_acc, G, ws,
+                                          parts.narrow(0, rank, 1))
+            torch.cuda.synchronize()
+            own = float(parts[rank].item())
+            parts.fill_(own)
+            norms.append(own)
+            zs.zs_clip_coefficient(parts, N, 0.5 * (N * own) ** 0.5, coef, bad)
+            zs.zs_shard_step_accumulated_clipped(plan, rank, 0, S, d_grads, zs.ZS_BF16, d_acc, G,
+                                                 d_master, d_m, d_v, d_full, zs.ZS_BF16,
+                                                 w.hparams, t, coef, bad)
+            torch.cuda.synchronize()
+            coefs.append(float(coef.item()))
+            assert int(bad.item()) == 0 and 0.0 < coefs[-1] < 1.0
+    zs.zs_check_device_error()
+    del d_grads, d_acc
+    g_master, g_m, g_v = _host(d_master, np.float32), _host(d_m, np.float32), _host(d_v, np.float32)
+    g_slot = _host(d_full.narrow(0, rank * S, S), np.uint8)
+    del d_master, d_m, d_v, d_full
+    torch.cuda.empty_cache()
+    check = bitwise_check(g_master, g_m, g_v, {oracle.BF16: g_slot})
+    hpo = oracle_hp(w.hparams)
+    sq = np.zeros((S + CHUNK - 1) // CHUNK * T).reshape(-1, T)
+
+    def work(c0, c1):
+        n = c1 - c0
+        master = synth.fill(n, index0=rank * S + c0, p_limit=P, threads=1, **master_kw)
+        m, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
+        acc = np.zeros(n, np.float32)
+        slot = np.zeros(n * 2, np.uint8)
+        for t in range(1, T + 1):
+            for mstep in range(1, G + 1):
+                grads = [synth.fill(n, index0=rank * S + c0, rank=j, step=(t - 1) * G + mstep,
+                                    p_limit=P, threads=1, **grad_kw) for j in range(N)]
+                if mstep < G:
+                    orc.grad_accumulate(world=N, S=n, lo=0, hi=n, grads=grads, accum=acc,
+                                        first=mstep == 1)
+                    continue
+                sq[c0 // CHUNK, t - 1] = orc.grad_sqnorm_accumulated(
+                    world=N, S=n, lo=0, hi=n, grads=grads, accum=acc, micro_steps=G)
+                orc.shard_step_accumulated_clipped(
+                    world=N, rank=0, S=n, lo=0, hi=n, grads=grads, accum=acc, micro_steps=G,
+                    master=master, m=m, v=v, full_flat=slot, coef=np.float32(coefs[t - 1]),
+                    skip=0, t=t, **hpo)
+        return check(c0, c1, master, m, v, {oracle.BF16: slot})
+
+    diff = run_chunks(work, 0, S)
+    assert diff == 0, f"{diff} elements differ in some bit (within the gates)"
+    for t in range(T):
+        want = float(np.sum(sq[:, t]))   # chunk sums added in chunk order
+        assert abs(norms[t] - want) <= (S + 16) * 2.0 ** -52 * want, (t, norms[t], want)
+    plan.free()
