@@ -52,6 +52,7 @@ struct NormArgs {
   unsigned int* err;       // checked build: the device error word
   const float* accum;      // ACC: fp32 sum of the earlier micro-steps' mean gradients
   float invG;              // ACC: fp32(1/G)
+  bool top_down;           // walk the range from its top (see the kernel)
 };
 
 __device__ __forceinline__ void ld32_nc(const void* p, uint32_t* r) {
@@ -92,7 +93,13 @@ __device__ __forceinline__ float mean_grad(const NormArgs<MAXN>& a, int64_t i) {
 
 // VEC: 16-element groups with 32-byte loads (all slices, and with ACC the
 // accumulator, 32-byte aligned); otherwise element by element. ACC: the norm
-// of the accumulated step's gradient (accum + mean) * (1/G).
+// of the accumulated step's gradient (accum + mean) * (1/G). A pass that reads
+// under 1 GiB walks the range from the top down: the clipped step that follows
+// reads the same slices (and accumulator) from the bottom up, so it starts on
+// the ones this pass read last, still in L2 (GPT-2-small, N = 8, in place in
+// the clip pipeline on GB300: 145.7 against 147.5 us per optimizer step).
+// Larger passes go bottom up: there the reuse is a fraction of a percent, and
+// the top-down walk measured up to 2 % slower on the Llama-7B shard.
 template <bool BF16G, bool VEC, int MAXN, bool ACC>
 __global__ void __launch_bounds__(kThreads, 2) grad_sqnorm_kernel(const __grid_constant__ NormArgs<MAXN> a) {
   overlap_wait();
@@ -105,7 +112,8 @@ __global__ void __launch_bounds__(kThreads, 2) grad_sqnorm_kernel(const __grid_c
     g1 = a.hi / kGW;
   }
   if (g0 >= g1) {
-    for (int64_t i = a.lo + tid; i < a.hi; i += stride) {
+    for (int64_t q = tid; q < a.hi - a.lo; q += stride) {
+      const int64_t i = a.top_down ? a.hi - 1 - q : a.lo + q;
       const float g = mean_grad<BF16G, ACC>(a, i);
       float s = 0.0f, c = 0.0f;
       acc_square(g, s, c);
@@ -123,7 +131,8 @@ __global__ void __launch_bounds__(kThreads, 2) grad_sqnorm_kernel(const __grid_c
     constexpr int W = BF16G ? kGW / 2 : kGW;          // 32-bit words per slice per group
     constexpr int KB = 64 / W;                        // slices loaded back to back
     constexpr int kStride = BF16G ? 2 * kGW : 4 * kGW;
-    for (int64_t g = g0 + tid; g < g1; g += stride) {
+    for (int64_t q = tid; q < g1 - g0; q += stride) {
+      const int64_t g = a.top_down ? g1 - 1 - q : g0 + q;
       if (!within(kGW * g, kGW * g + kGW, a.win_lo, a.win_hi, a.err)) continue;
       float acc[kGW];
 #pragma unroll
@@ -240,6 +249,8 @@ cudaError_t launch_norm(const NormLaunch& in, cudaStream_t stream) {
   if (ZS_BOUNDS_CHECK && !a.err) return cudaErrorInvalidSymbol;
   a.accum = in.accum;
   a.invG = in.invG;
+  const int64_t bytes_per_elem = (int64_t)in.world * (BF16G ? 2 : 4) + (ACC ? 4 : 0);
+  a.top_down = (in.hi - in.lo) * bytes_per_elem < (int64_t(1) << 30);
   cudaError_t e = cudaMemsetAsync(in.ticket, 0, sizeof(unsigned int), stream);
   if (e != cudaSuccess) return e;
   return launch_kernel(grad_sqnorm_kernel<BF16G, VEC, MAXN, ACC>, dim3(kNormPartials),
