@@ -784,17 +784,21 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
   // staged kernel is faster nearly everywhere with
   // 2048-element tiles (2^24 elements, N = 8 bf16: 1.002 against 0.897 of the
   // copy bandwidth; the GPT-2-small step 1.00 against 0.87; Llama-7B 1.041
-  // against 1.014); the register-streaming kernel keeps fp32 parameters with
-  // N <= 8 from 2^24 elements (2^30, N = 4: 1.036 against 0.987) and fp32 slices
-  // with N <= 4 from 2^25 (2^26, N = 4: 1.006 against 0.977). With 1024-element
+  // against 1.014); the register-streaming kernel keeps fp32 slices with N <= 4
+  // from 2^25 elements (2^26, N = 4: 1.006 against 0.977; with fp32 parameters
+  // 1.015 against 0.958) and fp32 parameters from bf16 slices with N = 4..8 from
+  // 2^26 (2^30, N = 8: 1.026 against 1.011), where it is ahead by up to 1.5 %;
+  // below 2^26 the staged kernel is ahead there too (2^24, N = 2 / 4 / 8: 0.913 /
+  // 0.969 / 0.959 against 0.823 / 0.906 / 0.911). With 1024-element
   // tiles (more slices than two 2048-element stages hold) the staged kernel wins
   // under 2^25 elements with bf16 slices (N = 48 at 2^24: 1.018 against 0.970)
   // and loses above (N = 32 at 2^26: 0.997 against 1.017); with fp32 slices it
   // wins or ties.
   const int64_t len = a.hi - a.lo;
   const bool direct_wins =
-      E == 4 ? (PD == kParamFp32 && a.world <= 8 && len >= (int64_t(1) << 24)) ||
-                   (!BF16G && a.world <= 4 && len >= (int64_t(1) << 25))
+      E == 4 ? (!BF16G && a.world <= 4 && len >= (int64_t(1) << 25)) ||
+                   (BF16G && PD == kParamFp32 && a.world >= 4 && a.world <= 8 &&
+                    len >= (int64_t(1) << 26))
              : BF16G && len >= (int64_t(1) << 25);
   if (path == 0 && direct_wins) return false;
   const int sms = sh.sms.load(std::memory_order_relaxed);

@@ -31,7 +31,8 @@ PDT = {2: (zs.ZS_BF16, oracle.BF16), 3: (zs.ZS_FP24, oracle.FP24), 4: (zs.ZS_FP3
     (1 << 26, 32, 2, 2, (1, 16)),    # the same above 2^25: register-streaming
     (1 << 28, 8, 2, 2, (2, 2048)),   # bf16, N = 8, large: staged
     (1 << 26, 4, 4, 2, (1, 16)),     # fp32 slices, N <= 4, from 2^25: register-streaming
-    (1 << 24, 8, 2, 4, (1, 16)),     # fp32 parameters, N <= 8, from 2^24: register-streaming
+    (1 << 24, 8, 2, 4, (2, 2048)),   # fp32 parameters under 2^26: staged
+    (1 << 26, 8, 2, 4, (1, 16)),     # fp32 parameters from bf16 slices, N = 4..8, from 2^26
     (1 << 10, 4, 2, 2, None),        # the smallest point
 ])
 def test_sweep_point_sampled(orc, S, N, gb, pb, kernel):
