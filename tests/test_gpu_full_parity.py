@@ -361,3 +361,79 @@ def test_qwen25_3b_accumulated_clipped_every_element(orc):
         want = float(np.sum(sq[:, t]))   # chunk sums added in chunk order
         assert abs(norms[t] - want) <= (S + 16) * 2.0 ** -52 * want, (t, norms[t], want)
     plan.free()
+
+
+def test_qwen25_3b_every_wrap_unit_copy_out(orc):
+    """FSDP2's copy-out at full size in the benchmark's launch configuration:
+    every wrap unit of Qwen2.5-3B (36 blocks + the root unit with the tied
+    embedding, N = 4, rows sharded per parameter), the rank-major gathered
+    buffer from the generator, one zs_unshard per unit; every parameter element
+    against the oracle's copy-out of the same gathered bytes."""
+    from synth.workloads import wrap_units
+    w = QWEN25_3B
+    stream = torch.cuda.current_stream().cuda_stream
+    units = wrap_units(w)
+    assert len(units) == 37
+    for k, idx in enumerate(units):
+        local_of = {g: i for i, g in enumerate(idx)}
+        ps = [w.params[i] for i in idx]
+        ties = [local_of[p.tied_to] if p.tied_to >= 0 else -1 for p in ps]
+        dims, numels = [p.shape[0] for p in ps], [p.numel for p in ps]
+        plan = zs.zs_rows_plan(dims, numels, ties, world=w.world, align_elems=w.align)
+        rp = orc.rows_plan(dims, numels, ties, world=w.world, align=w.align)
+        assert plan.P_pad == w.world * rp["S"]
+        gbuf = torch.empty(plan.P_pad, dtype=torch.int16, device=DEV)
+        synth.fill_device(gbuf.data_ptr(), plan.P_pad, seed=w.seed, rank=k, step=1,
+                          sigma=w.grad_sigma, bf16=True, cuda_stream=stream)
+        outs = [torch.empty(n, dtype=torch.int16, device=DEV) if t < 0 else None
+                for n, t in zip(numels, ties)]
+        zs.zs_unshard(plan, gbuf, zs.ZS_BF16, outs)
+        g_host = synth.fill(plan.P_pad, seed=w.seed, rank=k, step=1, sigma=w.grad_sigma,
+                            bf16=True)
+        refs = [np.zeros(n, np.uint16) if t < 0 else None for n, t in zip(numels, ties)]
+        orc.unshard(rp, g_host.view(np.uint8), 2,
+                    [None if x is None else x.view(np.uint8) for x in refs])
+        torch.cuda.synchronize()
+        for i, (d, r) in enumerate(zip(outs, refs)):
+            if r is not None:
+                assert np.array_equal(_host(d, np.uint16), r), (k, ps[i].name)
+        del gbuf, outs
+        plan.free()
+    zs.zs_check_device_error()
+    torch.cuda.empty_cache()
+
+
+def test_llama_7b_gather_every_element(orc):
+    """The emulated AllGather's assembly at full size (Llama-7B, N = 8, rank 5's
+    view): the other seven ranks' bf16 shards (842M elements each) into the
+    13.5 GB flat buffer, in the benchmark's launch configuration; every byte
+    against the oracle's gather of the same shards, the own slot untouched."""
+    w, rank = LLAMA_7B, 5
+    plan = zs.zs_flatten_plan(w.numels, w.tied_to, world=w.world, align_elems=w.align)
+    N, S, P_pad = plan.world, plan.S, plan.P_pad
+    stream = torch.cuda.current_stream().cuda_stream
+    kw = dict(seed=w.seed, step=3, sigma=w.grad_sigma, bf16=True)
+    srcs = []
+    for j in range(N):
+        if j == rank:
+            srcs.append(None)
+            continue
+        t = torch.empty(S, dtype=torch.int16, device=DEV)
+        synth.fill_device(t.data_ptr(), S, index0=j * S, rank=j, cuda_stream=stream, **kw)
+        srcs.append(t)
+    full = torch.full((P_pad,), 0x1234, dtype=torch.int16, device=DEV)
+    views = zs.zs_gather_assemble(plan, rank, srcs, full, zs.ZS_BF16)
+    torch.cuda.synchronize()
+    zs.zs_check_device_error()
+    del srcs
+    got = _host(full, np.uint16)
+    del full
+    torch.cuda.empty_cache()
+    expect = np.full(P_pad, 0x1234, np.uint16)
+    shards = [None if j == rank else synth.fill(S, index0=j * S, rank=j, **kw)
+              for j in range(N)]
+    orc.gather(world=N, S=S, elem_size=2, shards=shards, full_flat=expect)
+    assert np.array_equal(got, expect)
+    offs = zs.zs_plan_offsets(plan)
+    assert [v - views[0] for v in views] == [2 * (o - offs[0]) for o in offs]
+    plan.free()
