@@ -802,7 +802,6 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
              : BF16G && len >= (int64_t(1) << 25);
   if (path == 0 && direct_wins) return false;
   const int sms = sh.sms.load(std::memory_order_relaxed);
-  note_step_kernel(2, (int)T);
   const int smem_sm = sh.per_sm.load(std::memory_order_relaxed);
   if (E == 4)
     *result = launch_staged<BF16G, PD, ACC, 4>(a, stage_bytes, stages, per_sm_blocks, sms, smem_sm,
@@ -810,6 +809,7 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
   else
     *result = launch_staged<BF16G, PD, ACC, 2>(a, stage_bytes, stages, per_sm_blocks, sms, smem_sm,
                                                stream);
+  if (*result == cudaSuccess) note_step_kernel(2, (int)T);
   return true;
 }
 
@@ -817,13 +817,19 @@ template <bool BF16G, int PD, bool ACC>
 cudaError_t dispatch(const ShardStepLaunch& a, cudaStream_t stream) {
   cudaError_t staged_result = cudaSuccess;
   if (try_staged<BF16G, PD, ACC>(a, stream, &staged_result)) return staged_result;
-  note_step_kernel(1, a.vec_width);
-  if (a.vec_width == 16) {
-    if (a.world <= 16) return launch_one<16, BF16G, PD, 16, ACC>(a, stream);
-    return launch_one<16, BF16G, PD, ZS_MAX_WORLD, ACC>(a, stream);
-  }
-  if (a.vec_width == 8) return launch_one<8, BF16G, PD, ZS_MAX_WORLD, ACC>(a, stream);
-  return launch_one<0, BF16G, PD, ZS_MAX_WORLD, ACC>(a, stream);
+  cudaError_t e;
+  // Slice-pointer tables sized to the world (the table is the launch's
+  // parameter block: 128 B, 512 B or 8 KB).
+  if (a.vec_width == 16)
+    e = a.world <= 16   ? launch_one<16, BF16G, PD, 16, ACC>(a, stream)
+        : a.world <= 64 ? launch_one<16, BF16G, PD, 64, ACC>(a, stream)
+                        : launch_one<16, BF16G, PD, ZS_MAX_WORLD, ACC>(a, stream);
+  else if (a.vec_width == 8)
+    e = launch_one<8, BF16G, PD, ZS_MAX_WORLD, ACC>(a, stream);
+  else
+    e = launch_one<0, BF16G, PD, ZS_MAX_WORLD, ACC>(a, stream);
+  if (e == cudaSuccess) note_step_kernel(1, a.vec_width);
+  return e;
 }
 
 // The step with or without the micro-step accumulator, every dtype pair.

@@ -513,8 +513,8 @@ int32_t zs_set_launch_overlap(int32_t on);
  * group (16: 32-byte accesses, 8: 16-byte accesses, 0: element by element);
  * *kernel = 2 for the staged kernel, with *elems = the elements of one tile
  * (2048 or 1024). *kernel = 0 and *elems = 0 before the thread's first launch.
- * A call that launches nothing (an empty range, an error) leaves the record as
- * it was. For tests that must know which code path a call took; the pages
+ * A call that launches nothing (an empty range, an argument error, a launch
+ * that fails) leaves the record as it was. For tests that must know which code path a call took; the pages
  * have no counterpart. ZS_ERR_INVAL for NULL outputs. */
 zs_status zs_last_step_kernel(int32_t* kernel, int32_t* elems);
 /* Failure detection without a fault: enqueues one block that waits, through
