@@ -4,9 +4,9 @@
 // parameter shards so that every rank again holds identical full parameters).
 // A plain multi-source copy: 2 x slot bytes of HBM traffic per copied slot.
 // 32-byte loads and stores where every pointer and the slot size allow (on
-// GB300 0.975 / 0.992 of the measured copy bandwidth on the Llama-7B /
-// Qwen2.5-3B flat buffers, against 0.954 / 0.951 with 16-byte accesses),
-// else 16-byte, else bytes.
+// GB300 they measured 0.975 / 0.992 of the copy bandwidth on the Llama-7B /
+// Qwen2.5-3B flat buffers against 0.954 / 0.951 with 16-byte accesses, both
+// with 8 blocks per SM; the launch shape below), else 16-byte, else bytes.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
