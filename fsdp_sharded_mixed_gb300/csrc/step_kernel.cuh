@@ -750,34 +750,34 @@ bool try_staged(const ShardStepLaunch& a, cudaStream_t stream, cudaError_t* resu
     sh.sms.store(sms, std::memory_order_relaxed);
     sh.per_sm.store(per_sm, std::memory_order_release);
   }
-  // The widest tile (E = 4 or 2 elements per consumer thread) of which two
-  // stages fit.
-  int E = 0, stages = 0, per_sm_blocks = 0;
-  uint32_t stage_bytes = 0;
   // The call's algorithmic bytes against twice the L2 (the launch shape).
   const int64_t call_bytes =
       (a.hi - a.lo) * ((int64_t)a.world * (BF16G ? 2 : 4) + (ACC ? 28 : 24) +
                        (PD == kParamBf16 ? 2 : PD == kParamFp32 ? 4 : 3));
   const bool small = call_bytes < (int64_t(256) << 20);
+  // The widest tile (E = 4 or 2 elements per consumer thread) of which two
+  // stages fit, with at least 8 whole tiles in the range and a slot aligned
+  // for one thread's parameter stores. (4096-element tiles, E = 8, measured
+  // slower on GB300: Llama-7B 0.926 against 1.042, GPT-2-small 0.835 against
+  // 1.001 of the copy bandwidth.)
+  int E = 0, stages = 0, per_sm_blocks = 0;
+  uint32_t stage_bytes = 0;
   for (int e = 4; e >= 2 && E == 0; e /= 2) {
     const uint32_t t = (uint32_t)staged_tile(e);
     const uint32_t sb = (uint32_t)a.world * t * (BF16G ? 2u : 4u) + (ACC ? 4u : 3u) * t * 4u;
     int st = 0, bps = 0;
     staged_shape(sb, sh.per_sm.load(std::memory_order_relaxed),
                  sh.per_block.load(std::memory_order_relaxed), small, &st, &bps);
-    if (st >= 2) {
-      E = e;
-      stages = st;
-      per_sm_blocks = bps;
-      stage_bytes = sb;
-    }
+    if (st < 2 || a.hi / t - (a.lo + t - 1) / t < 8) continue;
+    const uintptr_t slot_align = PD == kParamBf16 ? 2u * e : PD == kParamFp32 ? 4u * e : e;
+    if ((uintptr_t)a.slot % slot_align != 0) continue;
+    E = e;
+    stages = st;
+    per_sm_blocks = bps;
+    stage_bytes = sb;
   }
   if (E == 0) return false;
   const int64_t T = staged_tile(E);
-  if (a.hi / T - (a.lo + T - 1) / T < 8) return false;
-  // Each consumer thread stores its E parameters in one access.
-  const uintptr_t slot_align = PD == kParamBf16 ? 2 * E : PD == kParamFp32 ? 4 * E : E;
-  if ((uintptr_t)a.slot % slot_align != 0) return false;
   // The per-call choice, from GB300 sweeps of both kernels (shard sizes 2^20 ..
   // 2^30 x N in 2..64 x slice and parameter dtypes, CUDA graphs of 20 steps)
   // and the named workloads' step, accumulated and clipped pipelines. The
