@@ -437,3 +437,65 @@ def test_llama_7b_gather_every_element(orc):
     offs = zs.zs_plan_offsets(plan)
     assert [v - views[0] for v in views] == [2 * (o - offs[0]) for o in offs]
     plan.free()
+
+
+def test_llama_7b_resume_into_half_world(orc, tmp_path):
+    """The pages' resume criterion at full size ("从 Data Parallel 到 ZeRO/FSDP",
+    "Checkpoint 不能假设每个 Rank 都有完整模型": verify that the next update
+    equals the uninterrupted run): Llama-7B at N = 8, ranks 0 and 1 take a
+    step and save their fp32 master / m / v (10.1 GB each); rank 0 of the same
+    model at N = 4 restores from those two files. The restored shard is the two
+    old shards back to back, bit for bit; then the next step, with every
+    rank's gradient equal to one bf16 x (its mean is x at any power-of-two
+    world), leaves the restored rank's master, m, v and parameters equal to the
+    uninterrupted ranks' bit for bit."""
+    w = LLAMA_7B
+    pa = zs.zs_flatten_plan(w.numels, w.tied_to, world=8, align_elems=w.align)
+    pb = zs.zs_flatten_plan(w.numels, w.tied_to, world=4, align_elems=w.align)
+    S, Sb, P = pa.S, pb.S, pa.P
+    assert Sb == 2 * S and pa.P_pad == pb.P_pad
+    stream = torch.cuda.current_stream().cuda_stream
+    grads = [torch.empty(S, dtype=torch.int16, device=DEV) for _ in range(8)]
+    full_a = torch.zeros(pa.P_pad, dtype=torch.int16, device=DEV)
+    state, paths = [], []
+    for r in (0, 1):
+        st = (dev_fill(S, bf16=False, index0=r * S, seed=w.seed, stream=synth.STREAM_MASTER,
+                       sigma=w.master_sigma, p_limit=P),
+              torch.zeros(S, dtype=torch.float32, device=DEV),
+              torch.zeros(S, dtype=torch.float32, device=DEV))
+        for j in range(8):
+            synth.fill_device(grads[j].data_ptr(), S, index0=r * S, seed=w.seed, rank=j, step=1,
+                              sigma=w.grad_sigma, p_limit=P, outlier_frac=w.outlier_frac,
+                              outlier_scale=w.outlier_scale, bf16=True, cuda_stream=stream)
+        zs.zs_shard_step(pa, r, 0, S, grads, zs.ZS_BF16, *st, full_a, zs.ZS_BF16, w.hparams, 1)
+        paths.append(str(tmp_path / f"llama7b.rank{r}"))
+        zs.zs_checkpoint_save(pa, r, *st, 1, paths[-1])
+        state.append(st)
+    del grads
+    torch.cuda.empty_cache()
+    restored = [torch.empty(Sb, dtype=torch.float32, device=DEV) for _ in range(3)]
+    assert zs.zs_checkpoint_load(pb, 0, paths + [None] * 6, *restored) == 1
+    for k in range(3):
+        assert torch.equal(restored[k].view(torch.int32),
+                           torch.cat([state[0][k], state[1][k]]).view(torch.int32)), k
+    for p in paths:
+        os.remove(p)
+    # the next update, uninterrupted (N = 8, ranks 0 and 1) and restored (N = 4, rank 0)
+    x = torch.empty(Sb, dtype=torch.int16, device=DEV)
+    synth.fill_device(x.data_ptr(), Sb, seed=77, step=2, sigma=w.grad_sigma, p_limit=P,
+                      bf16=True, cuda_stream=stream)
+    for r in (0, 1):
+        xr = x.narrow(0, r * S, S)
+        zs.zs_shard_step(pa, r, 0, S, [xr] * 8, zs.ZS_BF16, *state[r], full_a, zs.ZS_BF16,
+                         w.hparams, 2)
+    full_b = torch.zeros(pb.P_pad, dtype=torch.int16, device=DEV)
+    zs.zs_shard_step(pb, 0, 0, Sb, [x] * 4, zs.ZS_BF16, *restored, full_b, zs.ZS_BF16,
+                     w.hparams, 2)
+    torch.cuda.synchronize()
+    zs.zs_check_device_error()
+    for k in range(3):
+        assert torch.equal(restored[k].view(torch.int32),
+                           torch.cat([state[0][k], state[1][k]]).view(torch.int32)), k
+    assert torch.equal(full_b[:Sb], full_a[:Sb])
+    pa.free()
+    pb.free()
