@@ -345,6 +345,30 @@ def pin_cast_sampled(o):
             assert g24 == ref24, (hex(int(np.array(x).view(np.uint32))), hex(g24), hex(ref24))
 
 
+def pin_cast_ranges(o):
+    """The range casts (the expected values of the GPU's exhaustive cast test)
+    are the pinned element casts of the patterns first, first + 1, ... (mod
+    2^32), the 3-byte one stored little-endian: windows around every boundary
+    of both formats, random windows, and one that wraps past 0xFFFFFFFF."""
+    rng = np.random.default_rng(5)
+    starts = [0, 0x7F - 40, 0x00800000 - 300, 0x7F7FFF00 - 200, 0x7F800000 - 300,
+              0x7FFFFFFF - 100, 0x80000000 - 20, 0xFF7FFF00, 0xFFFFFFFF - 150]
+    starts += [int(x) for x in rng.integers(0, 1 << 32, size=12)]
+    # windows across bf16 rounding ties (low 16 bits 0x8000), where a pattern
+    # and its neighbour round differently
+    starts += [(int(k) << 16) + 0x8000 - 150 for k in rng.integers(0, 1 << 16, size=6)]
+    n = 400
+    for first in starts:
+        pats = (np.arange(first, first + n, dtype=np.uint64) % (1 << 32)).astype(np.uint32)
+        assert np.array_equal(o.bf16_bits_range(first, n), o.bf16(pats.view(np.float32))), \
+            hex(first)
+        b = o.fp24_bits_range(first, n).reshape(n, 3).astype(np.uint32)
+        packed = b[:, 0] | (b[:, 1] << 8) | (b[:, 2] << 16)
+        for i in range(n):
+            x = pats[i:i + 1].view(np.float32)[0]
+            assert int(packed[i]) == o.fp24(x), hex(int(pats[i]))
+
+
 def pin_param_store(o):
     """The parameter written into the slot is the nearest-even rounding of the
     updated fp32 master: bf16 (2 B), 3-byte (little-endian) or an fp32 copy."""
@@ -1391,6 +1415,7 @@ def pin_reshard_next_update(o, steps=3):
 
 
 ALL_PINS = [
+    pin_cast_ranges,
     pin_sign_law, pin_zero_grad, pin_constant_grad, pin_eps_placement, pin_lr0_wd0,
     pin_fp64_bound, pin_bias_correction_t2, pin_reduce_dyadic, pin_reduce_order,
     pin_reduce_mean, pin_cast_sampled, pin_param_store, pin_plan_bruteforce,

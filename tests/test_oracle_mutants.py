@@ -89,6 +89,17 @@ MUTANTS = [
      "local += rows_per_rank[i] * row_elems[i];", "local += rows_per_rank[i];"),
     ("local padding left uninitialised",
      "std::memset(local, 0, (size_t)S * elem_size);", "(void)0;"),
+    ("3-byte range cast big-endian",
+     "out[3 * i] = (uint8_t)(q & 0xFFu);\n    out[3 * i + 1] = (uint8_t)((q >> 8) & 0xFFu);\n"
+     "    out[3 * i + 2] = (uint8_t)((q >> 16) & 0xFFu);",
+     "out[3 * i + 2] = (uint8_t)(q & 0xFFu);\n    out[3 * i + 1] = (uint8_t)((q >> 8) & 0xFFu);\n"
+     "    out[3 * i] = (uint8_t)((q >> 16) & 0xFFu);"),
+    ("range cast one pattern ahead",
+     "uint32_t q = round_keep_high(bits_float(first + (uint32_t)i), 8);",
+     "uint32_t q = round_keep_high(bits_float(first + (uint32_t)i + 1u), 8);"),
+    ("bf16 range cast one pattern ahead",
+     "out[i] = (uint16_t)round_keep_high(bits_float(first + (uint32_t)i), 16);",
+     "out[i] = (uint16_t)round_keep_high(bits_float(first + (uint32_t)i + 1u), 16);"),
     ("copy-out ignores the rank's row offset",
      "uint8_t* dst = static_cast<uint8_t*>(params[i]) + (size_t)r * rows_per_rank[i] * row_bytes;",
      "uint8_t* dst = static_cast<uint8_t*>(params[i]) + (size_t)r * row_bytes;"),
